@@ -1,0 +1,193 @@
+"""Python binding of libforge.so, the fused weight-gradient + optimizer-step library.
+
+The binding only marshals arguments: every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.  If the
+library has not been built, every call raises ``ForgeUnavailable``: there is no
+fallback path.
+
+Entry points (same names as the C ABI in include/forge.h):
+  fused_dw_step(dY, X, W, m, v, qscales, opt, hp, step, seed, stream=None)
+  dw_gemm(dY, X, dW, stream=None)
+  opt_step(dW, W, m, v, qscales, opt, hp, step, seed, stream=None)
+  sync_status(stream=None), set_wait_limit_ns(ns), launch_count()
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Any, Optional
+
+__all__ = [
+    "OPT_KINDS", "STATE_FP32", "STATE_INT8_B64", "ForgeError", "ForgeUnavailable", "lib", "library_path",
+    "fused_dw_step", "dw_gemm", "opt_step", "sync_status", "set_wait_limit_ns", "launch_count", "build",
+    "ForgeShape", "ForgeHparams", "hparams_struct",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libforge.so")
+
+OPT_KINDS = {"adamw": 0, "nadam": 1, "radam": 2, "lion": 3, "rmsprop": 4, "adagrad": 5, "sgd": 6,
+             "sgd_momentum": 7}
+STATE_FP32 = 0
+STATE_INT8_B64 = 1
+STATUS = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARGUMENT", 2: "FORGE_ERR_UNSUPPORTED", 3: "FORGE_ERR_MISALIGNED",
+          4: "FORGE_ERR_CUDA", 5: "FORGE_ERR_NOT_SM103", 6: "FORGE_ERR_TIMEOUT"}
+
+
+class ForgeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+class ForgeUnavailable(RuntimeError):
+    pass
+
+
+class ForgeShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d_out", ctypes.c_int64), ("d_in", ctypes.c_int64),
+                ("state", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class ForgeHparams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in
+                ("lr", "beta1", "beta2", "eps", "weight_decay", "momentum", "alpha", "momentum_decay", "lr_decay")]
+
+
+_HP_DEFAULTS = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, momentum=0.9, alpha=0.99,
+                    momentum_decay=4e-3, lr_decay=0.0)
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    """Compile libforge.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library, with argument types declared."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ForgeUnavailable(f"{_LIB_PATH} is not built; run backward_optimizer_gb300.build() first")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i64, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64
+    L.forge_fused_dw_step.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.POINTER(ForgeHparams),
+                                      ctypes.POINTER(ForgeShape), i64, u64, vp]
+    L.forge_fused_dw_step.restype = ctypes.c_int
+    L.forge_dw_gemm.argtypes = [vp, vp, vp, ctypes.POINTER(ForgeShape), vp]
+    L.forge_dw_gemm.restype = ctypes.c_int
+    L.forge_opt_step.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.POINTER(ForgeHparams),
+                                 ctypes.POINTER(ForgeShape), i64, u64, vp]
+    L.forge_opt_step.restype = ctypes.c_int
+    L.forge_sync_status.argtypes = [vp]
+    L.forge_sync_status.restype = ctypes.c_int
+    L.forge_set_wait_limit_ns.argtypes = [u64]
+    L.forge_set_wait_limit_ns.restype = None
+    L.forge_launch_count.argtypes = []
+    L.forge_launch_count.restype = u64
+    L.forge_status_string.argtypes = [ctypes.c_int]
+    L.forge_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def hparams_struct(hp: Any = None, **overrides) -> ForgeHparams:
+    """A ForgeHparams from an object with the nine fields, a dict, or defaults + overrides."""
+    vals = dict(_HP_DEFAULTS)
+    if hp is not None:
+        for k in _HP_DEFAULTS:
+            if isinstance(hp, dict):
+                if k in hp:
+                    vals[k] = hp[k]
+            elif hasattr(hp, k):
+                vals[k] = getattr(hp, k)
+    vals.update(overrides)
+    return ForgeHparams(**{k: float(v) for k, v in vals.items()})
+
+
+# ------------------------------------------------------------------ torch-facing wrappers
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous (row-major)")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise ForgeError(status, what)
+
+
+def _shape(T: int, d_out: int, d_in: int, state: int) -> ForgeShape:
+    return ForgeShape(T=int(T), d_out=int(d_out), d_in=int(d_in), state=int(state), reserved=0)
+
+
+def _state_of(m, v) -> int:
+    import torch
+    for t in (m, v):
+        if t is not None:
+            return STATE_INT8_B64 if t.dtype == torch.int8 else STATE_FP32
+    return STATE_FP32
+
+
+def fused_dw_step(dY, X, W, m=None, v=None, qscales=None, opt: str = "adamw", hp: Any = None, step: int = 1,
+                  seed: int = 0, stream=None) -> None:
+    """One fused step on torch tensors: dY [T, d_out] bf16, X [T, d_in] bf16, W [d_out, d_in] bf16,
+    m/v FP32 or int8 [d_out, d_in], qscales FP32 [2 * d_out * d_in / 64] for int8 states."""
+    T, d_out = dY.shape
+    d_in = X.shape[1]
+    shape = _shape(T, d_out, d_in, _state_of(m, v))
+    st = lib().forge_fused_dw_step(_ptr(dY), _ptr(X), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), OPT_KINDS[opt],
+                                   ctypes.byref(hparams_struct(hp)), ctypes.byref(shape), int(step),
+                                   int(seed) & (2**64 - 1), _stream(stream))
+    _check(st, "forge_fused_dw_step")
+
+
+def dw_gemm(dY, X, dW, stream=None) -> None:
+    """dW [d_out, d_in] FP32 = dY^T X (the unfused baseline's gradient pass)."""
+    T, d_out = dY.shape
+    shape = _shape(T, d_out, X.shape[1], STATE_FP32)
+    _check(lib().forge_dw_gemm(_ptr(dY), _ptr(X), _ptr(dW), ctypes.byref(shape), _stream(stream)), "forge_dw_gemm")
+
+
+def opt_step(dW, W, m=None, v=None, qscales=None, opt: str = "adamw", hp: Any = None, step: int = 1, seed: int = 0,
+             stream=None) -> None:
+    """The unfused baseline's optimizer pass over a materialised FP32 gradient (None = zero gradient)."""
+    d_out, d_in = W.shape
+    shape = _shape(0, d_out, d_in, _state_of(m, v))
+    st = lib().forge_opt_step(_ptr(dW), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), OPT_KINDS[opt],
+                              ctypes.byref(hparams_struct(hp)), ctypes.byref(shape), int(step),
+                              int(seed) & (2**64 - 1), _stream(stream))
+    _check(st, "forge_opt_step")
+
+
+def sync_status(stream=None) -> int:
+    """Wait for the stream; return the device status (0, or 6 = a bounded wait ran out)."""
+    return int(lib().forge_sync_status(_stream(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib().forge_set_wait_limit_ns(int(ns))
+
+
+def launch_count() -> int:
+    return int(lib().forge_launch_count())

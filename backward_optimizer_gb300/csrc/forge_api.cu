@@ -1,0 +1,376 @@
+// forge_api.cu -- the C ABI (include/forge.h): argument checks, step-dependent scalars,
+// TMA descriptors, grid sizing and kernel dispatch.  Host code only, apart from the device
+// status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/forge.h"
+#include "launch.h"
+#include "opt_step_kernel.cuh"
+#include "tile_kernel.cuh"
+
+// Device status word: 0, or the forge_status of the first bounded wait that ran out.
+__device__ int g_forge_status_word;
+
+namespace {
+
+using forge::OptScalars;
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<uint64_t> g_launches{0};
+
+struct DeviceInfo {
+    bool ready = false;
+    bool sm103 = false;
+    int num_sms = 0;
+    int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+forge_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FORGE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FORGE_ERR_CUDA;
+        d.sm103 = (major == 10 && minor == 3);
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_forge_status_word) != cudaSuccess) return FORGE_ERR_CUDA;
+        d.status = static_cast<int*>(p);
+        if (g_encode == nullptr) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return FORGE_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    if (!d.sm103) return FORGE_ERR_NOT_SM103;
+    *out = &d;
+    return FORGE_OK;
+}
+
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+bool uses_m(forge_opt_kind k) {
+    return k == FORGE_ADAMW || k == FORGE_NADAM || k == FORGE_RADAM || k == FORGE_LION || k == FORGE_SGD_MOMENTUM;
+}
+bool uses_v(forge_opt_kind k) {
+    return k == FORGE_ADAMW || k == FORGE_NADAM || k == FORGE_RADAM || k == FORGE_RMSPROP || k == FORGE_ADAGRAD;
+}
+
+// Step-dependent factors in binary64, rounded once to binary32 (optimizer definitions as cited
+// in opt_math.cuh).
+OptScalars derive_scalars(forge_opt_kind k, const forge_hparams& hp, int64_t step) {
+    const double t = static_cast<double>(step);
+    const double lr = hp.lr, b1 = hp.beta1, b2 = hp.beta2, eps = hp.eps, wd = hp.weight_decay;
+    OptScalars s;
+    std::memset(&s, 0, sizeof(s));
+    s.lr = static_cast<float>(lr);
+    s.eps = static_cast<float>(eps);
+    s.wd = static_cast<float>(wd);
+    s.decay = static_cast<float>(1.0 - lr * wd);
+    s.b1 = static_cast<float>(b1);
+    s.omb1 = static_cast<float>(1.0 - b1);
+    s.b2 = static_cast<float>(b2);
+    s.omb2 = static_cast<float>(1.0 - b2);
+    const double bc1 = 1.0 - std::pow(b1, t), bc2 = 1.0 - std::pow(b2, t);
+    switch (k) {
+        case FORGE_ADAMW:
+            s.step_size = static_cast<float>(lr / bc1);
+            s.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+            break;
+        case FORGE_NADAM: {
+            const double psi = hp.momentum_decay;
+            auto mu = [&](double i) { return b1 * (1.0 - 0.5 * std::pow(0.96, i * psi)); };
+            double prod = 1.0;
+            for (int64_t i = 1; i <= step; ++i) prod *= mu(static_cast<double>(i));
+            const double mu_t = mu(t), mu_next = mu(t + 1.0);
+            s.c_g = static_cast<float>(lr * (1.0 - mu_t) / (1.0 - prod));
+            s.c_m = static_cast<float>(lr * mu_next / (1.0 - prod * mu_next));
+            s.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+            break;
+        }
+        case FORGE_RADAM: {
+            const double rho_inf = 2.0 / (1.0 - b2) - 1.0;
+            const double rho_t = rho_inf - 2.0 * t * std::pow(b2, t) / bc2;
+            if (rho_t > 5.0) {
+                const double r = std::sqrt((rho_t - 4.0) * (rho_t - 2.0) * rho_inf /
+                                           ((rho_inf - 4.0) * (rho_inf - 2.0) * rho_t));
+                s.rectified = 1;
+                s.step_size = static_cast<float>(lr * r * std::sqrt(bc2) / bc1);
+            } else {
+                s.rectified = 0;
+                s.step_size = static_cast<float>(lr / bc1);
+            }
+            break;
+        }
+        case FORGE_LION:
+            break;
+        case FORGE_RMSPROP:
+            s.b2 = hp.alpha;
+            s.omb2 = static_cast<float>(1.0 - static_cast<double>(hp.alpha));
+            break;
+        case FORGE_ADAGRAD:
+            s.lr = static_cast<float>(lr / (1.0 + (t - 1.0) * static_cast<double>(hp.lr_decay)));
+            break;
+        case FORGE_SGD:
+            break;
+        case FORGE_SGD_MOMENTUM:
+            s.mu = hp.momentum;
+            break;
+    }
+    return s;
+}
+
+forge_status make_operand_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows) {
+    // A [rows, cols] bf16 row-major operand, read in boxes of 64 columns x 64 rows with the
+    // 128-byte swizzle (each box row is exactly one 128-byte swizzle span).
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(forge::kBK)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_CUDA;
+}
+
+forge_status check_shape(const forge_shape* shape, bool need_T) {
+    if (shape == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    if (shape->d_out < 0 || shape->d_in < 0 || shape->T < 0 || shape->reserved != 0) return FORGE_ERR_INVALID_ARGUMENT;
+    if (shape->d_out % 128 != 0 || shape->d_in % 128 != 0) return FORGE_ERR_INVALID_ARGUMENT;
+    if (need_T && shape->T % forge::kBK != 0) return FORGE_ERR_INVALID_ARGUMENT;
+    // TMA coordinates are 32-bit; the tile scheduler counts tiles in int.
+    if (shape->d_out > (1ll << 30) || shape->d_in > (1ll << 30) || shape->T > (1ll << 30))
+        return FORGE_ERR_INVALID_ARGUMENT;
+    if ((shape->d_out / 128) * (shape->d_in / 128) > (1ll << 30)) return FORGE_ERR_INVALID_ARGUMENT;
+    if (shape->state != FORGE_STATE_FP32 && shape->state != FORGE_STATE_INT8_B64) return FORGE_ERR_INVALID_ARGUMENT;
+    return FORGE_OK;
+}
+
+forge_status check_opt_args(const void* W, const void* m, const void* v, const float* qscales, forge_opt_kind k,
+                            const forge_hparams* hp, const forge_shape* shape, int64_t step) {
+    if (static_cast<int>(k) < 0 || static_cast<int>(k) > 7 || hp == nullptr || step < 1)
+        return FORGE_ERR_INVALID_ARGUMENT;
+    if (W == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    if (uses_m(k) && m == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    if (uses_v(k) && v == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    const bool int8 = shape->state == FORGE_STATE_INT8_B64;
+    if (int8 && k == FORGE_SGD) return FORGE_ERR_UNSUPPORTED;
+    if (int8 && qscales == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    if (!aligned32(W) || (uses_m(k) && !aligned32(m)) || (uses_v(k) && !aligned32(v)) ||
+        (int8 && (reinterpret_cast<uintptr_t>(qscales) & 3u)))
+        return FORGE_ERR_MISALIGNED;
+    return FORGE_OK;
+}
+
+forge_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA; }
+
+// Dispatch tables (filled by template instantiation in the inst_*.cu units).
+using TileFn = cudaError_t (*)(const forge::TileLaunch&);
+using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
+
+TileFn tile_fn(forge_opt_kind k, bool int8) {
+    using namespace forge;
+    switch (k) {
+        case FORGE_ADAMW: return int8 ? launch_tile<kAdamW, kEpiOptINT8> : launch_tile<kAdamW, kEpiOptFP32>;
+        case FORGE_NADAM: return int8 ? launch_tile<kNAdam, kEpiOptINT8> : launch_tile<kNAdam, kEpiOptFP32>;
+        case FORGE_RADAM: return int8 ? launch_tile<kRAdam, kEpiOptINT8> : launch_tile<kRAdam, kEpiOptFP32>;
+        case FORGE_LION: return int8 ? launch_tile<kLion, kEpiOptINT8> : launch_tile<kLion, kEpiOptFP32>;
+        case FORGE_RMSPROP: return int8 ? launch_tile<kRMSprop, kEpiOptINT8> : launch_tile<kRMSprop, kEpiOptFP32>;
+        case FORGE_ADAGRAD: return int8 ? launch_tile<kAdaGrad, kEpiOptINT8> : launch_tile<kAdaGrad, kEpiOptFP32>;
+        case FORGE_SGD: return int8 ? nullptr : launch_tile<kSGD, kEpiOptFP32>;
+        case FORGE_SGD_MOMENTUM:
+            return int8 ? launch_tile<kSGDMomentum, kEpiOptINT8> : launch_tile<kSGDMomentum, kEpiOptFP32>;
+    }
+    return nullptr;
+}
+
+OptFn opt_fn(forge_opt_kind k, bool int8) {
+    using namespace forge;
+    switch (k) {
+        case FORGE_ADAMW: return int8 ? launch_opt<kAdamW, true> : launch_opt<kAdamW, false>;
+        case FORGE_NADAM: return int8 ? launch_opt<kNAdam, true> : launch_opt<kNAdam, false>;
+        case FORGE_RADAM: return int8 ? launch_opt<kRAdam, true> : launch_opt<kRAdam, false>;
+        case FORGE_LION: return int8 ? launch_opt<kLion, true> : launch_opt<kLion, false>;
+        case FORGE_RMSPROP: return int8 ? launch_opt<kRMSprop, true> : launch_opt<kRMSprop, false>;
+        case FORGE_ADAGRAD: return int8 ? launch_opt<kAdaGrad, true> : launch_opt<kAdaGrad, false>;
+        case FORGE_SGD: return int8 ? nullptr : launch_opt<kSGD, false>;
+        case FORGE_SGD_MOMENTUM: return int8 ? launch_opt<kSGDMomentum, true> : launch_opt<kSGDMomentum, false>;
+    }
+    return nullptr;
+}
+
+forge_status run_opt(const float* dW, void* W, void* m, void* v, float* qscales, forge_opt_kind k,
+                     const forge_hparams* hp, const forge_shape* shape, int64_t step, uint64_t seed,
+                     cudaStream_t stream, const DeviceInfo& dev) {
+    const bool int8 = shape->state == FORGE_STATE_INT8_B64;
+    const uint64_t n = static_cast<uint64_t>(shape->d_out) * static_cast<uint64_t>(shape->d_in);
+    forge::OptArgs a;
+    a.dW = dW;
+    a.W = static_cast<uint16_t*>(W);
+    a.m = m;
+    a.v = v;
+    a.m_scales = int8 ? qscales : nullptr;
+    a.v_scales = int8 ? qscales + n / 64 : nullptr;
+    a.n8 = n / 8;
+    a.s = derive_scalars(k, *hp, step);
+    a.seed = seed;
+    a.step = static_cast<uint64_t>(step);
+    const uint64_t blocks = (a.n8 + 255) / 256;
+    const uint64_t cap = static_cast<uint64_t>(dev.num_sms) * 8;
+    const int grid = static_cast<int>(blocks < cap ? blocks : cap);
+    OptFn fn = opt_fn(k, int8);
+    if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
+    g_launches.fetch_add(1);
+    return cuda_status(fn(a, grid, stream));
+}
+
+forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m, void* v, float* qscales,
+                      forge_opt_kind k, int epi, const forge_hparams* hp, const forge_shape* shape, int64_t step,
+                      uint64_t seed, cudaStream_t stream, const DeviceInfo& dev) {
+    const bool int8 = shape->state == FORGE_STATE_INT8_B64;
+    const uint64_t n = static_cast<uint64_t>(shape->d_out) * static_cast<uint64_t>(shape->d_in);
+    forge::TileArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.d_out = static_cast<int>(shape->d_out);
+    a.d_in = static_cast<int>(shape->d_in);
+    a.T = static_cast<int>(shape->T);
+    a.tiles_m = a.d_out / forge::kBM;
+    a.tiles_n = a.d_in / forge::kTileBN;
+    a.num_tiles = a.tiles_m * a.tiles_n;
+    // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
+    a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
+    a.dW = dW;
+    a.W = static_cast<uint16_t*>(W);
+    a.m = m;
+    a.v = v;
+    a.m_scales = int8 ? qscales : nullptr;
+    a.v_scales = int8 ? qscales + n / 64 : nullptr;
+    if (hp != nullptr) a.s = derive_scalars(k, *hp, step);
+    a.seed = seed;
+    a.step = static_cast<uint64_t>(step);
+    a.status = dev.status;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+
+    forge::TileLaunch l;
+    forge_status st = make_operand_map(&l.tmap_dy, dY, shape->d_out, shape->T);
+    if (st != FORGE_OK) return st;
+    st = make_operand_map(&l.tmap_x, X, shape->d_in, shape->T);
+    if (st != FORGE_OK) return st;
+    l.args = &a;
+    l.grid = a.num_tiles < dev.num_sms ? a.num_tiles : dev.num_sms;
+    l.stream = stream;
+    TileFn fn = (epi == forge::kEpiStoreGrad) ? forge::launch_tile<0, forge::kEpiStoreGrad> : tile_fn(k, int8);
+    if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
+    g_launches.fetch_add(1);
+    return cuda_status(fn(l));
+}
+
+}  // namespace
+
+extern "C" {
+
+forge_status forge_fused_dw_step(const void* dY, const void* X, void* W, void* m, void* v, float* qscales,
+                                 forge_opt_kind opt_kind, const forge_hparams* hp, const forge_shape* shape,
+                                 int64_t step, uint64_t seed, struct CUstream_st* stream) {
+    forge_status st = check_shape(shape, true);
+    if (st != FORGE_OK) return st;
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;  // empty layer: nothing to read or write
+    st = check_opt_args(W, m, v, qscales, opt_kind, hp, shape, step);
+    if (st != FORGE_OK) return st;
+    if (shape->T > 0 && (dY == nullptr || X == nullptr)) return FORGE_ERR_INVALID_ARGUMENT;
+    if (shape->T > 0 && (!aligned32(dY) || !aligned32(X))) return FORGE_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    if (shape->T == 0)  // no tokens: the gradient is exactly zero
+        return run_opt(nullptr, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream, *dev);
+    return run_tile(dY, X, nullptr, W, m, v, qscales, opt_kind, forge::kEpiOptFP32, hp, shape, step, seed, stream,
+                    *dev);
+}
+
+forge_status forge_dw_gemm(const void* dY, const void* X, float* dW, const forge_shape* shape,
+                           struct CUstream_st* stream) {
+    forge_status st = check_shape(shape, true);
+    if (st != FORGE_OK) return st;
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
+    if (dW == nullptr || (shape->T > 0 && (dY == nullptr || X == nullptr))) return FORGE_ERR_INVALID_ARGUMENT;
+    if (!aligned32(dW) || (shape->T > 0 && (!aligned32(dY) || !aligned32(X)))) return FORGE_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    if (shape->T == 0)
+        return cuda_status(cudaMemsetAsync(dW, 0, static_cast<size_t>(shape->d_out) * shape->d_in * sizeof(float),
+                                           stream));
+    return run_tile(dY, X, dW, nullptr, nullptr, nullptr, nullptr, FORGE_SGD, forge::kEpiStoreGrad, nullptr, shape,
+                    1, 0, stream, *dev);
+}
+
+forge_status forge_opt_step(const float* dW, void* W, void* m, void* v, float* qscales, forge_opt_kind opt_kind,
+                            const forge_hparams* hp, const forge_shape* shape, int64_t step, uint64_t seed,
+                            struct CUstream_st* stream) {
+    forge_status st = check_shape(shape, false);
+    if (st != FORGE_OK) return st;
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
+    st = check_opt_args(W, m, v, qscales, opt_kind, hp, shape, step);
+    if (st != FORGE_OK) return st;
+    if (dW != nullptr && !aligned32(dW)) return FORGE_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    return run_opt(dW, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream, *dev);
+}
+
+forge_status forge_sync_status(struct CUstream_st* stream) {
+    DeviceInfo* dev = nullptr;
+    forge_status st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FORGE_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FORGE_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FORGE_ERR_CUDA;
+        return static_cast<forge_status>(word);
+    }
+    return FORGE_OK;
+}
+
+void forge_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns < 1000000ull ? 1000000ull : ns); }
+
+uint64_t forge_launch_count(void) { return g_launches.load(); }
+
+const char* forge_status_string(forge_status s) {
+    switch (s) {
+        case FORGE_OK: return "ok";
+        case FORGE_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case FORGE_ERR_UNSUPPORTED: return "unsupported combination";
+        case FORGE_ERR_MISALIGNED: return "pointer not 32-byte aligned";
+        case FORGE_ERR_CUDA: return "CUDA error";
+        case FORGE_ERR_NOT_SM103: return "device is not compute capability 10.3 (sm_103a)";
+        case FORGE_ERR_TIMEOUT: return "a bounded on-device wait ran out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

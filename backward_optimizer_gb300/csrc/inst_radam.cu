@@ -1,0 +1,4 @@
+// Kernel instantiations for one optimizer (radam).
+#include "instantiate.cuh"
+FORGE_INSTANTIATE_OPT(forge::kRAdam)
+FORGE_INSTANTIATE_OPT_INT8(forge::kRAdam)

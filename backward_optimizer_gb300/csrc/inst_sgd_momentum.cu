@@ -1,0 +1,4 @@
+// Kernel instantiations for one optimizer (sgd_momentum).
+#include "instantiate.cuh"
+FORGE_INSTANTIATE_OPT(forge::kSGDMomentum)
+FORGE_INSTANTIATE_OPT_INT8(forge::kSGDMomentum)

@@ -1,0 +1,435 @@
+// tile_kernel.cuh -- the persistent weight-gradient tile kernel for sm_103a.
+//
+// FORGE ("FORGE: Fused On-Register Gradient Elimination for Memory-Efficient LLM Training",
+// gist.science technical summary), §2 Methodology, Core mechanism: for one weight tile,
+// (1) accumulate dY^T X over all tokens in FP32 on chip, (2) apply the optimizer to the
+// finished tile on chip, (3) discard the gradient tile, (4) write back only the weight and
+// moment tiles.
+//
+// GB300 mapping of that mechanism:
+//   warp 0      TMA producer: 128 x 64-token slices of dY and BN x 64-token slices of X into a
+//               shared-memory ring (128-byte swizzle, both operands MN-major as stored).
+//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> f32), M = 128, N = BN, K = 16,
+//               accumulating the whole tile in TMEM (step 1 happens in TMEM, not registers).
+//               TMEM holds two accumulators so the next tile's mainloop overlaps this tile's
+//               epilogue.
+//   warps 2-9   epilogue: tcgen05.ld moves a 32-column strip of the finished tile into
+//               registers (thread = weight row); the optimizer runs in registers (step 2); the
+//               gradient registers are then dropped (step 3); W/m/v are read and written with
+//               256-bit accesses (step 4).  The gradient never reaches device memory.
+// Tiles are visited by a static persistent schedule (tile = blockIdx.x + k * gridDim.x) in
+// grouped order so that concurrently running CTAs share dY and X slices in L2.
+//
+// Every wait is bounded in time: on expiry the kernel records FORGE_ERR_TIMEOUT in the device
+// status word, raises a CTA-wide abort flag that every other wait observes, waits (bounded)
+// for its own copies and MMAs in flight, frees TMEM and returns.
+#pragma once
+
+#include <cstdint>
+
+#include "opt_math.cuh"
+#include "ptx.cuh"
+
+namespace forge {
+
+constexpr int kBM = 128;         // tile rows (d_out) = TMEM lanes
+constexpr int kBK = 64;          // tokens per pipeline stage = 128 bytes of one operand column
+constexpr int kUmmaK = 16;       // K of one kind::f16 MMA
+constexpr int kNumEpiWarps = 8;  // two warps per TMEM lane quarter, each owning half the columns
+constexpr int kThreads = 64 + 32 * kNumEpiWarps;
+constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
+constexpr int kTileBN = 128;     // tile columns (d_in) of the compiled kernels: the 128 x 128 tile
+
+enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2 };
+
+template <int BN>
+struct TileCfg {
+    static_assert(BN == 128 || BN == 256, "tile width");
+    static constexpr int kStages = BN == 128 ? 6 : 4;
+    static constexpr int kABytes = kBM * kBK * 2;  // one stage of dY^T: 2 boxes of [64 tokens][64 rows]
+    static constexpr int kBBytes = BN * kBK * 2;   // one stage of X: BN/64 boxes of [64 tokens][64 cols]
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator
+    static constexpr int kBarrierBytes = 256;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+struct TileArgs {
+    int d_out, d_in, T;
+    int tiles_m, tiles_n, num_tiles, group_m;
+    float* dW;                    // kEpiStoreGrad: [d_out, d_in] FP32
+    uint16_t* W;                  // bf16 [d_out, d_in]
+    void* m;                      // FP32 or int8 [d_out, d_in]
+    void* v;
+    float* m_scales;              // INT8: [d_out, d_in/64]
+    float* v_scales;
+    OptScalars s;
+    uint64_t seed, step;
+    int* status;                  // device status word
+    uint64_t wait_limit_ns;
+};
+
+// ---------------------------------------------------------------- bounded waits
+
+struct AbortCtx {
+    volatile int* flag;
+    int* status;
+    uint64_t limit_ns;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const AbortCtx& ab) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*ab.flag) return false;
+        if ((n & 15u) == 0 && global_timer_ns() - t0 > ab.limit_ns) {
+            *ab.flag = 1;
+            atomicCAS(ab.status, 0, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// Used only after an abort, to let this thread's own asynchronous work land before exit.
+__device__ __forceinline__ void drain_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return;
+    }
+}
+
+__device__ __forceinline__ void tile_coords(int tile, const TileArgs& a, int& mb, int& nb) {
+    const int per_group = a.group_m * a.tiles_n;
+    const int group = tile / per_group;
+    const int first_m = group * a.group_m;
+    const int gm = min(a.tiles_m - first_m, a.group_m);
+    const int in_group = tile - group * per_group;
+    mb = first_m + in_group % gm;
+    nb = in_group / gm;
+}
+
+// ---------------------------------------------------------------- epilogues
+// Each is called by one warp for one tile: `row` is this thread's weight row, `col0` the first
+// weight column of the warp's strip, `taddr` the TMEM address of (its lane quarter, col0).
+
+__device__ __forceinline__ void st_v8_f32(float* p, const uint32_t* r) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+template <int WIDTH>
+__device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row, int col0, uint32_t taddr) {
+    float* dst = a.dW + static_cast<size_t>(row) * a.d_in + col0;
+#pragma unroll 1
+    for (int c = 0; c < WIDTH; c += 32) {
+        uint32_t g[32];
+        tmem_ld_32x32b_x32(taddr + c, g);
+        tmem_ld_wait(g);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_v8_f32(dst + c + 8 * q, &g[8 * q]);
+    }
+}
+
+template <int OPT, int WIDTH>
+__device__ __forceinline__ void epi_opt_fp32(const TileArgs& a, int row, int col0, uint32_t taddr) {
+    using Tr = OptTraits<OPT>;
+    const size_t row_base = static_cast<size_t>(row) * a.d_in + col0;
+    float* mp = static_cast<float*>(a.m);
+    float* vp = static_cast<float*>(a.v);
+#pragma unroll 1
+    for (int c = 0; c < WIDTH; c += 32) {
+        const size_t e0 = row_base + c;
+        uint32_t w[16], m[32], v[32];
+        ld_cs_v8(a.W + e0, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
+        ld_cs_v8(a.W + e0 + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
+        if constexpr (Tr::kM) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ld_cs_v8(mp + e0 + 8 * q, *reinterpret_cast<uint32_t(*)[8]>(&m[8 * q]));
+        }
+        if constexpr (Tr::kV) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ld_cs_v8(vp + e0 + 8 * q, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * q]));
+        }
+        uint32_t g[32];
+        tmem_ld_32x32b_x32(taddr + c, g);
+        tmem_ld_wait(g);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const Philox4 p = sr_words((e0 >> 3) + q, a.seed, a.step);
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                const int i = 8 * q + j;
+                const uint32_t wp = w[i >> 1];
+                float m0 = Tr::kM ? __uint_as_float(m[i]) : 0.f, m1 = Tr::kM ? __uint_as_float(m[i + 1]) : 0.f;
+                float v0 = Tr::kV ? __uint_as_float(v[i]) : 0.f, v1 = Tr::kV ? __uint_as_float(v[i + 1]) : 0.f;
+                const float w0 = opt_update<OPT>(__uint_as_float(g[i]), bf16_lo(wp), m0, v0, a.s);
+                const float w1 = opt_update<OPT>(__uint_as_float(g[i + 1]), bf16_hi(wp), m1, v1, a.s);
+                w[i >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
+                if constexpr (Tr::kM) { m[i] = __float_as_uint(m0); m[i + 1] = __float_as_uint(m1); }
+                if constexpr (Tr::kV) { v[i] = __float_as_uint(v0); v[i + 1] = __float_as_uint(v1); }
+            }
+        }
+        st_cs_v8(a.W + e0, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
+        st_cs_v8(a.W + e0 + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
+        if constexpr (Tr::kM) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_cs_v8(mp + e0 + 8 * q, *reinterpret_cast<uint32_t(*)[8]>(&m[8 * q]));
+        }
+        if constexpr (Tr::kV) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_cs_v8(vp + e0 + 8 * q, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * q]));
+        }
+    }
+}
+
+// INT8 moments: one 64-column block per step, entirely in this thread's row, so the block's
+// absmax needs no cross-thread reduction.  Pass 1 computes the new moments and their absmax;
+// pass 2 reloads the gradient from TMEM, recomputes the same moments bit for bit, updates the
+// weight with the unquantised moments and writes the codes under the new scales.
+template <int OPT, int WIDTH>
+__device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row, int col0, uint32_t taddr) {
+    using Tr = OptTraits<OPT>;
+    const size_t row_base = static_cast<size_t>(row) * a.d_in + col0;
+    int8_t* mp = static_cast<int8_t*>(a.m);
+    int8_t* vp = static_cast<int8_t*>(a.v);
+#pragma unroll 1
+    for (int c = 0; c < WIDTH; c += 64) {
+        const size_t e0 = row_base + c;
+        const size_t blk = e0 >> 6;
+        uint32_t w[32], mq[16], vq[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ld_cs_v8(a.W + e0 + 16 * q, *reinterpret_cast<uint32_t(*)[8]>(&w[8 * q]));
+        float ms = 0.f, vs = 0.f;
+        if constexpr (Tr::kM) {
+            ld_cs_v8(mp + e0, *reinterpret_cast<uint32_t(*)[8]>(&mq[0]));
+            ld_cs_v8(mp + e0 + 32, *reinterpret_cast<uint32_t(*)[8]>(&mq[8]));
+            ms = a.m_scales[blk];
+        }
+        if constexpr (Tr::kV) {
+            ld_cs_v8(vp + e0, *reinterpret_cast<uint32_t(*)[8]>(&vq[0]));
+            ld_cs_v8(vp + e0 + 32, *reinterpret_cast<uint32_t(*)[8]>(&vq[8]));
+            vs = a.v_scales[blk];
+        }
+        // pass 1: absmax of the new moments
+        float am = 0.f, av = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t g[32];
+            tmem_ld_32x32b_x32(taddr + c + 32 * h, g);
+            tmem_ld_wait(g);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int i = 32 * h + j;
+                const float wf = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+                float mm = Tr::kM ? __fmul_rn(int8_at(mq[i >> 2], i & 3), ms) : 0.f;
+                float vv = Tr::kV ? __fmul_rn(int8_at(vq[i >> 2], i & 3), vs) : 0.f;
+                opt_moments<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
+                am = fmaxf(am, fabsf(mm));
+                av = fmaxf(av, fabsf(vv));
+            }
+        }
+        const float nms = __fdiv_rn(am, 127.0f), nvs = __fdiv_rn(av, 127.0f);
+        // pass 2: update, round, requantise
+        uint32_t mo[16], vo[16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t g[32];
+            tmem_ld_32x32b_x32(taddr + c + 32 * h, g);
+            tmem_ld_wait(g);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const Philox4 p = sr_words((e0 >> 3) + 4 * h + q, a.seed, a.step);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int i = 32 * h + 8 * q + j;
+                    const float wf = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
+                    float mm = Tr::kM ? __fmul_rn(int8_at(mq[i >> 2], i & 3), ms) : 0.f;
+                    float vv = Tr::kV ? __fmul_rn(int8_at(vq[i >> 2], i & 3), vs) : 0.f;
+                    const float wn = opt_update<OPT>(__uint_as_float(g[8 * q + j]), wf, mm, vv, a.s);
+                    const uint32_t b = sr_bf16(wn, sr_r16(p, j));
+                    w[i >> 1] = (i & 1) ? ((w[i >> 1] & 0xFFFFu) | (b << 16)) : ((w[i >> 1] & 0xFFFF0000u) | b);
+                    const uint32_t cm = Tr::kM ? int8_code(mm, nms) : 0u;
+                    const uint32_t cv = Tr::kV ? int8_code(vv, nvs) : 0u;
+                    if ((i & 3) == 0) { mo[i >> 2] = cm; vo[i >> 2] = cv; }
+                    else { mo[i >> 2] |= cm << (8 * (i & 3)); vo[i >> 2] |= cv << (8 * (i & 3)); }
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_cs_v8(a.W + e0 + 16 * q, *reinterpret_cast<uint32_t(*)[8]>(&w[8 * q]));
+        if constexpr (Tr::kM) {
+            st_cs_v8(mp + e0, *reinterpret_cast<uint32_t(*)[8]>(&mo[0]));
+            st_cs_v8(mp + e0 + 32, *reinterpret_cast<uint32_t(*)[8]>(&mo[8]));
+            a.m_scales[blk] = nms;
+        }
+        if constexpr (Tr::kV) {
+            st_cs_v8(vp + e0, *reinterpret_cast<uint32_t(*)[8]>(&vo[0]));
+            st_cs_v8(vp + e0 + 32, *reinterpret_cast<uint32_t(*)[8]>(&vo[8]));
+            a.v_scales[blk] = nvs;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int BN, int EPI, int OPT>
+__global__ void __launch_bounds__(kThreads, 1)
+    forge_tile_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
+                      const TileArgs a) {
+    using C = TileCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 128B-swizzle atoms need 1024B alignment
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + C::kStages * C::kABytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* acc_full = empty + C::kStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], kNumEpiWarps);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_dy);
+        tma_prefetch_desc(&tmap_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const AbortCtx ab{abort_flag, a.status, a.wait_limit_ns};
+    const int kblocks = a.T / kBK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_phase = 0;
+            bool ok = true;
+            const uint64_t keep = policy_evict_last();
+            for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, a, mb, nb);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded(&empty[stage], phase ^ 1u, ab)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                    uint8_t* a_dst = sA + stage * C::kABytes;
+                    uint8_t* b_dst = sB + stage * C::kBBytes;
+                    const int k0 = kb * kBK;
+                    tma_load_2d_hint(a_dst, &tmap_dy, &full[stage], mb * kBM, k0, keep);
+                    tma_load_2d_hint(a_dst + kBK * 128, &tmap_dy, &full[stage], mb * kBM + 64, k0, keep);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d_hint(b_dst + j * kBK * 128, &tmap_x, &full[stage], nb * BN + 64 * j, k0, keep);
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::kStages; ++s)
+                    if ((issued >> s) & 1u) drain_bounded(&full[s], (issued_phase >> s) & 1u, a.wait_limit_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32_mn_major(kBM, BN);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true, issued_any = false;
+            for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+                if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, ab)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded(&full[stage], phase, ab)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_addr(sA + stage * C::kABytes);
+                    const uint32_t b_base = smem_addr(sB + stage * C::kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                        // 16 tokens = 16 rows of 128 bytes: advance 2048 bytes per MMA.  Within a
+                        // stage, the MN-direction 64-element column blocks are kBK*128 bytes apart
+                        // (leading byte offset) and 8-token row groups 1024 bytes apart (stride).
+                        const uint64_t ad = smem_desc_sw128(a_base + kk * 2048, kBK * 128, 1024);
+                        const uint64_t bd = smem_desc_sw128(b_base + kk * 2048, kBK * 128, 1024);
+                        tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued_any = true;
+                    tc_commit(&empty[stage]);
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(&acc_full[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok && issued_any) {
+                tc_commit(drain);
+                drain_bounded(drain, 0, a.wait_limit_ns);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue warps
+        const int e = warp - 2;
+        const int quarter = warp & 3;   // a warp may only touch TMEM lanes 32*(warp%4) .. +31
+        const int half = e >> 2;
+        constexpr int kWidth = BN / 2;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, a, mb, nb);
+            int ok = 1;
+            if (lane == 0) ok = wait_bounded(&acc_full[acc], acc_phase, ab) ? 1 : 0;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int row = mb * kBM + quarter * 32 + lane;
+            const int col0 = nb * BN + half * kWidth;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + half * kWidth);
+            if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth>(a, row, col0, taddr);
+            else if constexpr (EPI == kEpiOptFP32) epi_opt_fp32<OPT, kWidth>(a, row, col0, taddr);
+            else epi_opt_int8<OPT, kWidth>(a, row, col0, taddr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace forge

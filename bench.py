@@ -1,0 +1,386 @@
+"""Benchmark of the fused weight-gradient + optimizer step (one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch: for every linear layer of the
+workload, dW = dY^T X accumulated in FP32 on chip and consumed by the optimizer in the same
+kernel (weights and moments updated in place).  Default workload: the Llama-3.1-8B MLP weight
+updates (gate/up 14336x4096, down 4096x14336, T = 4096 tokens, AdamW with FP32 moments at step
+10), inputs seeded and synthetic, resident in HBM before timing starts.
+
+  value       fused TFLOP/s = sum over layers of 2 T d_out d_in per step / device time per step
+  unfused     the two-phase baseline (dW written to HBM, then the optimizer pass) on the same data
+  e2e         the same metric with dY/X copied from pinned host memory each step and the updated
+              weights copied back, through the same C-ABI calls
+  roofline    the fused kernel's average launch time (CUDA events on its stream) against the
+              measured dense BF16 tensor peak
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
+
+--impl reference times the CPU oracle as the reference arm (there is no other implementation of
+this method to run).  Under torchrun every rank runs its own copy of the per-GPU work (the layers
+are independent; no data-path collective), so the scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "backward_optimizer_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(workload: str, opt: str, state: str):
+    """DRAM bytes per launch of the fused kernel from a committed ncu summary, if it was taken
+    from the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{workload}/{opt}/{state}")
+    if not e or e.get("source_hash") != _kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        if self.out:
+            self.out.close()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------ GPU arm
+
+def _make_layer(wl, i, opt, state, device, seed):
+    import torch
+    from workloads import activations, layer_state
+    dy, x = activations(wl, i, 1, seed, device=device)
+    w, m, v = layer_state(wl, i, opt, seed, device=device)
+    q = None
+    if state == "int8":
+        l = wl.layers[i]
+        n = l.d_out * l.d_in
+        m = None if m is None else torch.randint(-127, 128, (l.d_out, l.d_in), dtype=torch.int8, device=device)
+        v = None if v is None else torch.randint(0, 128, (l.d_out, l.d_in), dtype=torch.int8, device=device)
+        q = torch.rand(2 * n // 64, device=device) * 1e-5
+    return dict(dy=dy, x=x, w=w, m=m, v=v, q=q)
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import backward_optimizer_gb300 as fg
+    from workloads import WORKLOADS, default_hparams
+
+    fg.build()
+    fg.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = WORKLOADS[args.workload]
+    hp = default_hparams(args.opt)
+    t_step = wl.steps[-1]
+    layers = [_make_layer(wl, i, args.opt, args.state, dev, seed=1000 * rank) for i in range(len(wl.layers))]
+    stream = torch.cuda.current_stream()
+    flops_step = wl.flops_per_step()
+
+    def fused_pass(ev=None):
+        for i, L in enumerate(layers):
+            if ev is not None:
+                ev[i][0].record(stream)
+            fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step,
+                             seed=0x5EED + i, stream=stream)
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- fused, device-resident
+    for _ in range(args.warmup):
+        fused_pass()
+    torch.cuda.synchronize()
+    status = fg.sync_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    per_launch = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in layers] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = fg.launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        start.record(stream)
+        for k in range(args.steps):
+            fused_pass(per_launch[k])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = fg.launch_count() - launches0
+    elapsed_ms = start.elapsed_time(stop)
+    launch_ms = [a.elapsed_time(b) for step_ev in per_launch for (a, b) in step_ev]
+    status = fg.sync_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+
+    # ---- unfused two-phase baseline on the same data: all dW to HBM, then every optimizer pass
+    dws = [torch.empty(l.d_out, l.d_in, dtype=torch.float32, device=dev) for l in wl.layers]
+    torch.cuda.synchronize()
+    mem0 = torch.cuda.memory_allocated()
+
+    def unfused_pass():
+        for L, dW in zip(layers, dws):
+            fg.dw_gemm(L["dy"], L["x"], dW, stream=stream)
+        for i, (L, dW) in enumerate(zip(layers, dws)):
+            fg.opt_step(dW, L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step, seed=0x5EED + i, stream=stream)
+
+    for _ in range(args.warmup):
+        unfused_pass()
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    u0.record(stream)
+    for _ in range(args.steps):
+        unfused_pass()
+    u1.record(stream)
+    torch.cuda.synchronize()
+    unfused_ms = u0.elapsed_time(u1) / args.steps
+    grad_pool_unfused = sum(d.numel() * 4 for d in dws)
+    del dws
+    torch.cuda.synchronize()
+
+    # ---- end to end: dY/X from pinned host memory each step, updated W copied back
+    host_in = [(L["dy"].cpu().pin_memory(), L["x"].cpu().pin_memory()) for L in layers]
+    host_out = [torch.empty(L["w"].shape, dtype=L["w"].dtype).pin_memory() for L in layers]
+    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_pass():
+        for i, L in enumerate(layers):
+            L["dy"].copy_(host_in[i][0], non_blocking=True)
+            L["x"].copy_(host_in[i][1], non_blocking=True)
+            fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step,
+                             seed=0x5EED + i, stream=stream)
+            host_out[i].copy_(L["w"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_pass()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_pass()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    # ---- max over ranks
+    times = torch.tensor([elapsed_ms, unfused_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    elapsed_ms, unfused_ms, e2e_ms = times.tolist()
+    ms_step = elapsed_ms / args.steps
+    return dict(ms_step=ms_step, flops_step=flops_step, launch_ms=launch_ms, launches=launches,
+                unfused_ms=unfused_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks.summary(),
+                grad_pool_unfused=grad_pool_unfused, mem_fused=mem0, wl=wl)
+
+
+# ------------------------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(workload: str, opt: str, rows: int, seed: int = 0):
+    """Time the oracle's whole step on the first `rows` weight rows of every layer (a bounded
+    sample of the workload).  Returns (flops done, seconds)."""
+    import numpy as np
+    from oracle import step as ostep
+    from tests.helpers import bits, f32
+    from workloads import WORKLOADS, activations, default_hparams, layer_state
+
+    wl = WORKLOADS[workload]
+    hp = default_hparams(opt)
+    flops, secs = 0, 0.0
+    for i, l in enumerate(wl.layers[:3]):
+        r = min(rows, l.d_out)
+        dy, x = activations(wl, i, 1, seed)
+        w, m, v = layer_state(wl, i, opt, seed)
+        dyb, xb, wb = bits(dy)[:, :r], bits(x), bits(w)[:r]
+        mm = None if m is None else f32(m)[:r]
+        vv = None if v is None else f32(v)[:r]
+        t0 = time.perf_counter()
+        ostep.fused_step(opt, np.ascontiguousarray(dyb), xb, np.ascontiguousarray(wb), mm, vv, hp, wl.steps[-1], 1 + i)
+        secs += time.perf_counter() - t0
+        flops += 2 * wl.T * r * l.d_in
+    return flops, secs
+
+
+def cpu_baseline(args):
+    flops, secs = oracle_sample(args.workload, args.opt, args.oracle_rows)
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {args.oracle_rows} weight rows of each of the first 3 layers of {args.workload} "
+                      f"(float64 NumPy oracle, whole step incl. Philox/SR), {secs:.1f} s"}
+
+
+# ------------------------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="forge", choices=["forge", "reference"])
+    ap.add_argument("--workload", default="llama8b-mlp")
+    ap.add_argument("--opt", default="adamw")
+    ap.add_argument("--state", default="fp32", choices=["fp32", "int8"])
+    ap.add_argument("--oracle-rows", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    from workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    metric = "fused dW+AdamW TFLOP/s & step ms per layer sweep vs unfused; % of BF16 tensor peak"
+    config = {"workload": f"{wl.name}: {wl.description}", "opt": args.opt, "state": args.state,
+              "T": wl.T, "layers": [f"{l.name} {l.d_out}x{l.d_in}" for l in wl.layers[:7]],
+              "n_layers": len(wl.layers), "l2": "inputs larger than L2 (W/m/v/dY/X per step >> 129 MB)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        t0 = time.perf_counter()
+        vals = []
+        for _ in range(args.warmup + args.steps):
+            flops, secs = oracle_sample(args.workload, args.opt, args.oracle_rows)
+            vals.append(flops / secs / 1e12)
+        vals = vals[args.warmup:]
+        v = statistics.median(vals)
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": f"first {args.oracle_rows} rows of each of 3 layers per step"},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": time.perf_counter() - t0}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    r = run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    peaks, peaks_src = _peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    n_layers = len(r["wl"].layers)
+    avg_launch_ms = statistics.mean(r["launch_ms"])
+    flops_launch = r["flops_step"] / n_layers
+    achieved = flops_launch / (avg_launch_ms * 1e-3) / 1e12
+    value = world * r["flops_step"] / (r["ms_step"] * 1e-3) / 1e12
+    line = {
+        "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+        "unfused": {"ms_per_step": r["unfused_ms"], "value": world * r["flops_step"] / (r["unfused_ms"] * 1e-3) / 1e12,
+                    "speedup_fused": r["unfused_ms"] / r["ms_step"]},
+        "grad_pool_bytes": {"fused_hbm": 0, "unfused_hbm": r["grad_pool_unfused"],
+                            "fused_on_chip": "2 TMEM accumulators x 128x128 FP32 per SM (128 KiB)"},
+        "e2e": {"value": world * r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": _ncu_traffic(args.workload, args.opt, args.state),
+                     "kernel": "forge_tile_kernel (fused)", "avg_launch_ms": avg_launch_ms,
+                     "flops_per_launch": flops_launch, "peak_source": f"bf16_tflops of {peaks_src}"},
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

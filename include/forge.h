@@ -1,0 +1,177 @@
+/*
+ * forge.h -- C ABI of the fused weight-gradient + optimizer-step library (libforge.so).
+ *
+ * The method is FORGE ("FORGE: Fused On-Register Gradient Elimination for
+ * Memory-Efficient LLM Training", gist.science technical summary).  Its §2
+ * Methodology, Core mechanism, processes the weight matrix of a linear layer
+ * one 128 x 128 tile at a time: (1) the tile of the weight gradient
+ * dW = dY^T X is accumulated in FP32 on chip, (2) the optimizer update is
+ * applied to the finished tile on chip, (3) the gradient tile is discarded and
+ * never written to device memory, (4) only the updated weight tile and the
+ * (optionally quantised) moment tiles are written back.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - The layer is Y = X W^T with W of shape [d_out, d_in].
+ *  - dY is [T, d_out] and X is [T, d_in]: bfloat16, row-major (token-major), as
+ *    the forward and backward passes of a linear layer leave them.
+ *  - W is [d_out, d_in] bfloat16, row-major.  m and v are [d_out, d_in] row-major,
+ *    binary32 (FORGE_STATE_FP32) or int8 codes (FORGE_STATE_INT8_B64).
+ *  - INT8 states (§2 Precision and fidelity, third low-precision point: blocks
+ *    of 64): each run of 64 consecutive elements of a row shares one binary32
+ *    scale s = absmax / 127; code q = clamp(round_half_even(x / s), -127, 127);
+ *    value = q * s.  `qscales` then points to 2 * d_out * d_in / 64 binary32
+ *    scales: the m scales first ([d_out, d_in/64] row-major), then the v scales.
+ *  - All pointers are DEVICE pointers of the current CUDA device, 32-byte
+ *    aligned, owned by the caller.  The library allocates no device memory and
+ *    keeps no pointer after a call returns.  W, m, v and qscales are updated in
+ *    place.
+ *  - Sizes: d_out and d_in multiples of 128 (the tile, §2 Methodology), T a
+ *    multiple of 64 (the token slice of one pipeline stage) or T == 0; d_out or
+ *    d_in == 0 is an empty layer and a no-op.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and return after the launch is queued.  Argument errors
+ *    are detected on the host before anything is launched and are returned
+ *    synchronously; nothing is written in that case.
+ *  - Every on-device wait in the kernels is bounded in time.  A wait that runs
+ *    out sets a device status word and the kernel returns early; the word is
+ *    read and cleared by forge_sync_status().
+ *  - Ordering (§5 Significance and claims, limitations: the input gradient must
+ *    be read before the weights are updated): any dX = dY W that needs the old W
+ *    must be enqueued before forge_fused_dw_step on the same stream.  The library
+ *    does not compute dX.
+ */
+#ifndef FORGE_H_
+#define FORGE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+#if defined(__GNUC__)
+#define FORGE_API __attribute__((visibility("default")))
+#else
+#define FORGE_API
+#endif
+
+typedef enum forge_status {
+    FORGE_OK = 0,
+    FORGE_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, bad enum, step < 1 */
+    FORGE_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. INT8 states for SGD) */
+    FORGE_ERR_MISALIGNED = 3,       /* a pointer is not 32-byte aligned */
+    FORGE_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
+    FORGE_ERR_NOT_SM103 = 5,        /* current device is not compute capability 10.3 */
+    FORGE_ERR_TIMEOUT = 6           /* a bounded on-device wait ran out (from forge_sync_status) */
+} forge_status;
+
+/* The eight element-wise optimizers of §3 Key contributions, "Generality". */
+typedef enum forge_opt_kind {
+    FORGE_ADAMW = 0,        /* m, v; weight decay decoupled: W <- W (1 - lr wd) */
+    FORGE_NADAM = 1,        /* m, v; weight decay coupled:   g <- g + wd W       */
+    FORGE_RADAM = 2,        /* m, v; coupled */
+    FORGE_LION = 3,         /* m;    decoupled */
+    FORGE_RMSPROP = 4,      /* v;    coupled */
+    FORGE_ADAGRAD = 5,      /* v;    coupled */
+    FORGE_SGD = 6,          /* none; coupled */
+    FORGE_SGD_MOMENTUM = 7  /* m;    coupled; m <- momentum m + g (no dampening, not Nesterov) */
+} forge_opt_kind;
+
+typedef enum forge_state_dtype {
+    FORGE_STATE_FP32 = 0,
+    FORGE_STATE_INT8_B64 = 1
+} forge_state_dtype;
+
+typedef struct forge_shape {
+    int64_t T;      /* tokens: the contraction length of dW = dY^T X */
+    int64_t d_out;  /* rows of W */
+    int64_t d_in;   /* columns of W */
+    int32_t state;  /* a forge_state_dtype */
+    int32_t reserved; /* must be 0 */
+} forge_shape;
+
+/* Hyperparameters, each a binary32.  Fields an optimizer does not use are ignored.
+ * Step-dependent factors (bias corrections, the NAdam momentum product, the RAdam
+ * rectification) are derived on the host in binary64 from these and `step`,
+ * assuming the run started at step 1 with the same hyperparameters. */
+typedef struct forge_hparams {
+    float lr;
+    float beta1;          /* Adam-family / Lion first coefficient */
+    float beta2;          /* Adam-family second moment / Lion moment coefficient */
+    float eps;
+    float weight_decay;
+    float momentum;       /* SGD-momentum */
+    float alpha;          /* RMSprop smoothing constant */
+    float momentum_decay; /* NAdam psi */
+    float lr_decay;       /* AdaGrad */
+} forge_hparams;
+
+/*
+ * forge_fused_dw_step -- one fused step for one linear layer (§2 Methodology,
+ * Core mechanism, steps 1-4).
+ *
+ *   For every 128 x 128 tile of W: g = sum_t dY[t, rows]^T X[t, cols] in FP32 on
+ *   chip (never written to device memory); the optimizer `opt_kind` updates the
+ *   tile's W, m, v with g; the new moments are stored as binary32 or requantised
+ *   to INT8 (the update itself uses the unquantised new moments); the new weight,
+ *   computed in binary32, is stored as bfloat16 by stochastic rounding (§2
+ *   Precision and fidelity, second low-precision point) with 16 bits of a
+ *   Philox4x32-10 stream: key (seed mod 2^32, seed div 2^32), counter
+ *   (e div 8 as 64 bits, step as 64 bits) for row-major element index e, element
+ *   e taking the low (e even) or high (e odd) half of output word (e div 2) mod 4.
+ *
+ *   m: required for ADAMW, NADAM, RADAM, LION, SGD_MOMENTUM; ignored otherwise.
+ *   v: required for ADAMW, NADAM, RADAM, RMSPROP, ADAGRAD; ignored otherwise.
+ *   qscales: required iff shape->state == FORGE_STATE_INT8_B64 (not allowed for SGD).
+ *   step: the 1-based optimizer step t.  seed: the layer's SR seed.
+ *   T == 0 applies the update with a zero gradient.
+ */
+FORGE_API forge_status forge_fused_dw_step(const void *dY, const void *X, void *W, void *m, void *v,
+                                 float *qscales, forge_opt_kind opt_kind,
+                                 const forge_hparams *hp, const forge_shape *shape,
+                                 int64_t step, uint64_t seed, struct CUstream_st *stream);
+
+/*
+ * forge_dw_gemm -- the weight gradient alone, written to device memory: dW [d_out,
+ * d_in] binary32 row-major, dW = dY^T X accumulated in FP32.  This is the first
+ * half of the two-phase schedule of §1 The problem (backward writes the full
+ * gradient, the optimizer reads it back); it exists only as the unfused
+ * baseline.  shape->state is ignored.
+ */
+FORGE_API forge_status forge_dw_gemm(const void *dY, const void *X, float *dW, const forge_shape *shape,
+                           struct CUstream_st *stream);
+
+/*
+ * forge_opt_step -- the optimizer half of the two-phase schedule: reads a
+ * materialised gradient dW [d_out, d_in] binary32 and applies exactly the update,
+ * state write-back and stochastic rounding of forge_fused_dw_step.  shape->T is
+ * ignored.  dW == NULL means a zero gradient.
+ */
+FORGE_API forge_status forge_opt_step(const float *dW, void *W, void *m, void *v, float *qscales,
+                            forge_opt_kind opt_kind, const forge_hparams *hp,
+                            const forge_shape *shape, int64_t step, uint64_t seed,
+                            struct CUstream_st *stream);
+
+/* Waits for `stream`, then reads and clears the device status word of the current
+ * device: FORGE_ERR_TIMEOUT if a bounded wait ran out in a kernel since the last
+ * call, FORGE_ERR_CUDA if the stream reported an error, FORGE_OK otherwise. */
+FORGE_API forge_status forge_sync_status(struct CUstream_st *stream);
+
+/* Time limit of every bounded on-device wait, in nanoseconds (default 2e9).
+ * Values below 1e6 are raised to 1e6.  Host-side setting, applies to later launches. */
+FORGE_API void forge_set_wait_limit_ns(uint64_t ns);
+
+/* Number of the library's own kernel launches queued since load (all entry points). */
+FORGE_API uint64_t forge_launch_count(void);
+
+/* A static, NUL-terminated description of a status code. */
+FORGE_API const char *forge_status_string(forge_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FORGE_H_ */

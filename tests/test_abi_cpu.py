@@ -1,0 +1,121 @@
+"""The C-ABI library builds, loads, exports what include/forge.h declares, and rejects bad
+arguments on the host before touching a device (CPU only: no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import backward_optimizer_gb300 as fg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    fg.build()
+    return fg.lib()
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(forge_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("forge_fused_dw_step", "forge_dw_gemm", "forge_opt_step", "forge_sync_status",
+              "forge_status_string"):
+        assert n in names
+
+
+@pytest.mark.parametrize("name", _declared_functions())
+def test_every_declared_symbol_is_exported(L, name):
+    assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.forge_status_string(code)
+    assert b"unknown" in L.forge_status_string(99)
+
+
+def _shape(T=256, d_out=512, d_in=256, state=0, reserved=0):
+    return fg.ForgeShape(T=T, d_out=d_out, d_in=d_in, state=state, reserved=reserved)
+
+
+A = 0x10000  # aligned fake addresses: every call below is rejected before any dereference
+
+
+def _fused(L, shape, opt=0, step=1, W=A, m=A, v=A, q=None, dY=A, X=A, hp=True):
+    hps = fg.hparams_struct() if hp else None
+    return L.forge_fused_dw_step(dY, X, W, m, v, q, opt, ctypes.byref(hps) if hps else None,
+                                 ctypes.byref(shape) if shape is not None else None, step, 0, None)
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(shape=None), 1),
+    (dict(shape=_shape(d_out=500)), 1),
+    (dict(shape=_shape(d_in=200)), 1),
+    (dict(shape=_shape(T=100)), 1),
+    (dict(shape=_shape(T=-64)), 1),
+    (dict(shape=_shape(reserved=1)), 1),
+    (dict(shape=_shape(state=5)), 1),
+    (dict(shape=_shape(), opt=9), 1),
+    (dict(shape=_shape(), step=0), 1),
+    (dict(shape=_shape(), hp=False), 1),
+    (dict(shape=_shape(), W=None), 1),
+    (dict(shape=_shape(), m=None), 1),
+    (dict(shape=_shape(), v=None), 1),
+    (dict(shape=_shape(state=1), q=None), 1),
+    (dict(shape=_shape(state=1), opt=6, q=A), 2),
+    (dict(shape=_shape(), W=A + 8), 3),
+    (dict(shape=_shape(), m=A + 16), 3),
+    (dict(shape=_shape(), dY=A + 2), 3),
+    (dict(shape=_shape(), X=None), 1),
+])
+def test_fused_rejects_bad_arguments_on_host(L, kw, code):
+    shape = kw.pop("shape")
+    assert _fused(L, shape, **kw) == code
+
+
+def test_unused_moments_may_be_null(L):
+    # SGD uses neither moment: only the device step can fail here (no GPU on a CPU machine)
+    if _cuda_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    st = _fused(L, _shape(), opt=6, m=None, v=None)
+    assert st == 4  # FORGE_ERR_CUDA: argument checks passed, no device
+
+
+def test_dw_gemm_and_opt_step_reject_bad_arguments(L):
+    assert L.forge_dw_gemm(A, A, None, ctypes.byref(_shape()), None) == 1
+    assert L.forge_dw_gemm(A, A, A + 4, ctypes.byref(_shape()), None) == 3
+    assert L.forge_dw_gemm(A, A, A, ctypes.byref(_shape(d_in=64)), None) == 1
+    hp = fg.hparams_struct()
+    assert L.forge_opt_step(A, None, A, A, None, 0, ctypes.byref(hp), ctypes.byref(_shape()), 1, 0, None) == 1
+    assert L.forge_opt_step(A + 4, A, A, A, None, 0, ctypes.byref(hp), ctypes.byref(_shape()), 1, 0, None) == 3
+    assert L.forge_opt_step(A, A, A, A, None, 0, ctypes.byref(hp), ctypes.byref(_shape()), 0, 0, None) == 1
+
+
+def test_wait_limit_setter_and_launch_counter(L):
+    L.forge_set_wait_limit_ns(5)
+    L.forge_set_wait_limit_ns(2_000_000_000)
+    assert L.forge_launch_count() >= 0
+
+
+def _cuda_available():
+    import torch
+    return torch.cuda.is_available()
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(fg, "_lib", None)
+    monkeypatch.setattr(fg, "_LIB_PATH", "/nonexistent/libforge.so")
+    with pytest.raises(fg.ForgeUnavailable):
+        fg.lib()
