@@ -11,7 +11,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/forge.h"
+#include "forge.h"
 #include "launch.h"
 #include "opt_step_kernel.cuh"
 #include "tile_kernel.cuh"
@@ -189,20 +189,33 @@ forge_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : F
 using TileFn = cudaError_t (*)(const forge::TileLaunch&);
 using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
 
-TileFn tile_fn(forge_opt_kind k, bool int8) {
+template <int BN>
+TileFn tile_fn_bn(forge_opt_kind k, bool int8) {
     using namespace forge;
     switch (k) {
-        case FORGE_ADAMW: return int8 ? launch_tile<kAdamW, kEpiOptINT8> : launch_tile<kAdamW, kEpiOptFP32>;
-        case FORGE_NADAM: return int8 ? launch_tile<kNAdam, kEpiOptINT8> : launch_tile<kNAdam, kEpiOptFP32>;
-        case FORGE_RADAM: return int8 ? launch_tile<kRAdam, kEpiOptINT8> : launch_tile<kRAdam, kEpiOptFP32>;
-        case FORGE_LION: return int8 ? launch_tile<kLion, kEpiOptINT8> : launch_tile<kLion, kEpiOptFP32>;
-        case FORGE_RMSPROP: return int8 ? launch_tile<kRMSprop, kEpiOptINT8> : launch_tile<kRMSprop, kEpiOptFP32>;
-        case FORGE_ADAGRAD: return int8 ? launch_tile<kAdaGrad, kEpiOptINT8> : launch_tile<kAdaGrad, kEpiOptFP32>;
-        case FORGE_SGD: return int8 ? nullptr : launch_tile<kSGD, kEpiOptFP32>;
+        case FORGE_ADAMW: return int8 ? launch_tile<kAdamW, kEpiOptINT8, BN> : launch_tile<kAdamW, kEpiOptFP32, BN>;
+        case FORGE_NADAM: return int8 ? launch_tile<kNAdam, kEpiOptINT8, BN> : launch_tile<kNAdam, kEpiOptFP32, BN>;
+        case FORGE_RADAM: return int8 ? launch_tile<kRAdam, kEpiOptINT8, BN> : launch_tile<kRAdam, kEpiOptFP32, BN>;
+        case FORGE_LION: return int8 ? launch_tile<kLion, kEpiOptINT8, BN> : launch_tile<kLion, kEpiOptFP32, BN>;
+        case FORGE_RMSPROP:
+            return int8 ? launch_tile<kRMSprop, kEpiOptINT8, BN> : launch_tile<kRMSprop, kEpiOptFP32, BN>;
+        case FORGE_ADAGRAD:
+            return int8 ? launch_tile<kAdaGrad, kEpiOptINT8, BN> : launch_tile<kAdaGrad, kEpiOptFP32, BN>;
+        case FORGE_SGD: return int8 ? nullptr : launch_tile<kSGD, kEpiOptFP32, BN>;
         case FORGE_SGD_MOMENTUM:
-            return int8 ? launch_tile<kSGDMomentum, kEpiOptINT8> : launch_tile<kSGDMomentum, kEpiOptFP32>;
+            return int8 ? launch_tile<kSGDMomentum, kEpiOptINT8, BN> : launch_tile<kSGDMomentum, kEpiOptFP32, BN>;
     }
     return nullptr;
+}
+
+// Tile width per CTA: 256 columns (two 128 x 128 tiles, halving the operand traffic per flop
+// through shared memory and L2) whenever d_in allows it, else 128.
+int pick_bn(int64_t d_in) { return d_in % 256 == 0 ? 256 : 128; }
+
+TileFn tile_fn(forge_opt_kind k, bool int8, int epi, int bn) {
+    if (epi == forge::kEpiStoreGrad)
+        return bn == 256 ? forge::launch_tile<0, forge::kEpiStoreGrad, 256> : forge::launch_tile<0, forge::kEpiStoreGrad, 128>;
+    return bn == 256 ? tile_fn_bn<256>(k, int8) : tile_fn_bn<128>(k, int8);
 }
 
 OptFn opt_fn(forge_opt_kind k, bool int8) {
@@ -256,7 +269,8 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.d_in = static_cast<int>(shape->d_in);
     a.T = static_cast<int>(shape->T);
     a.tiles_m = a.d_out / forge::kBM;
-    a.tiles_n = a.d_in / forge::kTileBN;
+    const int bn = pick_bn(shape->d_in);
+    a.tiles_n = a.d_in / bn;
     a.num_tiles = a.tiles_m * a.tiles_n;
     // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
     a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
@@ -280,7 +294,7 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     l.args = &a;
     l.grid = a.num_tiles < dev.num_sms ? a.num_tiles : dev.num_sms;
     l.stream = stream;
-    TileFn fn = (epi == forge::kEpiStoreGrad) ? forge::launch_tile<0, forge::kEpiStoreGrad> : tile_fn(k, int8);
+    TileFn fn = tile_fn(k, int8, epi, bn);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(l));

@@ -1,6 +1,5 @@
-// Kernel instantiation of the unfused weight-gradient GEMM (FP32 dW to device memory).
+// Kernel instantiations of the unfused weight-gradient GEMM (FP32 dW to device memory).
 #include "instantiate.cuh"
 
-template cudaError_t forge::launch_tile<0, forge::kEpiStoreGrad>(const forge::TileLaunch&);
-
-int forge::tile_smem_bytes() { return forge::TileCfg<forge::kTileBN>::kSmemBytes; }
+template cudaError_t forge::launch_tile<0, forge::kEpiStoreGrad, 128>(const forge::TileLaunch&);
+template cudaError_t forge::launch_tile<0, forge::kEpiStoreGrad, 256>(const forge::TileLaunch&);

@@ -9,10 +9,10 @@
 
 namespace forge {
 
-template <int OPT, int EPI>
+template <int OPT, int EPI, int BN>
 cudaError_t launch_tile(const TileLaunch& l) {
-    using C = TileCfg<kTileBN>;
-    auto kernel = forge_tile_kernel<kTileBN, EPI, OPT>;
+    using C = TileCfg<BN>;
+    auto kernel = forge_tile_kernel<BN, EPI, OPT>;
     static std::atomic<uint64_t> configured{0};  // one bit per device ordinal
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -35,10 +35,12 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 
 }  // namespace forge
 
-#define FORGE_INSTANTIATE_OPT(OPT)                                                      \
-    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptFP32>(const forge::TileLaunch&); \
+#define FORGE_INSTANTIATE_OPT(OPT)                                                             \
+    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptFP32, 128>(const forge::TileLaunch&); \
+    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptFP32, 256>(const forge::TileLaunch&); \
     template cudaError_t forge::launch_opt<OPT, false>(const forge::OptArgs&, int, cudaStream_t);
 
-#define FORGE_INSTANTIATE_OPT_INT8(OPT)                                                 \
-    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptINT8>(const forge::TileLaunch&); \
+#define FORGE_INSTANTIATE_OPT_INT8(OPT)                                                        \
+    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptINT8, 128>(const forge::TileLaunch&); \
+    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptINT8, 256>(const forge::TileLaunch&); \
     template cudaError_t forge::launch_opt<OPT, true>(const forge::OptArgs&, int, cudaStream_t);

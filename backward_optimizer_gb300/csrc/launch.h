@@ -21,10 +21,9 @@ struct TileLaunch {
 };
 
 // EPI: 0 = store FP32 dW, 1 = fused optimizer with FP32 states, 2 = fused optimizer with INT8 states.
-template <int OPT, int EPI> cudaError_t launch_tile(const TileLaunch& l);
+// BN: tile columns per CTA (128, or 256 = two 128 x 128 tiles side by side).
+template <int OPT, int EPI, int BN> cudaError_t launch_tile(const TileLaunch& l);
 template <int OPT, bool INT8> cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream);
 
-// Shared-memory bytes the tile kernel needs (for the host's capacity check).
-int tile_smem_bytes();
 
 }  // namespace forge

@@ -181,6 +181,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_mn_major(int M, int N) {
            | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
 }
 
+// ---------------------------------------------------------------- shared memory
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t* r) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- 256-bit global accesses
 // ".cs": streamed once, allocated evict-first, so the weight/moment stream does not push
 // the dY/X operand tiles out of L2.

@@ -38,7 +38,6 @@ constexpr int kUmmaK = 16;       // K of one kind::f16 MMA
 constexpr int kNumEpiWarps = 8;  // two warps per TMEM lane quarter, each owning half the columns
 constexpr int kThreads = 64 + 32 * kNumEpiWarps;
 constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
-constexpr int kTileBN = 128;     // tile columns (d_in) of the compiled kernels: the 128 x 128 tile
 
 enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2 };
 
@@ -50,8 +49,10 @@ struct TileCfg {
     static constexpr int kBBytes = BN * kBK * 2;   // one stage of X: BN/64 boxes of [64 tokens][64 cols]
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator
+    static constexpr int kStripBytes = 32 * 32 * 4;                 // one warp's 32 x 32 FP32 transpose strip
+    static constexpr int kEpiBytes = kNumEpiWarps * kStripBytes;    // 32 KiB
     static constexpr int kBarrierBytes = 256;
-    static constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // + alignment slack
+    static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + kBarrierBytes + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -111,76 +112,101 @@ __device__ __forceinline__ void tile_coords(int tile, const TileArgs& a, int& mb
 }
 
 // ---------------------------------------------------------------- epilogues
-// Each is called by one warp for one tile: `row` is this thread's weight row, `col0` the first
-// weight column of the warp's strip, `taddr` the TMEM address of (its lane quarter, col0).
+// Each is called by one warp for one tile.  The warp owns weight rows row0 .. row0+31 (its TMEM
+// lane quarter) and columns col0 .. col0+WIDTH-1; `taddr` is the TMEM address of (row0, col0);
+// `strip` is the warp's private 4 KiB shared-memory transpose buffer.
 
-__device__ __forceinline__ void st_v8_f32(float* p, const uint32_t* r) {
+__device__ __forceinline__ void st_v8_f32(float* p, const uint32_t (&r)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
                  "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");
 }
 
+// Moves a 32-row x 32-column FP32 strip of the accumulator from TMEM, where thread i holds row i,
+// to the ownership used for device-memory accesses: lane l receives columns 8(l mod 4) .. +7 of
+// rows (l div 4) + 8k, k = 0..3, in out[k][0..7].  Four consecutive lanes then cover one row's
+// 32 columns, so every warp-wide access touches 8 rows x one contiguous span instead of 32 rows.
+// The strip is written with its 16-byte chunks XOR-swizzled by (row mod 8), which makes both the
+// row-wise writes and the column-wise reads free of bank conflicts.
+__device__ __forceinline__ void strip_transpose(uint32_t taddr, uint8_t* strip, uint32_t (&out)[4][8]) {
+    const uint32_t lane = threadIdx.x & 31u;
+    uint32_t g[32];
+    tmem_ld_32x32b_x32(taddr, g);
+    tmem_ld_wait(g);
+    const uint32_t base = smem_addr(strip);
+#pragma unroll
+    for (uint32_t j = 0; j < 8; ++j)
+        st_shared_v4(base + lane * 128u + ((j ^ (lane & 7u)) << 4), g[4 * j], g[4 * j + 1], g[4 * j + 2],
+                     g[4 * j + 3]);
+    __syncwarp();
+    const uint32_t sub_row = lane >> 2;  // < 8, so (row mod 8) of every row this lane reads
+#pragma unroll
+    for (uint32_t k = 0; k < 4; ++k) {
+        const uint32_t r = sub_row + 8u * k;
+#pragma unroll
+        for (uint32_t h = 0; h < 2; ++h) {
+            const uint32_t chunk = 2u * (lane & 3u) + h;
+            ld_shared_v4(base + r * 128u + ((chunk ^ sub_row) << 4), &out[k][4 * h]);
+        }
+    }
+    __syncwarp();  // the strip may be overwritten by the next call
+}
+
 template <int WIDTH>
-__device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row, int col0, uint32_t taddr) {
-    float* dst = a.dW + static_cast<size_t>(row) * a.d_in + col0;
+__device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int col0, uint32_t taddr,
+                                               uint8_t* strip) {
+    const int lane = threadIdx.x & 31;
+    float* base = a.dW + static_cast<size_t>(row0 + (lane >> 2)) * a.d_in + col0 + 8 * (lane & 3);
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 32) {
-        uint32_t g[32];
-        tmem_ld_32x32b_x32(taddr + c, g);
-        tmem_ld_wait(g);
+        uint32_t t[4][8];
+        strip_transpose(taddr + c, strip, t);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) st_v8_f32(dst + c + 8 * q, &g[8 * q]);
+        for (int k = 0; k < 4; ++k) st_v8_f32(base + static_cast<size_t>(8 * k) * a.d_in + c, t[k]);
     }
 }
 
 template <int OPT, int WIDTH>
-__device__ __forceinline__ void epi_opt_fp32(const TileArgs& a, int row, int col0, uint32_t taddr) {
+__device__ __forceinline__ void epi_opt_fp32(const TileArgs& a, int row0, int col0, uint32_t taddr,
+                                             uint8_t* strip) {
     using Tr = OptTraits<OPT>;
-    const size_t row_base = static_cast<size_t>(row) * a.d_in + col0;
+    const int lane = threadIdx.x & 31;
+    // first element of this lane's 8-column run in row (row0 + lane/4); rows k = 1..3 follow at +8 rows
+    const size_t lane_base = static_cast<size_t>(row0 + (lane >> 2)) * a.d_in + col0 + 8 * (lane & 3);
+    const size_t row_step = static_cast<size_t>(8) * a.d_in;
     float* mp = static_cast<float*>(a.m);
     float* vp = static_cast<float*>(a.v);
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 32) {
-        const size_t e0 = row_base + c;
-        uint32_t w[16], m[32], v[32];
-        ld_cs_v8(a.W + e0, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
-        ld_cs_v8(a.W + e0 + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
-        if constexpr (Tr::kM) {
+        uint32_t w[4][4], m[4][8], v[4][8];
+        // the W/m/v loads do not depend on the gradient: issue them before the TMEM read
 #pragma unroll
-            for (int q = 0; q < 4; ++q) ld_cs_v8(mp + e0 + 8 * q, *reinterpret_cast<uint32_t(*)[8]>(&m[8 * q]));
+        for (int k = 0; k < 4; ++k) {
+            const size_t e = lane_base + k * row_step + c;
+            ld_cs_v4(a.W + e, w[k]);
+            if constexpr (Tr::kM) ld_cs_v8(mp + e, m[k]);
+            if constexpr (Tr::kV) ld_cs_v8(vp + e, v[k]);
         }
-        if constexpr (Tr::kV) {
+        uint32_t g[4][8];
+        strip_transpose(taddr + c, strip, g);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) ld_cs_v8(vp + e0 + 8 * q, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * q]));
-        }
-        uint32_t g[32];
-        tmem_ld_32x32b_x32(taddr + c, g);
-        tmem_ld_wait(g);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const Philox4 p = sr_words((e0 >> 3) + q, a.seed, a.step);
+        for (int k = 0; k < 4; ++k) {
+            const size_t e = lane_base + k * row_step + c;
+            const Philox4 p = sr_words(e >> 3, a.seed, a.step);
 #pragma unroll
             for (int j = 0; j < 8; j += 2) {
-                const int i = 8 * q + j;
-                const uint32_t wp = w[i >> 1];
-                float m0 = Tr::kM ? __uint_as_float(m[i]) : 0.f, m1 = Tr::kM ? __uint_as_float(m[i + 1]) : 0.f;
-                float v0 = Tr::kV ? __uint_as_float(v[i]) : 0.f, v1 = Tr::kV ? __uint_as_float(v[i + 1]) : 0.f;
-                const float w0 = opt_update<OPT>(__uint_as_float(g[i]), bf16_lo(wp), m0, v0, a.s);
-                const float w1 = opt_update<OPT>(__uint_as_float(g[i + 1]), bf16_hi(wp), m1, v1, a.s);
-                w[i >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
-                if constexpr (Tr::kM) { m[i] = __float_as_uint(m0); m[i + 1] = __float_as_uint(m1); }
-                if constexpr (Tr::kV) { v[i] = __float_as_uint(v0); v[i + 1] = __float_as_uint(v1); }
+                const uint32_t wp = w[k][j >> 1];
+                float m0 = Tr::kM ? __uint_as_float(m[k][j]) : 0.f, m1 = Tr::kM ? __uint_as_float(m[k][j + 1]) : 0.f;
+                float v0 = Tr::kV ? __uint_as_float(v[k][j]) : 0.f, v1 = Tr::kV ? __uint_as_float(v[k][j + 1]) : 0.f;
+                const float w0 = opt_update<OPT>(__uint_as_float(g[k][j]), bf16_lo(wp), m0, v0, a.s);
+                const float w1 = opt_update<OPT>(__uint_as_float(g[k][j + 1]), bf16_hi(wp), m1, v1, a.s);
+                w[k][j >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
+                if constexpr (Tr::kM) { m[k][j] = __float_as_uint(m0); m[k][j + 1] = __float_as_uint(m1); }
+                if constexpr (Tr::kV) { v[k][j] = __float_as_uint(v0); v[k][j + 1] = __float_as_uint(v1); }
             }
-        }
-        st_cs_v8(a.W + e0, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
-        st_cs_v8(a.W + e0 + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
-        if constexpr (Tr::kM) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) st_cs_v8(mp + e0 + 8 * q, *reinterpret_cast<uint32_t(*)[8]>(&m[8 * q]));
-        }
-        if constexpr (Tr::kV) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) st_cs_v8(vp + e0 + 8 * q, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * q]));
+            st_cs_v4(a.W + e, w[k]);
+            if constexpr (Tr::kM) st_cs_v8(mp + e, m[k]);
+            if constexpr (Tr::kV) st_cs_v8(vp + e, v[k]);
         }
     }
 }
@@ -190,7 +216,8 @@ __device__ __forceinline__ void epi_opt_fp32(const TileArgs& a, int row, int col
 // pass 2 reloads the gradient from TMEM, recomputes the same moments bit for bit, updates the
 // weight with the unquantised moments and writes the codes under the new scales.
 template <int OPT, int WIDTH>
-__device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row, int col0, uint32_t taddr) {
+__device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int col0, uint32_t taddr) {
+    const int row = row0 + static_cast<int>(threadIdx.x & 31);
     using Tr = OptTraits<OPT>;
     const size_t row_base = static_cast<size_t>(row) * a.d_in + col0;
     int8_t* mp = static_cast<int8_t*>(a.m);
@@ -285,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 128B-swizzle atoms need 1024B alignment
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::kStages * C::kABytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+    uint8_t* strips = smem + C::kStages * C::kStageBytes;  // kNumEpiWarps x 4 KiB transpose strips
+    uint64_t* full = reinterpret_cast<uint64_t*>(strips + C::kEpiBytes);
     uint64_t* empty = full + C::kStages;
     uint64_t* acc_full = empty + C::kStages;
     uint64_t* acc_empty = acc_full + 2;
@@ -408,13 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int row = mb * kBM + quarter * 32 + lane;
+            const int row0 = mb * kBM + quarter * 32;
             const int col0 = nb * BN + half * kWidth;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + half * kWidth);
-            if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth>(a, row, col0, taddr);
-            else if constexpr (EPI == kEpiOptFP32) epi_opt_fp32<OPT, kWidth>(a, row, col0, taddr);
-            else epi_opt_int8<OPT, kWidth>(a, row, col0, taddr);
+            uint8_t* strip = strips + e * C::kStripBytes;
+            if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth>(a, row0, col0, taddr, strip);
+            else if constexpr (EPI == kEpiOptFP32) epi_opt_fp32<OPT, kWidth>(a, row0, col0, taddr, strip);
+            else epi_opt_int8<OPT, kWidth>(a, row0, col0, taddr);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);

@@ -135,9 +135,10 @@ def test_tiny_workload_three_steps():
         rw, rm, rv = bits(W), f32(M), f32(V)  # continue from the GPU's state: per-step parity
 
 
-@pytest.mark.parametrize("opt", OPTIMIZERS)
-def test_fused_matches_oracle_every_optimizer(opt):
-    dy, x, w, m, v = _layer(384, 256, 192, opt, seed=2)
+@pytest.mark.parametrize("opt, d_in", [(o, 256) for o in OPTIMIZERS] + [(o, 384) for o in ("adamw", "nadam", "sgd")])
+def test_fused_matches_oracle_every_optimizer(opt, d_in):
+    """d_in = 256 runs the 128 x 256 CTA tile, d_in = 384 the 128 x 128 one."""
+    dy, x, w, m, v = _layer(384, d_in, 192, opt, seed=2)
     hp = default_hparams(opt, lr=1e-3)
     W, M, V = dev(w), dev(m), dev(v)
     fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, None, opt, hp, 4, seed=11)
@@ -151,9 +152,9 @@ def test_fused_matches_oracle_every_optimizer(opt):
         assert_moments(f32(V), ref["v"], "v")
 
 
-@pytest.mark.parametrize("opt", [o for o in OPTIMIZERS if o != "sgd"])
-def test_fused_int8_matches_oracle(opt):
-    dy, x, w, _, _ = _layer(256, 384, 128, opt, seed=4)
+@pytest.mark.parametrize("opt, d_in", [(o, 384) for o in OPTIMIZERS if o != "sgd"] + [("adamw", 512), ("lion", 768)])
+def test_fused_int8_matches_oracle(opt, d_in):
+    dy, x, w, _, _ = _layer(256, d_in, 128, opt, seed=4)
     mq, ms, vq, vs = _int8_state(w.shape, 9)
     hp = default_hparams(opt, lr=1e-3)
     W, M, V, Q = dev(w), torch.from_numpy(mq).cuda(), torch.from_numpy(vq).cuda(), _qscales_tensor(ms, vs)
@@ -192,9 +193,11 @@ def test_fused_equals_unfused_bitwise(opt):
         assert torch.equal(V1, V2)
 
 
-def test_many_tiles_with_a_ragged_persistent_tail():
-    """160 tiles on 152 SMs: eight CTAs take a second tile."""
-    dy, x, w, m, v = _layer(2048, 1280, 128, "adamw", seed=8)
+@pytest.mark.parametrize("d_in", [2560, 1408])
+def test_many_tiles_with_a_ragged_persistent_tail(d_in):
+    """More CTA tiles than SMs, not a multiple of them: 160 tiles of 128 x 256 (d_in = 2560) or
+    176 tiles of 128 x 128 (d_in = 1408, not a multiple of 256)."""
+    dy, x, w, m, v = _layer(2048, d_in, 128, "adamw", seed=8)
     hp = default_hparams("adamw", lr=1e-3)
     W, M, V = dev(w), dev(m), dev(v)
     fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, None, "adamw", hp, 7, seed=21)
