@@ -189,33 +189,51 @@ forge_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : F
 using TileFn = cudaError_t (*)(const forge::TileLaunch&);
 using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
 
-template <int BN>
-TileFn tile_fn_bn(forge_opt_kind k, bool int8) {
+template <int BN, int CG>
+TileFn tile_fn_v(forge_opt_kind k, bool int8) {
     using namespace forge;
     switch (k) {
-        case FORGE_ADAMW: return int8 ? launch_tile<kAdamW, kEpiOptINT8, BN> : launch_tile<kAdamW, kEpiOptFP32, BN>;
-        case FORGE_NADAM: return int8 ? launch_tile<kNAdam, kEpiOptINT8, BN> : launch_tile<kNAdam, kEpiOptFP32, BN>;
-        case FORGE_RADAM: return int8 ? launch_tile<kRAdam, kEpiOptINT8, BN> : launch_tile<kRAdam, kEpiOptFP32, BN>;
-        case FORGE_LION: return int8 ? launch_tile<kLion, kEpiOptINT8, BN> : launch_tile<kLion, kEpiOptFP32, BN>;
+        case FORGE_ADAMW:
+            return int8 ? launch_tile<kAdamW, kEpiOptINT8, BN, CG> : launch_tile<kAdamW, kEpiOptFP32, BN, CG>;
+        case FORGE_NADAM:
+            return int8 ? launch_tile<kNAdam, kEpiOptINT8, BN, CG> : launch_tile<kNAdam, kEpiOptFP32, BN, CG>;
+        case FORGE_RADAM:
+            return int8 ? launch_tile<kRAdam, kEpiOptINT8, BN, CG> : launch_tile<kRAdam, kEpiOptFP32, BN, CG>;
+        case FORGE_LION:
+            return int8 ? launch_tile<kLion, kEpiOptINT8, BN, CG> : launch_tile<kLion, kEpiOptFP32, BN, CG>;
         case FORGE_RMSPROP:
-            return int8 ? launch_tile<kRMSprop, kEpiOptINT8, BN> : launch_tile<kRMSprop, kEpiOptFP32, BN>;
+            return int8 ? launch_tile<kRMSprop, kEpiOptINT8, BN, CG> : launch_tile<kRMSprop, kEpiOptFP32, BN, CG>;
         case FORGE_ADAGRAD:
-            return int8 ? launch_tile<kAdaGrad, kEpiOptINT8, BN> : launch_tile<kAdaGrad, kEpiOptFP32, BN>;
-        case FORGE_SGD: return int8 ? nullptr : launch_tile<kSGD, kEpiOptFP32, BN>;
+            return int8 ? launch_tile<kAdaGrad, kEpiOptINT8, BN, CG> : launch_tile<kAdaGrad, kEpiOptFP32, BN, CG>;
+        case FORGE_SGD: return int8 ? nullptr : launch_tile<kSGD, kEpiOptFP32, BN, CG>;
         case FORGE_SGD_MOMENTUM:
-            return int8 ? launch_tile<kSGDMomentum, kEpiOptINT8, BN> : launch_tile<kSGDMomentum, kEpiOptFP32, BN>;
+            return int8 ? launch_tile<kSGDMomentum, kEpiOptINT8, BN, CG>
+                        : launch_tile<kSGDMomentum, kEpiOptFP32, BN, CG>;
     }
     return nullptr;
 }
 
-// Tile width per CTA: 256 columns (two 128 x 128 tiles, halving the operand traffic per flop
-// through shared memory and L2) whenever d_in allows it, else 128.
-int pick_bn(int64_t d_in) { return d_in % 256 == 0 ? 256 : 128; }
+// Tile shape per call.  A CTA pair on a 256 x 256 tile stages half as many X bytes per SM as a
+// single CTA on 128 x 256, which in turn stages fewer operand bytes per flop than 128 x 128 (the
+// mainloop is bound by operand traffic from L2 into shared memory).  Each is two or four of the
+// method's 128 x 128 tiles side by side.
+struct TileShape {
+    int bn, cg;
+};
+TileShape pick_shape(int64_t d_out, int64_t d_in) {
+    if (d_out % 256 == 0 && d_in % 256 == 0) return {256, 2};
+    if (d_in % 256 == 0) return {256, 1};
+    return {128, 1};
+}
 
-TileFn tile_fn(forge_opt_kind k, bool int8, int epi, int bn) {
-    if (epi == forge::kEpiStoreGrad)
-        return bn == 256 ? forge::launch_tile<0, forge::kEpiStoreGrad, 256> : forge::launch_tile<0, forge::kEpiStoreGrad, 128>;
-    return bn == 256 ? tile_fn_bn<256>(k, int8) : tile_fn_bn<128>(k, int8);
+TileFn tile_fn(forge_opt_kind k, bool int8, int epi, TileShape t) {
+    using namespace forge;
+    if (epi == kEpiStoreGrad) {
+        if (t.cg == 2) return launch_tile<0, kEpiStoreGrad, 256, 2>;
+        return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1> : launch_tile<0, kEpiStoreGrad, 128, 1>;
+    }
+    if (t.cg == 2) return tile_fn_v<256, 2>(k, int8);
+    return t.bn == 256 ? tile_fn_v<256, 1>(k, int8) : tile_fn_v<128, 1>(k, int8);
 }
 
 OptFn opt_fn(forge_opt_kind k, bool int8) {
@@ -268,9 +286,9 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.d_out = static_cast<int>(shape->d_out);
     a.d_in = static_cast<int>(shape->d_in);
     a.T = static_cast<int>(shape->T);
-    a.tiles_m = a.d_out / forge::kBM;
-    const int bn = pick_bn(shape->d_in);
-    a.tiles_n = a.d_in / bn;
+    const TileShape ts = pick_shape(shape->d_out, shape->d_in);
+    a.tiles_m = a.d_out / (forge::kBM * ts.cg);
+    a.tiles_n = a.d_in / ts.bn;
     a.num_tiles = a.tiles_m * a.tiles_n;
     // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
     a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
@@ -292,9 +310,10 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     st = make_operand_map(&l.tmap_x, X, shape->d_in, shape->T);
     if (st != FORGE_OK) return st;
     l.args = &a;
-    l.grid = a.num_tiles < dev.num_sms ? a.num_tiles : dev.num_sms;
+    l.num_tiles = a.num_tiles;
+    l.num_sms = dev.num_sms;
     l.stream = stream;
-    TileFn fn = tile_fn(k, int8, epi, bn);
+    TileFn fn = tile_fn(k, int8, epi, ts);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(l));

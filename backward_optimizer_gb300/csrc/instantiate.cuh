@@ -9,22 +9,45 @@
 
 namespace forge {
 
-template <int OPT, int EPI, int BN>
+template <int OPT, int EPI, int BN, int CG>
 cudaError_t launch_tile(const TileLaunch& l) {
-    using C = TileCfg<BN>;
-    auto kernel = forge_tile_kernel<BN, EPI, OPT>;
+    using C = TileCfg<BN, CG, EPI>;
+    auto kernel = forge_tile_kernel<BN, CG, EPI, OPT>;
     static std::atomic<uint64_t> configured{0};  // one bit per device ordinal
+    static std::atomic<int> max_clusters[64];    // co-resident CTA pairs per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
+    dev &= 63;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = CG;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = l.stream;
+    cfg.attrs = CG == 2 ? &attr : nullptr;
+    cfg.numAttrs = CG == 2 ? 1 : 0;
+    const uint64_t bit = 1ull << dev;
     if (!(configured.load() & bit)) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (err != cudaSuccess) return err;
+        if (CG == 2) {
+            int n = 0;
+            cfg.gridDim = dim3(2 * l.num_sms, 1, 1);
+            err = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+            if (err != cudaSuccess) return err;
+            max_clusters[dev].store(n > 0 ? n : 1);
+        }
         configured.fetch_or(bit);
     }
-    kernel<<<l.grid, kThreads, C::kSmemBytes, l.stream>>>(l.tmap_dy, l.tmap_x, *l.args);
-    return cudaGetLastError();
+    // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more units than tiles
+    const int cap = CG == 1 ? l.num_sms : max_clusters[dev].load();
+    const int units = l.num_tiles < cap ? l.num_tiles : cap;
+    cfg.gridDim = dim3(units * CG, 1, 1);
+    return cudaLaunchKernelEx(&cfg, kernel, l.tmap_dy, l.tmap_x, *l.args);
 }
 
 template <int OPT, bool INT8>
@@ -35,12 +58,15 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 
 }  // namespace forge
 
-#define FORGE_INSTANTIATE_OPT(OPT)                                                             \
-    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptFP32, 128>(const forge::TileLaunch&); \
-    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptFP32, 256>(const forge::TileLaunch&); \
+#define FORGE_INSTANTIATE_TILES(OPT, EPI)                                                      \
+    template cudaError_t forge::launch_tile<OPT, EPI, 128, 1>(const forge::TileLaunch&);       \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 1>(const forge::TileLaunch&);       \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2>(const forge::TileLaunch&);
+
+#define FORGE_INSTANTIATE_OPT(OPT)                    \
+    FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptFP32) \
     template cudaError_t forge::launch_opt<OPT, false>(const forge::OptArgs&, int, cudaStream_t);
 
-#define FORGE_INSTANTIATE_OPT_INT8(OPT)                                                        \
-    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptINT8, 128>(const forge::TileLaunch&); \
-    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptINT8, 256>(const forge::TileLaunch&); \
+#define FORGE_INSTANTIATE_OPT_INT8(OPT)               \
+    FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptINT8) \
     template cudaError_t forge::launch_opt<OPT, true>(const forge::OptArgs&, int, cudaStream_t);

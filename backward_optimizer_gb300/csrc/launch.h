@@ -16,13 +16,15 @@ struct TileLaunch {
     CUtensorMap tmap_dy;
     CUtensorMap tmap_x;
     const TileArgs* args;
-    int grid;
+    int num_tiles;  // CTA tiles (CG = 1) or CTA-pair tiles (CG = 2)
+    int num_sms;
     cudaStream_t stream;
 };
 
 // EPI: 0 = store FP32 dW, 1 = fused optimizer with FP32 states, 2 = fused optimizer with INT8 states.
-// BN: tile columns per CTA (128, or 256 = two 128 x 128 tiles side by side).
-template <int OPT, int EPI, int BN> cudaError_t launch_tile(const TileLaunch& l);
+// BN: tile columns (128, or 256 = two 128 x 128 tiles side by side).
+// CG: CTAs per tile (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair).
+template <int OPT, int EPI, int BN, int CG> cudaError_t launch_tile(const TileLaunch& l);
 template <int OPT, bool INT8> cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream);
 
 

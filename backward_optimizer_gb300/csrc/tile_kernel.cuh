@@ -41,19 +41,25 @@ constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
 
 enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2 };
 
-template <int BN>
+template <int BN, int CG, int EPI>
 struct TileCfg {
     static_assert(BN == 128 || BN == 256, "tile width");
-    static constexpr int kStages = BN == 128 ? 6 : 4;
+    static_assert(CG == 1 || CG == 2, "CTA group");
+    static constexpr int kBLoad = BN / CG;         // X columns staged by this CTA
     static constexpr int kABytes = kBM * kBK * 2;  // one stage of dY^T: 2 boxes of [64 tokens][64 rows]
-    static constexpr int kBBytes = BN * kBK * 2;   // one stage of X: BN/64 boxes of [64 tokens][64 cols]
+    static constexpr int kBBytes = kBLoad * kBK * 2;  // one stage of X: kBLoad/64 boxes of [64 tokens][64 cols]
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator
-    static constexpr int kStripBytes = 32 * 32 * 4;                 // one warp's 32 x 32 FP32 transpose strip
-    static constexpr int kEpiBytes = kNumEpiWarps * kStripBytes;    // 32 KiB
+    static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator (128 lanes x BN)
+    static constexpr int kStripBytes = 32 * 32 * 4;  // one warp's 32 x 32 FP32 transpose strip
+    static constexpr int kEpiBytes = kNumEpiWarps * kStripBytes;
     static constexpr int kBarrierBytes = 256;
+    static constexpr int kMaxSmem = 232448;
+    // as many operand stages as fit beside the epilogue buffers, at most 6
+    static constexpr int kFitStages = (kMaxSmem - kEpiBytes - kBarrierBytes - 1024) / kStageBytes;
+    static constexpr int kStages = kFitStages < 6 ? kFitStages : 6;
     static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + kBarrierBytes + 1024;  // + alignment slack
-    static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kStages >= 3, "operand pipeline depth");
+    static_assert(kSmemBytes <= kMaxSmem, "shared memory");
 };
 
 struct TileArgs {
@@ -301,12 +307,20 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
 }
 
 // ---------------------------------------------------------------- the kernel
+//
+// CG = 1: one CTA owns a 128 x BN tile (M = 128 MMA).
+// CG = 2: a cluster of two CTAs owns a 256 x BN tile.  Each CTA stages its own 128 rows of dY^T and
+//         its own BN/2 columns of X; the even CTA issues tcgen05.mma.cta_group::2 (M = 256), which
+//         reads both CTAs' shared memory and writes each CTA's 128 accumulator rows into that CTA's
+//         TMEM.  Both CTAs' TMA copies complete on the even CTA's stage barrier; the MMA commits
+//         are multicast to both CTAs; both epilogues release a TMEM buffer on the even CTA's
+//         barrier.  Per SM this halves the X bytes pulled from L2 for the same flops.
 
-template <int BN, int EPI, int OPT>
+template <int BN, int CG, int EPI, int OPT>
 __global__ void __launch_bounds__(kThreads, 1)
     forge_tile_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
                       const TileArgs a) {
-    using C = TileCfg<BN>;
+    using C = TileCfg<BN, CG, EPI>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 128B-swizzle atoms need 1024B alignment
@@ -323,6 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // 0 = the CTA that issues the MMAs
+    const int first_tile = static_cast<int>(blockIdx.x) / CG;
+    const int tile_stride = static_cast<int>(gridDim.x) / CG;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
@@ -331,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], kNumEpiWarps);
+            mbar_init(&acc_empty[i], kNumEpiWarps * CG);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -340,11 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmap_x);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, C::kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<CG>(tmem_slot, C::kTmemCols);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anything signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const AbortCtx ab{abort_flag, a.status, a.wait_limit_ns};
@@ -352,43 +370,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA producer
+            // ------------------------------------------------ TMA producer (every CTA)
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_phase = 0;
             bool ok = true;
             const uint64_t keep = policy_evict_last();
-            for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+            for (int tile = first_tile; ok && tile < a.num_tiles; tile += tile_stride) {
                 int mb, nb;
                 tile_coords(tile, a, mb, nb);
+                const int row_a = mb * kBM * CG + static_cast<int>(rank) * kBM;
+                const int col_b = nb * BN + static_cast<int>(rank) * C::kBLoad;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, ab)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                    uint32_t bar = smem_addr(&full[stage]);
+                    if constexpr (CG == 2) bar = map_to_rank(bar, 0);
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], CG * C::kStageBytes);
                     uint8_t* a_dst = sA + stage * C::kABytes;
                     uint8_t* b_dst = sB + stage * C::kBBytes;
                     const int k0 = kb * kBK;
-                    tma_load_2d_hint(a_dst, &tmap_dy, &full[stage], mb * kBM, k0, keep);
-                    tma_load_2d_hint(a_dst + kBK * 128, &tmap_dy, &full[stage], mb * kBM + 64, k0, keep);
+                    tma_load_2d_cg<CG>(a_dst, &tmap_dy, bar, row_a, k0, keep);
+                    tma_load_2d_cg<CG>(a_dst + kBK * 128, &tmap_dy, bar, row_a + 64, k0, keep);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d_hint(b_dst + j * kBK * 128, &tmap_x, &full[stage], nb * BN + 64 * j, k0, keep);
+                    for (int j = 0; j < C::kBLoad / 64; ++j)
+                        tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep);
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
-                for (int s = 0; s < C::kStages; ++s)
-                    if ((issued >> s) & 1u) drain_bounded(&full[s], (issued_phase >> s) & 1u, a.wait_limit_ns);
+                if (rank == 0) {
+                    for (int s = 0; s < C::kStages; ++s)
+                        if ((issued >> s) & 1u) drain_bounded(&full[s], (issued_phase >> s) & 1u, a.wait_limit_ns);
+                } else {
+                    // this CTA's copies complete on the peer's barrier, which it cannot wait on:
+                    // give copies in flight a grace period to land before teardown
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 200000ull) {
+                    }
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32_mn_major(kBM, BN);
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ MMA issuer (the even CTA of a pair)
+            constexpr uint32_t idesc = idesc_bf16_f32_mn_major(kBM * CG, BN);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued_any = false;
-            for (int tile = blockIdx.x; ok && tile < a.num_tiles; tile += gridDim.x) {
+            for (int tile = first_tile; ok && tile < a.num_tiles; tile += tile_stride) {
                 if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, ab)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -404,31 +434,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // (leading byte offset) and 8-token row groups 1024 bytes apart (stride).
                         const uint64_t ad = smem_desc_sw128(a_base + kk * 2048, kBK * 128, 1024);
                         const uint64_t bd = smem_desc_sw128(b_base + kk * 2048, kBK * 128, 1024);
-                        tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
-                    tc_commit(&empty[stage]);
+                    tc_commit_all<CG>(&empty[stage]);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit(&acc_full[acc]);
+                tc_commit_all<CG>(&acc_full[acc]);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (!ok && issued_any) {
-                tc_commit(drain);
+                tc_commit_local<CG>(drain);
                 drain_bounded(drain, 0, a.wait_limit_ns);
             }
         }
     } else {
-        // ---------------------------------------------------- epilogue warps
+        // ---------------------------------------------------- epilogue warps (every CTA)
         const int e = warp - 2;
         const int quarter = warp & 3;   // a warp may only touch TMEM lanes 32*(warp%4) .. +31
         const int half = e >> 2;
         constexpr int kWidth = BN / 2;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+        for (int tile = first_tile; tile < a.num_tiles; tile += tile_stride) {
             int mb, nb;
             tile_coords(tile, a, mb, nb);
             int ok = 1;
@@ -436,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int row0 = mb * kBM + quarter * 32;
+            const int row0 = mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
             const int col0 = nb * BN + half * kWidth;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + half * kWidth);
@@ -446,7 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             else epi_opt_int8<OPT, kWidth>(a, row0, col0, taddr);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) {
+                if constexpr (CG == 2) mbar_arrive_remote(map_to_rank(smem_addr(&acc_empty[acc]), 0));
+                else mbar_arrive(&acc_empty[acc]);
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -454,10 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    // a pair tears down together: the even CTA's MMAs read the odd CTA's shared memory and write
+    // its TMEM, and commits land on both CTAs' barriers
+    if constexpr (CG == 2) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc<CG>(tmem_base, C::kTmemCols);
     }
 }
 

@@ -34,7 +34,8 @@ def _layer(d_out, d_in, T, opt, seed=0, dy_std=1e-3, m_init="absnormal:1e-4", v_
 
 # ---------------------------------------------------------------------------- weight gradient
 
-@pytest.mark.parametrize("d_out, d_in, T", [(128, 128, 64), (512, 256, 256), (384, 640, 192)])
+@pytest.mark.parametrize("d_out, d_in, T", [(128, 128, 64), (512, 256, 256), (384, 640, 192), (384, 512, 128),
+                                            (768, 1024, 320)])
 def test_dw_gemm_matches_oracle(d_out, d_in, T):
     dy = normal_bf16((T, d_out), 1e-2, seed=d_out + T)
     x = normal_bf16((T, d_in), 1.0, seed=d_in + 7 * T)
@@ -72,7 +73,7 @@ def test_opt_step_matches_oracle_fp32(opt):
     e = np.arange(w.numel(), dtype=np.uint64).reshape(w.shape)
     ref = ostep.apply_update(opt, g, bits(w), None if m is None else f32(m), None if v is None else f32(v),
                              hp, t, 77, e)
-    assert_weights(bits(W), ref["W"])
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
     if m is not None:
         assert_moments(f32(M), ref["m"], "m")
     if v is not None:
@@ -104,7 +105,7 @@ def test_opt_step_matches_oracle_int8(opt):
     torch.cuda.synchronize()
     e = np.arange(w.numel(), dtype=np.uint64).reshape(w.shape)
     ref = ostep.apply_update(opt, g, bits(w), mq, vq, hp, 2, 3, e, "int8", ms, vs)
-    assert_weights(bits(W), ref["W"])
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
     q = Q.cpu().numpy()
     n64 = w.numel() // 64
     if ref["m"] is not None:
@@ -129,39 +130,45 @@ def test_tiny_workload_three_steps():
         fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, None, "adamw", hp, t, seed=0)
         ref = ostep.fused_step("adamw", bits(dy), bits(x), rw, rm, rv, hp, t, 0)
         torch.cuda.synchronize()
-        assert_weights(bits(W), ref["W"], f"W step {t}")
+        assert_weights(bits(W), ref["W"], f"W step {t}", w_old_bits=rw)
         assert_moments(f32(M), ref["m"], f"m step {t}")
         assert_moments(f32(V), ref["v"], f"v step {t}")
         rw, rm, rv = bits(W), f32(M), f32(V)  # continue from the GPU's state: per-step parity
 
 
-@pytest.mark.parametrize("opt, d_in", [(o, 256) for o in OPTIMIZERS] + [(o, 384) for o in ("adamw", "nadam", "sgd")])
-def test_fused_matches_oracle_every_optimizer(opt, d_in):
-    """d_in = 256 runs the 128 x 256 CTA tile, d_in = 384 the 128 x 128 one."""
-    dy, x, w, m, v = _layer(384, d_in, 192, opt, seed=2)
+# (d_out, d_in) -> tile shape: (512, 512) a CTA pair on 256 x 256; (384, 256) one CTA on 128 x 256;
+# (384, 384) one CTA on 128 x 128.
+SHAPES = [(512, 512), (384, 256), (384, 384)]
+
+
+@pytest.mark.parametrize("opt, d_out, d_in", [(o, 512, 512) for o in OPTIMIZERS] + [(o, 384, 256) for o in OPTIMIZERS]
+                         + [(o, 384, 384) for o in ("adamw", "nadam", "sgd")])
+def test_fused_matches_oracle_every_optimizer(opt, d_out, d_in):
+    dy, x, w, m, v = _layer(d_out, d_in, 192, opt, seed=2)
     hp = default_hparams(opt, lr=1e-3)
     W, M, V = dev(w), dev(m), dev(v)
     fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, None, opt, hp, 4, seed=11)
     torch.cuda.synchronize()
     ref = ostep.fused_step(opt, bits(dy), bits(x), bits(w), None if m is None else f32(m),
                            None if v is None else f32(v), hp, 4, 11)
-    assert_weights(bits(W), ref["W"])
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
     if m is not None:
         assert_moments(f32(M), ref["m"], "m")
     if v is not None:
         assert_moments(f32(V), ref["v"], "v")
 
 
-@pytest.mark.parametrize("opt, d_in", [(o, 384) for o in OPTIMIZERS if o != "sgd"] + [("adamw", 512), ("lion", 768)])
-def test_fused_int8_matches_oracle(opt, d_in):
-    dy, x, w, _, _ = _layer(256, d_in, 128, opt, seed=4)
+@pytest.mark.parametrize("opt, d_out, d_in", [(o, 256, 384) for o in OPTIMIZERS if o != "sgd"]
+                         + [(o, 256, 512) for o in OPTIMIZERS if o != "sgd"] + [("adamw", 384, 512), ("lion", 256, 768)])
+def test_fused_int8_matches_oracle(opt, d_out, d_in):
+    dy, x, w, _, _ = _layer(d_out, d_in, 128, opt, seed=4)
     mq, ms, vq, vs = _int8_state(w.shape, 9)
     hp = default_hparams(opt, lr=1e-3)
     W, M, V, Q = dev(w), torch.from_numpy(mq).cuda(), torch.from_numpy(vq).cuda(), _qscales_tensor(ms, vs)
     fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, Q, opt, hp, 5, seed=12)
     torch.cuda.synchronize()
     ref = ostep.fused_step(opt, bits(dy), bits(x), bits(w), mq, vq, hp, 5, 12, "int8", ms, vs)
-    assert_weights(bits(W), ref["W"])
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
     q = Q.cpu().numpy()
     n64 = w.numel() // 64
     if ref["m"] is not None:
@@ -172,11 +179,12 @@ def test_fused_int8_matches_oracle(opt, d_in):
         assert_moments(q[n64:], ref["v_scales"].ravel(), "v scales")
 
 
-@pytest.mark.parametrize("opt", ["adamw", "lion", "adagrad"])
-def test_fused_equals_unfused_bitwise(opt):
+@pytest.mark.parametrize("opt, d_out, d_in", [(o, d_out, d_in) for o in ("adamw", "lion", "adagrad")
+                                               for d_out, d_in in SHAPES])
+def test_fused_equals_unfused_bitwise(opt, d_out, d_in):
     """The summary's exactness statement on the GPU: same mainloop order, so the fused step and
     the two-phase step (dW to memory, then the optimizer) give identical bits."""
-    dy, x, w, m, v = _layer(512, 384, 256, opt, seed=6)
+    dy, x, w, m, v = _layer(d_out, d_in, 256, opt, seed=6)
     hp = default_hparams(opt, lr=1e-3)
     W1, M1, V1 = dev(w), dev(m), dev(v)
     W2, M2, V2 = dev(w), dev(m), dev(v)
@@ -193,17 +201,17 @@ def test_fused_equals_unfused_bitwise(opt):
         assert torch.equal(V1, V2)
 
 
-@pytest.mark.parametrize("d_in", [2560, 1408])
-def test_many_tiles_with_a_ragged_persistent_tail(d_in):
-    """More CTA tiles than SMs, not a multiple of them: 160 tiles of 128 x 256 (d_in = 2560) or
-    176 tiles of 128 x 128 (d_in = 1408, not a multiple of 256)."""
-    dy, x, w, m, v = _layer(2048, d_in, 128, "adamw", seed=8)
+@pytest.mark.parametrize("d_out, d_in", [(2048, 2560), (2176, 2560), (2048, 1408)])
+def test_many_tiles_with_a_ragged_persistent_tail(d_out, d_in):
+    """More tiles than resident CTAs (or CTA pairs), not a multiple of them: 80 pair tiles of
+    256 x 256; 170 tiles of 128 x 256 (d_out not a multiple of 256); 176 tiles of 128 x 128."""
+    dy, x, w, m, v = _layer(d_out, d_in, 128, "adamw", seed=8)
     hp = default_hparams("adamw", lr=1e-3)
     W, M, V = dev(w), dev(m), dev(v)
     fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, None, "adamw", hp, 7, seed=21)
     torch.cuda.synchronize()
     ref = ostep.fused_step("adamw", bits(dy), bits(x), bits(w), f32(m), f32(v), hp, 7, 21)
-    assert_weights(bits(W), ref["W"])
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
     assert_moments(f32(M), ref["m"], "m")
     assert_moments(f32(V), ref["v"], "v")
 
@@ -218,7 +226,7 @@ def test_zero_tokens_is_a_zero_gradient_step():
     torch.cuda.synchronize()
     e = np.arange(w.numel(), dtype=np.uint64).reshape(w.shape)
     ref = ostep.apply_update("adamw", np.zeros(w.shape, np.float32), bits(w), f32(m), f32(v), hp, 3, 1, e)
-    assert_weights(bits(W), ref["W"])
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
     assert_moments(f32(M), ref["m"])
     assert_moments(f32(V), ref["v"])
 
