@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
     L.forge_sync_status.restype = ctypes.c_int
     L.forge_set_wait_limit_ns.argtypes = [u64]
     L.forge_set_wait_limit_ns.restype = None
+    L.forge_debug_withhold_next_stage.argtypes = []
+    L.forge_debug_withhold_next_stage.restype = None
     L.forge_launch_count.argtypes = []
     L.forge_launch_count.restype = u64
     L.forge_status_string.argtypes = [ctypes.c_int]
@@ -191,3 +193,8 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def launch_count() -> int:
     return int(lib().forge_launch_count())
+
+
+def debug_withhold_next_stage() -> None:
+    """Test switch: the next fused launch withholds one pipeline stage so a bounded wait runs out."""
+    lib().forge_debug_withhold_next_stage()

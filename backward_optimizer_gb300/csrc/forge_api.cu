@@ -26,6 +26,7 @@ using forge::OptScalars;
 constexpr int kMaxDevices = 64;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_withhold_next{0};  // test switch, consumed by the next fused launch
 
 struct DeviceInfo {
     bool ready = false;
@@ -303,6 +304,7 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.step = static_cast<uint64_t>(step);
     a.status = dev.status;
     a.wait_limit_ns = g_wait_limit_ns.load();
+    a.withhold_first_stage = epi == forge::kEpiStoreGrad ? 0 : g_withhold_next.exchange(0);
 
     forge::TileLaunch l;
     forge_status st = make_operand_map(&l.tmap_dy, dY, shape->d_out, shape->T);
@@ -390,6 +392,8 @@ forge_status forge_sync_status(struct CUstream_st* stream) {
 }
 
 void forge_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns < 1000000ull ? 1000000ull : ns); }
+
+void forge_debug_withhold_next_stage(void) { g_withhold_next.store(1); }
 
 uint64_t forge_launch_count(void) { return g_launches.load(); }
 

@@ -75,6 +75,7 @@ struct TileArgs {
     uint64_t seed, step;
     int* status;                  // device status word
     uint64_t wait_limit_ns;
+    int withhold_first_stage;     // test switch: the producer skips the first stage, so a wait runs out
 };
 
 // ---------------------------------------------------------------- bounded waits
@@ -382,6 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int col_b = nb * BN + static_cast<int>(rank) * C::kBLoad;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, ab)) { ok = false; break; }
+                    if (a.withhold_first_stage && rank == 0 && tile == first_tile && kb == 0) {
+                        // test switch: never fill this stage, so the MMA thread's wait for it runs out
+                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     uint32_t bar = smem_addr(&full[stage]);
                     if constexpr (CG == 2) bar = map_to_rank(bar, 0);
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], CG * C::kStageBytes);

@@ -164,6 +164,14 @@ FORGE_API forge_status forge_sync_status(struct CUstream_st *stream);
  * Values below 1e6 are raised to 1e6.  Host-side setting, applies to later launches. */
 FORGE_API void forge_set_wait_limit_ns(uint64_t ns);
 
+/* Test switch for the failure-detection path (the method has no counterpart; it exists so that
+ * the bounded waits can be exercised without a real fault).  The next forge_fused_dw_step launch
+ * with T > 0 withholds the first pipeline stage of its first tile: the MMA thread's wait for that
+ * stage runs out after the wait limit, the kernel records FORGE_ERR_TIMEOUT, stops every other
+ * wait, frees its TMEM and returns; forge_sync_status() then reports FORGE_ERR_TIMEOUT and the
+ * CUDA context stays usable.  The outputs of that one call are unspecified.  No fault is raised. */
+FORGE_API void forge_debug_withhold_next_stage(void);
+
 /* Number of the library's own kernel launches queued since load (all entry points). */
 FORGE_API uint64_t forge_launch_count(void);
 

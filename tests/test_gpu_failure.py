@@ -1,0 +1,56 @@
+"""Failure detection on the GPU without a fault: a bounded wait is made to run out (the producer
+withholds one pipeline stage that nothing else will fill), the kernel reports FORGE_ERR_TIMEOUT
+through the device status word and returns, and the context stays usable (needs a GB300)."""
+import numpy as np
+import pytest
+import torch
+
+import backward_optimizer_gb300 as fg
+from oracle import step as ostep
+from tests.compare import assert_moments, assert_weights
+from tests.helpers import bits, f32
+from workloads import Layer, Workload, activations, default_hparams, layer_state
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT = 6  # FORGE_ERR_TIMEOUT
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fg.build()
+    fg.lib()
+    assert fg.sync_status() == 0
+    fg.set_wait_limit_ns(50_000_000)  # 50 ms
+    yield
+    fg.set_wait_limit_ns(2_000_000_000)
+    fg.sync_status()
+
+
+def _layer(d_out, d_in, T):
+    wl = Workload("t", (Layer("w", d_out, d_in),), T, 1.0, 1e-3, m_init="absnormal:1e-4", v_init="uniform:1e-6")
+    dy, x = activations(wl, 0, 1, 3)
+    w, m, v = layer_state(wl, 0, "adamw", 3)
+    return dy, x, w, m, v
+
+
+# (512, 512): CTA pair; (384, 256): one CTA, 128 x 256; (384, 384): one CTA, 128 x 128
+@pytest.mark.parametrize("d_out, d_in", [(512, 512), (384, 256), (384, 384)])
+def test_withheld_stage_times_out_and_context_survives(d_out, d_in):
+    dy, x, w, m, v = _layer(d_out, d_in, 512)
+    hp = default_hparams("adamw", lr=1e-3)
+    D, X = dy.cuda(), x.cuda()
+    fg.debug_withhold_next_stage()
+    fg.fused_dw_step(D, X, w.cuda(), m.cuda(), v.cuda(), None, "adamw", hp, 2, seed=1)
+    assert fg.sync_status() == TIMEOUT
+    assert fg.sync_status() == 0  # the status word was cleared by the read
+    # the next call on the same context is complete and correct
+    W, M, V = w.cuda(), m.cuda(), v.cuda()
+    fg.fused_dw_step(D, X, W, M, V, None, "adamw", hp, 2, seed=1)
+    assert fg.sync_status() == 0
+    ref = ostep.fused_step("adamw", bits(dy), bits(x), bits(w), f32(m), f32(v), hp, 2, 1)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    assert_moments(f32(M), ref["m"], "m")
+    assert_moments(f32(V), ref["v"], "v")
