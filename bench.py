@@ -124,10 +124,21 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------ GPU arm
 
-def _make_layer(wl, i, opt, state, device, seed):
+def _act_key(wl, i):
+    """Activation buffer of layer i: its own for small workloads; for a many-layer sweep one dY/X
+    buffer per distinct layer shape, shared by the layers of that shape."""
+    l = wl.layers[i]
+    return (l.d_out, l.d_in) if len(wl.layers) > 8 else i
+
+
+def _make_layer(wl, i, opt, state, device, seed, act_cache):
+    """One layer's W/m/v (its own) and dY/X (see _act_key)."""
     import torch
     from workloads import activations, layer_state
-    dy, x = activations(wl, i, 1, seed, device=device)
+    key = _act_key(wl, i)
+    if key not in act_cache:
+        act_cache[key] = activations(wl, i, 1, seed, device=device)
+    dy, x = act_cache[key]
     w, m, v = layer_state(wl, i, opt, seed, device=device)
     q = None
     if state == "int8":
@@ -150,7 +161,8 @@ def run_gpu(args, rank, world):
     wl = WORKLOADS[args.workload]
     hp = default_hparams(args.opt)
     t_step = wl.steps[-1]
-    layers = [_make_layer(wl, i, args.opt, args.state, dev, seed=1000 * rank) for i in range(len(wl.layers))]
+    act_cache = {}
+    layers = [_make_layer(wl, i, args.opt, args.state, dev, 1000 * rank, act_cache) for i in range(len(wl.layers))]
     stream = torch.cuda.current_stream()
     flops_step = wl.flops_per_step()
 
@@ -222,8 +234,12 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
 
     # ---- end to end: dY/X from pinned host memory each step, updated W copied back
-    host_in = [(L["dy"].cpu().pin_memory(), L["x"].cpu().pin_memory()) for L in layers]
-    host_out = [torch.empty(L["w"].shape, dtype=L["w"].dtype).pin_memory() for L in layers]
+    # (one pinned host copy per distinct layer shape; every layer's dY/X is copied in each step)
+    host_act = {k: (dy.cpu().pin_memory(), x.cpu().pin_memory()) for k, (dy, x) in act_cache.items()}
+    host_in = [host_act[_act_key(wl, i)] for i in range(len(wl.layers))]
+    out_by_key = {k: torch.empty((dy.shape[1], x.shape[1]), dtype=torch.bfloat16).pin_memory()
+                  for k, (dy, x) in act_cache.items()}
+    host_out = [out_by_key[_act_key(wl, i)] for i in range(len(wl.layers))]
     h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
 
@@ -261,35 +277,51 @@ def run_gpu(args, rank, world):
 
 # ------------------------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(workload: str, opt: str, rows: int, seed: int = 0):
-    """Time the oracle's whole step on the first `rows` weight rows of every layer (a bounded
-    sample of the workload).  Returns (flops done, seconds)."""
-    import numpy as np
-    from oracle import step as ostep
-    from tests.helpers import bits, f32
-    from workloads import WORKLOADS, activations, default_hparams, layer_state
+class OracleSample:
+    """The CPU oracle's whole step (float64 dW, optimizer, Philox + stochastic rounding) timed on
+    the first `rows` weight rows of the workload's first three layers: a bounded sample of the
+    same workload.  Inputs are generated once."""
 
-    wl = WORKLOADS[workload]
-    hp = default_hparams(opt)
-    flops, secs = 0, 0.0
-    for i, l in enumerate(wl.layers[:3]):
-        r = min(rows, l.d_out)
-        dy, x = activations(wl, i, 1, seed)
-        w, m, v = layer_state(wl, i, opt, seed)
-        dyb, xb, wb = bits(dy)[:, :r], bits(x), bits(w)[:r]
-        mm = None if m is None else f32(m)[:r]
-        vv = None if v is None else f32(v)[:r]
-        t0 = time.perf_counter()
-        ostep.fused_step(opt, np.ascontiguousarray(dyb), xb, np.ascontiguousarray(wb), mm, vv, hp, wl.steps[-1], 1 + i)
-        secs += time.perf_counter() - t0
-        flops += 2 * wl.T * r * l.d_in
-    return flops, secs
+    def __init__(self, workload: str, opt: str, seed: int = 0):
+        from tests.helpers import bits, f32
+        from workloads import WORKLOADS, activations, default_hparams, layer_state
+        self.wl = WORKLOADS[workload]
+        self.opt = opt
+        self.hp = default_hparams(opt)
+        self.layers = []
+        for i, l in enumerate(self.wl.layers[:3]):
+            dy, x = activations(self.wl, i, 1, seed)
+            w, m, v = layer_state(self.wl, i, opt, seed)
+            self.layers.append((l, bits(dy), bits(x), bits(w), None if m is None else f32(m),
+                                None if v is None else f32(v)))
+
+    def run(self, rows: int):
+        """Returns (flops done, seconds) for one sampled step of `rows` rows per layer."""
+        import numpy as np
+        from oracle import step as ostep
+        flops, secs = 0, 0.0
+        for i, (l, dyb, xb, wb, m, v) in enumerate(self.layers):
+            r = min(rows, l.d_out)
+            args = (np.ascontiguousarray(dyb[:, :r]), xb, np.ascontiguousarray(wb[:r]),
+                    None if m is None else m[:r], None if v is None else v[:r])
+            t0 = time.perf_counter()
+            ostep.fused_step(self.opt, *args, self.hp, self.wl.steps[-1], 1 + i)
+            secs += time.perf_counter() - t0
+            flops += 2 * self.wl.T * r * l.d_in
+        return flops, secs
+
+    def rows_for(self, seconds: float) -> int:
+        """Sample size (a multiple of 128 rows, 128 .. 4096) whose step takes about `seconds`."""
+        f, s = self.run(128)
+        return int(min(4096, max(128, 128 * int(seconds / max(s, 1e-6)))))
 
 
 def cpu_baseline(args):
-    flops, secs = oracle_sample(args.workload, args.opt, args.oracle_rows)
+    sample = OracleSample(args.workload, args.opt)
+    rows = sample.rows_for(15.0) if args.oracle_rows <= 0 else args.oracle_rows
+    flops, secs = sample.run(rows)
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"first {args.oracle_rows} weight rows of each of the first 3 layers of {args.workload} "
+            "sample": f"first {rows} weight rows of each of the first 3 layers of {args.workload} "
                       f"(float64 NumPy oracle, whole step incl. Philox/SR), {secs:.1f} s"}
 
 
@@ -304,7 +336,7 @@ def main():
     ap.add_argument("--workload", default="llama8b-mlp")
     ap.add_argument("--opt", default="adamw")
     ap.add_argument("--state", default="fp32", choices=["fp32", "int8"])
-    ap.add_argument("--oracle-rows", type=int, default=4096)
+    ap.add_argument("--oracle-rows", type=int, default=0, help="rows per layer of the oracle sample (0: sized by time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -323,17 +355,24 @@ def main():
         if rank != 0:
             return
         t0 = time.perf_counter()
+        sample = OracleSample(args.workload, args.opt)
+        # whole --steps/--warmup run within ~2 minutes of oracle time
+        rows = sample.rows_for(120.0 / (args.steps + args.warmup)) if args.oracle_rows <= 0 else args.oracle_rows
         vals = []
         for _ in range(args.warmup + args.steps):
-            flops, secs = oracle_sample(args.workload, args.opt, args.oracle_rows)
+            flops, secs = sample.run(rows)
             vals.append(flops / secs / 1e12)
         vals = vals[args.warmup:]
         v = statistics.median(vals)
+        flops_step = wl.flops_per_step()
         line = {"impl": "reference", "metric": metric, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": flops_step / (v * 1e12) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": dict(config, ms_per_step="extrapolated to the full step at the "
+                                                                        "oracle's measured rate"),
                 "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                                 "sample": f"first {args.oracle_rows} rows of each of 3 layers per step"},
+                                 "sample": f"first {rows} weight rows of each of the first 3 layers per step "
+                                           f"(float64 NumPy oracle, whole step incl. Philox/SR)"},
                 "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "wall_s": time.perf_counter() - t0}
         print(json.dumps(line))
@@ -367,7 +406,7 @@ def main():
         "unfused": {"ms_per_step": r["unfused_ms"], "value": world * r["flops_step"] / (r["unfused_ms"] * 1e-3) / 1e12,
                     "speedup_fused": r["unfused_ms"] / r["ms_step"]},
         "grad_pool_bytes": {"fused_hbm": 0, "unfused_hbm": r["grad_pool_unfused"],
-                            "fused_on_chip": "2 TMEM accumulators x 128x128 FP32 per SM (128 KiB)"},
+                            "fused_on_chip": "two FP32 accumulators per SM in TMEM (at most 2 x 128x256 = 256 KiB), independent of model size"},
         "e2e": {"value": world * r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
