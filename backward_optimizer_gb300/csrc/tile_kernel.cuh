@@ -50,7 +50,8 @@ struct TileCfg {
     static constexpr int kBBytes = kBLoad * kBK * 2;  // one stage of X: kBLoad/64 boxes of [64 tokens][64 cols]
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator (128 lanes x BN)
-    static constexpr int kStripBytes = 32 * 32 * 4;  // one warp's 32 x 32 FP32 transpose strip
+    // one warp's 32 x 32 FP32 transpose strip; the INT8 epilogue stages two (a 64-column block)
+    static constexpr int kStripBytes = (EPI == kEpiOptINT8 ? 2 : 1) * 32 * 32 * 4;
     static constexpr int kEpiBytes = kNumEpiWarps * kStripBytes;
     static constexpr int kBarrierBytes = 256;
     static constexpr int kMaxSmem = 232448;
@@ -159,6 +160,32 @@ __device__ __forceinline__ void strip_transpose(uint32_t taddr, uint8_t* strip, 
     __syncwarp();  // the strip may be overwritten by the next call
 }
 
+// The two halves of strip_transpose, for callers that consume one row group at a time: the strip
+// is written once, then lane l reads the 8 columns it owns of row (l div 4) + 8k.
+__device__ __forceinline__ void strip_store(uint32_t taddr, uint8_t* strip) {
+    const uint32_t lane = threadIdx.x & 31u;
+    uint32_t g[32];
+    tmem_ld_32x32b_x32(taddr, g);
+    tmem_ld_wait(g);
+    const uint32_t base = smem_addr(strip);
+    __syncwarp();  // earlier reads of the strip are complete
+#pragma unroll
+    for (uint32_t j = 0; j < 8; ++j)
+        st_shared_v4(base + lane * 128u + ((j ^ (lane & 7u)) << 4), g[4 * j], g[4 * j + 1], g[4 * j + 2],
+                     g[4 * j + 3]);
+    __syncwarp();
+}
+
+__device__ __forceinline__ void strip_load_row(const uint8_t* strip, int k, uint32_t (&out)[8]) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t sub_row = lane >> 2;
+    const uint32_t r = sub_row + 8u * static_cast<uint32_t>(k);
+    const uint32_t base = smem_addr(strip);
+#pragma unroll
+    for (uint32_t h = 0; h < 2; ++h)
+        ld_shared_v4(base + r * 128u + (((2u * (lane & 3u) + h) ^ sub_row) << 4), &out[4 * h]);
+}
+
 template <int WIDTH>
 __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int col0, uint32_t taddr,
                                                uint8_t* strip) {
@@ -218,91 +245,107 @@ __device__ __forceinline__ void epi_opt_fp32(const TileArgs& a, int row0, int co
     }
 }
 
-// INT8 moments: one 64-column block per step, entirely in this thread's row, so the block's
-// absmax needs no cross-thread reduction.  Pass 1 computes the new moments and their absmax;
-// pass 2 reloads the gradient from TMEM, recomputes the same moments bit for bit, updates the
-// weight with the unquantised moments and writes the codes under the new scales.
-template <int OPT, int WIDTH>
-__device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int col0, uint32_t taddr) {
-    const int row = row0 + static_cast<int>(threadIdx.x & 31);
+// INT8 moments, on the transposed ownership of strip_transpose.  For each group of 64 columns (one
+// quantisation block per row) the warp stages both 32-column gradient strips; lane l then owns 8
+// consecutive columns in each half of rows (l div 4) + 8k, and the 4 lanes 4q .. 4q+3 together
+// hold each of those rows' 64-element block, so a block's absmax takes two shuffles.  Rows are
+// handled one at a time (the next row's W, codes and scales are loaded while the current one is
+// computed): pass 1 computes the row block's new moments and absmax, pass 2 recomputes the same
+// moments bit for bit, updates the weight with the unquantised moments and writes the codes under
+// the new scales.
+template <int OPT>
+struct Int8RowIn {
+    uint32_t w[2][4];   // 2 halves x 8 bf16
+    uint32_t mq[2][2];  // 2 halves x 8 codes
+    uint32_t vq[2][2];
+    float ms, vs;
+};
+
+template <int OPT>
+__device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e_row, Int8RowIn<OPT>& in) {
     using Tr = OptTraits<OPT>;
-    const size_t row_base = static_cast<size_t>(row) * a.d_in + col0;
-    int8_t* mp = static_cast<int8_t*>(a.m);
-    int8_t* vp = static_cast<int8_t*>(a.v);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        ld_cs_v4(a.W + e_row + 32 * h, in.w[h]);
+        if constexpr (Tr::kM) ld_cs_v2(static_cast<int8_t*>(a.m) + e_row + 32 * h, in.mq[h]);
+        if constexpr (Tr::kV) ld_cs_v2(static_cast<int8_t*>(a.v) + e_row + 32 * h, in.vq[h]);
+    }
+    in.ms = Tr::kM ? a.m_scales[e_row >> 6] : 0.f;
+    in.vs = Tr::kV ? a.v_scales[e_row >> 6] : 0.f;
+}
+
+template <int OPT>
+__device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row, const uint8_t* strip, int k,
+                                                Int8RowIn<OPT>& in) {
+    using Tr = OptTraits<OPT>;
+    // pass 1: absmax of the row block's new moments
+    float am = 0.f, av = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t g[8];
+        strip_load_row(strip + h * 4096, k, g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
+            float mm = Tr::kM ? __fmul_rn(int8_at(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
+            float vv = Tr::kV ? __fmul_rn(int8_at(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
+            opt_moments<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
+            am = fmaxf(am, fabsf(mm));
+            av = fmaxf(av, fabsf(vv));
+        }
+    }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
+        av = fmaxf(av, __shfl_xor_sync(0xFFFFFFFFu, av, off));
+    }
+    const float nms = __fdiv_rn(am, 127.0f), nvs = __fdiv_rn(av, 127.0f);
+    // pass 2: update, round, requantise, store
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t g[8];
+        strip_load_row(strip + h * 4096, k, g);
+        const size_t e = e_row + 32 * h;
+        const Philox4 p = sr_words(e >> 3, a.seed, a.step);
+        uint32_t mo[2] = {0u, 0u}, vo[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
+            float mm = Tr::kM ? __fmul_rn(int8_at(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
+            float vv = Tr::kV ? __fmul_rn(int8_at(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
+            const float wn = opt_update<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
+            const uint32_t b = sr_bf16(wn, sr_r16(p, j));
+            in.w[h][j >> 1] = (j & 1) ? ((in.w[h][j >> 1] & 0xFFFFu) | (b << 16)) : ((in.w[h][j >> 1] & 0xFFFF0000u) | b);
+            if constexpr (Tr::kM) mo[j >> 2] |= int8_code(mm, nms) << (8 * (j & 3));
+            if constexpr (Tr::kV) vo[j >> 2] |= int8_code(vv, nvs) << (8 * (j & 3));
+        }
+        st_cs_v4(a.W + e, in.w[h]);
+        if constexpr (Tr::kM) st_cs_v2(static_cast<int8_t*>(a.m) + e, mo);
+        if constexpr (Tr::kV) st_cs_v2(static_cast<int8_t*>(a.v) + e, vo);
+    }
+    if ((threadIdx.x & 3u) == 0) {
+        if constexpr (Tr::kM) a.m_scales[e_row >> 6] = nms;
+        if constexpr (Tr::kV) a.v_scales[e_row >> 6] = nvs;
+    }
+}
+
+template <int OPT, int WIDTH>
+__device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int col0, uint32_t taddr,
+                                             uint8_t* strip) {
+    static_assert(WIDTH % 64 == 0, "whole quantisation blocks");
+    const int lane = threadIdx.x & 31;
+    const size_t lane_base = static_cast<size_t>(row0 + (lane >> 2)) * a.d_in + col0 + 8 * (lane & 3);
+    const size_t row_step = static_cast<size_t>(8) * a.d_in;
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 64) {
-        const size_t e0 = row_base + c;
-        const size_t blk = e0 >> 6;
-        uint32_t w[32], mq[16], vq[16];
+        Int8RowIn<OPT> in[2];
+        int8_row_load<OPT>(a, lane_base + c, in[0]);
+        strip_store(taddr + c, strip);
+        strip_store(taddr + c + 32, strip + 4096);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ld_cs_v8(a.W + e0 + 16 * q, *reinterpret_cast<uint32_t(*)[8]>(&w[8 * q]));
-        float ms = 0.f, vs = 0.f;
-        if constexpr (Tr::kM) {
-            ld_cs_v8(mp + e0, *reinterpret_cast<uint32_t(*)[8]>(&mq[0]));
-            ld_cs_v8(mp + e0 + 32, *reinterpret_cast<uint32_t(*)[8]>(&mq[8]));
-            ms = a.m_scales[blk];
-        }
-        if constexpr (Tr::kV) {
-            ld_cs_v8(vp + e0, *reinterpret_cast<uint32_t(*)[8]>(&vq[0]));
-            ld_cs_v8(vp + e0 + 32, *reinterpret_cast<uint32_t(*)[8]>(&vq[8]));
-            vs = a.v_scales[blk];
-        }
-        // pass 1: absmax of the new moments
-        float am = 0.f, av = 0.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t g[32];
-            tmem_ld_32x32b_x32(taddr + c + 32 * h, g);
-            tmem_ld_wait(g);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int i = 32 * h + j;
-                const float wf = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
-                float mm = Tr::kM ? __fmul_rn(int8_at(mq[i >> 2], i & 3), ms) : 0.f;
-                float vv = Tr::kV ? __fmul_rn(int8_at(vq[i >> 2], i & 3), vs) : 0.f;
-                opt_moments<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
-                am = fmaxf(am, fabsf(mm));
-                av = fmaxf(av, fabsf(vv));
-            }
-        }
-        const float nms = __fdiv_rn(am, 127.0f), nvs = __fdiv_rn(av, 127.0f);
-        // pass 2: update, round, requantise
-        uint32_t mo[16], vo[16];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t g[32];
-            tmem_ld_32x32b_x32(taddr + c + 32 * h, g);
-            tmem_ld_wait(g);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const Philox4 p = sr_words((e0 >> 3) + 4 * h + q, a.seed, a.step);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int i = 32 * h + 8 * q + j;
-                    const float wf = (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
-                    float mm = Tr::kM ? __fmul_rn(int8_at(mq[i >> 2], i & 3), ms) : 0.f;
-                    float vv = Tr::kV ? __fmul_rn(int8_at(vq[i >> 2], i & 3), vs) : 0.f;
-                    const float wn = opt_update<OPT>(__uint_as_float(g[8 * q + j]), wf, mm, vv, a.s);
-                    const uint32_t b = sr_bf16(wn, sr_r16(p, j));
-                    w[i >> 1] = (i & 1) ? ((w[i >> 1] & 0xFFFFu) | (b << 16)) : ((w[i >> 1] & 0xFFFF0000u) | b);
-                    const uint32_t cm = Tr::kM ? int8_code(mm, nms) : 0u;
-                    const uint32_t cv = Tr::kV ? int8_code(vv, nvs) : 0u;
-                    if ((i & 3) == 0) { mo[i >> 2] = cm; vo[i >> 2] = cv; }
-                    else { mo[i >> 2] |= cm << (8 * (i & 3)); vo[i >> 2] |= cv << (8 * (i & 3)); }
-                }
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) st_cs_v8(a.W + e0 + 16 * q, *reinterpret_cast<uint32_t(*)[8]>(&w[8 * q]));
-        if constexpr (Tr::kM) {
-            st_cs_v8(mp + e0, *reinterpret_cast<uint32_t(*)[8]>(&mo[0]));
-            st_cs_v8(mp + e0 + 32, *reinterpret_cast<uint32_t(*)[8]>(&mo[8]));
-            a.m_scales[blk] = nms;
-        }
-        if constexpr (Tr::kV) {
-            st_cs_v8(vp + e0, *reinterpret_cast<uint32_t(*)[8]>(&vo[0]));
-            st_cs_v8(vp + e0 + 32, *reinterpret_cast<uint32_t(*)[8]>(&vo[8]));
-            a.v_scales[blk] = nvs;
+        for (int k = 0; k < 4; ++k) {
+            if (k < 3) int8_row_load<OPT>(a, lane_base + (k + 1) * row_step + c, in[(k + 1) & 1]);
+            int8_row_update<OPT>(a, lane_base + k * row_step + c, strip, k, in[k & 1]);
         }
     }
 }
@@ -479,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* strip = strips + e * C::kStripBytes;
             if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth>(a, row0, col0, taddr, strip);
             else if constexpr (EPI == kEpiOptFP32) epi_opt_fp32<OPT, kWidth>(a, row0, col0, taddr, strip);
-            else epi_opt_int8<OPT, kWidth>(a, row0, col0, taddr);
+            else epi_opt_int8<OPT, kWidth>(a, row0, col0, taddr, strip);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
