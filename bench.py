@@ -122,6 +122,24 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------------------------ ranks
+
+def max_over_ranks(values, world: int, device="cpu"):
+    """Element-wise maximum of per-rank timings (the slowest rank defines the job's time).  The
+    only collective of the benchmark besides barriers; no data of the path is exchanged."""
+    import torch
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s under weak scaling: every rank does the same per-GPU work."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------------------------ GPU arm
 
 def _act_key(wl, i):
@@ -263,12 +281,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
-    # ---- max over ranks
-    times = torch.tensor([elapsed_ms, unfused_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms, unfused_ms, e2e_ms = times.tolist()
+    elapsed_ms, unfused_ms, e2e_ms = max_over_ranks([elapsed_ms, unfused_ms, e2e_ms], world, dev)
     ms_step = elapsed_ms / args.steps
     return dict(ms_step=ms_step, flops_step=flops_step, launch_ms=launch_ms, launches=launches,
                 unfused_ms=unfused_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks.summary(),
@@ -398,16 +411,16 @@ def main():
     avg_launch_ms = statistics.mean(r["launch_ms"])
     flops_launch = r["flops_step"] / n_layers
     achieved = flops_launch / (avg_launch_ms * 1e-3) / 1e12
-    value = world * r["flops_step"] / (r["ms_step"] * 1e-3) / 1e12
+    value = job_throughput(r["flops_step"], world, r["ms_step"])
     line = {
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
-        "unfused": {"ms_per_step": r["unfused_ms"], "value": world * r["flops_step"] / (r["unfused_ms"] * 1e-3) / 1e12,
+        "unfused": {"ms_per_step": r["unfused_ms"], "value": job_throughput(r["flops_step"], world, r["unfused_ms"]),
                     "speedup_fused": r["unfused_ms"] / r["ms_step"]},
         "grad_pool_bytes": {"fused_hbm": 0, "unfused_hbm": r["grad_pool_unfused"],
                             "fused_on_chip": "two FP32 accumulators per SM in TMEM (at most 2 x 128x256 = 256 KiB), independent of model size"},
-        "e2e": {"value": world * r["flops_step"] / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_throughput(r["flops_step"], world, r["e2e_ms"]), "unit": "TFLOP/s",
                 "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
