@@ -93,6 +93,9 @@ def lib() -> ctypes.CDLL:
     L.forge_set_wait_limit_ns.restype = None
     L.forge_debug_withhold_next_stage.argtypes = []
     L.forge_debug_withhold_next_stage.restype = None
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    L.forge_launch_shape.argtypes = [ctypes.POINTER(ForgeShape), i32p, i32p, i32p, i32p]
+    L.forge_launch_shape.restype = ctypes.c_int
     L.forge_launch_count.argtypes = []
     L.forge_launch_count.restype = u64
     L.forge_status_string.argtypes = [ctypes.c_int]
@@ -193,6 +196,14 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def launch_count() -> int:
     return int(lib().forge_launch_count())
+
+
+def launch_shape(d_out: int, d_in: int, T: int = 64) -> dict:
+    """Tile rows x columns, cluster size and CTA count the fused step uses for a layer."""
+    vals = [ctypes.c_int32() for _ in range(4)]
+    _check(lib().forge_launch_shape(ctypes.byref(_shape(T, d_out, d_in, STATE_FP32)), *[ctypes.byref(v) for v in vals]),
+           "forge_launch_shape")
+    return dict(zip(("tile_rows", "tile_cols", "cluster", "ctas"), (v.value for v in vals)))
 
 
 def debug_withhold_next_stage() -> None:

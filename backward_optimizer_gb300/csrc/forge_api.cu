@@ -190,50 +190,57 @@ forge_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : F
 using TileFn = cudaError_t (*)(const forge::TileLaunch&);
 using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
 
-template <int BN, int CG>
+template <int BN, int CL>
 TileFn tile_fn_v(forge_opt_kind k, bool int8) {
     using namespace forge;
     switch (k) {
         case FORGE_ADAMW:
-            return int8 ? launch_tile<kAdamW, kEpiOptINT8, BN, CG> : launch_tile<kAdamW, kEpiOptFP32, BN, CG>;
+            return int8 ? launch_tile<kAdamW, kEpiOptINT8, BN, CL> : launch_tile<kAdamW, kEpiOptFP32, BN, CL>;
         case FORGE_NADAM:
-            return int8 ? launch_tile<kNAdam, kEpiOptINT8, BN, CG> : launch_tile<kNAdam, kEpiOptFP32, BN, CG>;
+            return int8 ? launch_tile<kNAdam, kEpiOptINT8, BN, CL> : launch_tile<kNAdam, kEpiOptFP32, BN, CL>;
         case FORGE_RADAM:
-            return int8 ? launch_tile<kRAdam, kEpiOptINT8, BN, CG> : launch_tile<kRAdam, kEpiOptFP32, BN, CG>;
+            return int8 ? launch_tile<kRAdam, kEpiOptINT8, BN, CL> : launch_tile<kRAdam, kEpiOptFP32, BN, CL>;
         case FORGE_LION:
-            return int8 ? launch_tile<kLion, kEpiOptINT8, BN, CG> : launch_tile<kLion, kEpiOptFP32, BN, CG>;
+            return int8 ? launch_tile<kLion, kEpiOptINT8, BN, CL> : launch_tile<kLion, kEpiOptFP32, BN, CL>;
         case FORGE_RMSPROP:
-            return int8 ? launch_tile<kRMSprop, kEpiOptINT8, BN, CG> : launch_tile<kRMSprop, kEpiOptFP32, BN, CG>;
+            return int8 ? launch_tile<kRMSprop, kEpiOptINT8, BN, CL> : launch_tile<kRMSprop, kEpiOptFP32, BN, CL>;
         case FORGE_ADAGRAD:
-            return int8 ? launch_tile<kAdaGrad, kEpiOptINT8, BN, CG> : launch_tile<kAdaGrad, kEpiOptFP32, BN, CG>;
-        case FORGE_SGD: return int8 ? nullptr : launch_tile<kSGD, kEpiOptFP32, BN, CG>;
+            return int8 ? launch_tile<kAdaGrad, kEpiOptINT8, BN, CL> : launch_tile<kAdaGrad, kEpiOptFP32, BN, CL>;
+        case FORGE_SGD: return int8 ? nullptr : launch_tile<kSGD, kEpiOptFP32, BN, CL>;
         case FORGE_SGD_MOMENTUM:
-            return int8 ? launch_tile<kSGDMomentum, kEpiOptINT8, BN, CG>
-                        : launch_tile<kSGDMomentum, kEpiOptFP32, BN, CG>;
+            return int8 ? launch_tile<kSGDMomentum, kEpiOptINT8, BN, CL>
+                        : launch_tile<kSGDMomentum, kEpiOptFP32, BN, CL>;
     }
     return nullptr;
 }
 
-// Tile shape per call.  A CTA pair on a 256 x 256 tile stages half as many X bytes per SM as a
-// single CTA on 128 x 256, which in turn stages fewer operand bytes per flop than 128 x 128 (the
-// mainloop is bound by operand traffic from L2 into shared memory).  Each is two or four of the
-// method's 128 x 128 tiles side by side.
+// Tile shape per call.  The mainloop is bound by operand traffic from L2 into shared memory, so a
+// wide shape is used: a CTA pair on 256 x 256 (each CTA stages half of X), one CTA on 128 x 256,
+// one CTA on 128 x 128; each is a group of the method's 128 x 128 tiles side by side.  Two pairs
+// sharing dY slices by multicast (256 x 512) cut operand traffic further but fit only 144 of the
+// 152 SMs as 4-CTA clusters; measured, they pay off only for long token runs (T >= 8192).
 struct TileShape {
-    int bn, cg;
+    int bn;     // columns per CTA pair (or per CTA)
+    int cg;     // CTAs per MMA
+    int cl;     // CTAs per cluster
+    int pairs;  // MMA groups per cluster
 };
-TileShape pick_shape(int64_t d_out, int64_t d_in) {
-    if (d_out % 256 == 0 && d_in % 256 == 0) return {256, 2};
-    if (d_in % 256 == 0) return {256, 1};
-    return {128, 1};
+TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t T) {
+    if (d_out % 256 == 0 && d_in % 512 == 0 && T >= 8192) return {256, 2, 4, 2};
+    if (d_out % 256 == 0 && d_in % 256 == 0) return {256, 2, 2, 1};
+    if (d_in % 256 == 0) return {256, 1, 1, 1};
+    return {128, 1, 1, 1};
 }
 
 TileFn tile_fn(forge_opt_kind k, bool int8, int epi, TileShape t) {
     using namespace forge;
     if (epi == kEpiStoreGrad) {
-        if (t.cg == 2) return launch_tile<0, kEpiStoreGrad, 256, 2>;
+        if (t.cl == 4) return launch_tile<0, kEpiStoreGrad, 256, 4>;
+        if (t.cl == 2) return launch_tile<0, kEpiStoreGrad, 256, 2>;
         return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1> : launch_tile<0, kEpiStoreGrad, 128, 1>;
     }
-    if (t.cg == 2) return tile_fn_v<256, 2>(k, int8);
+    if (t.cl == 4) return tile_fn_v<256, 4>(k, int8);
+    if (t.cl == 2) return tile_fn_v<256, 2>(k, int8);
     return t.bn == 256 ? tile_fn_v<256, 1>(k, int8) : tile_fn_v<128, 1>(k, int8);
 }
 
@@ -287,9 +294,9 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.d_out = static_cast<int>(shape->d_out);
     a.d_in = static_cast<int>(shape->d_in);
     a.T = static_cast<int>(shape->T);
-    const TileShape ts = pick_shape(shape->d_out, shape->d_in);
+    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T);
     a.tiles_m = a.d_out / (forge::kBM * ts.cg);
-    a.tiles_n = a.d_in / ts.bn;
+    a.tiles_n = a.d_in / (ts.bn * ts.pairs);
     a.num_tiles = a.tiles_m * a.tiles_n;
     // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
     a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
@@ -394,6 +401,28 @@ forge_status forge_sync_status(struct CUstream_st* stream) {
 void forge_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns < 1000000ull ? 1000000ull : ns); }
 
 void forge_debug_withhold_next_stage(void) { g_withhold_next.store(1); }
+
+forge_status forge_launch_shape(const forge_shape* shape, int32_t* tile_rows, int32_t* tile_cols,
+                                int32_t* cluster, int32_t* ctas) {
+    forge_status st = check_shape(shape, false);
+    if (st != FORGE_OK) return st;
+    if (tile_rows == nullptr || tile_cols == nullptr || cluster == nullptr || ctas == nullptr)
+        return FORGE_ERR_INVALID_ARGUMENT;
+    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T);
+    *tile_rows = forge::kBM * ts.cg;
+    *tile_cols = ts.bn * ts.pairs;
+    *cluster = ts.cl;
+    *ctas = 0;
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    const int64_t tiles = (shape->d_out / *tile_rows) * (shape->d_in / *tile_cols);
+    int n = 0;
+    if (forge::tile_ctas(ts.bn, ts.cl, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
+    *ctas = n;
+    return FORGE_OK;
+}
 
 uint64_t forge_launch_count(void) { return g_launches.load(); }
 

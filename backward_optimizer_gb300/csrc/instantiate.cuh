@@ -9,45 +9,74 @@
 
 namespace forge {
 
-template <int OPT, int EPI, int BN, int CG>
+template <int OPT, int EPI, int BN, int CL>
 cudaError_t launch_tile(const TileLaunch& l) {
+    constexpr int CG = CL == 1 ? 1 : 2;
     using C = TileCfg<BN, CG, EPI>;
-    auto kernel = forge_tile_kernel<BN, CG, EPI, OPT>;
+    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT>;
     static std::atomic<uint64_t> configured{0};  // one bit per device ordinal
-    static std::atomic<int> max_clusters[64];    // co-resident CTA pairs per device
+    static std::atomic<int> max_clusters[64];    // co-resident clusters per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     dev &= 63;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = CG;
+    attr.val.clusterDim.x = CL;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = l.stream;
-    cfg.attrs = CG == 2 ? &attr : nullptr;
-    cfg.numAttrs = CG == 2 ? 1 : 0;
+    cfg.attrs = CL > 1 ? &attr : nullptr;
+    cfg.numAttrs = CL > 1 ? 1 : 0;
     const uint64_t bit = 1ull << dev;
     if (!(configured.load() & bit)) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (err != cudaSuccess) return err;
-        if (CG == 2) {
+        if (CL > 1) {
             int n = 0;
-            cfg.gridDim = dim3(2 * l.num_sms, 1, 1);
+            cfg.gridDim = dim3(CL * l.num_sms, 1, 1);
             err = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
             if (err != cudaSuccess) return err;
             max_clusters[dev].store(n > 0 ? n : 1);
         }
         configured.fetch_or(bit);
     }
-    // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more units than tiles
-    const int cap = CG == 1 ? l.num_sms : max_clusters[dev].load();
+    // persistent grid: one CTA per SM (or one cluster per CL SMs), never more units than tiles
+    const int cap = CL == 1 ? l.num_sms : max_clusters[dev].load();
     const int units = l.num_tiles < cap ? l.num_tiles : cap;
-    cfg.gridDim = dim3(units * CG, 1, 1);
+    cfg.gridDim = dim3(units * CL, 1, 1);
     return cudaLaunchKernelEx(&cfg, kernel, l.tmap_dy, l.tmap_x, *l.args);
+}
+
+// CTA count and cluster size a launch_tile<..., BN, CL> call with `num_tiles` tiles would use.
+template <int OPT, int EPI, int BN, int CL>
+cudaError_t tile_grid(int num_tiles, int num_sms, int* ctas) {
+    constexpr int CG = CL == 1 ? 1 : 2;
+    using C = TileCfg<BN, CG, EPI>;
+    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT>;
+    int cap = num_sms;
+    if (CL > 1) {
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (err != cudaSuccess) return err;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = CL;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(CL * num_sms, 1, 1);
+        err = cudaOccupancyMaxActiveClusters(&cap, kernel, &cfg);
+        if (err != cudaSuccess) return err;
+    }
+    *ctas = (num_tiles < cap ? num_tiles : cap) * CL;
+    return cudaSuccess;
 }
 
 template <int OPT, bool INT8>
@@ -61,7 +90,8 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 #define FORGE_INSTANTIATE_TILES(OPT, EPI)                                                      \
     template cudaError_t forge::launch_tile<OPT, EPI, 128, 1>(const forge::TileLaunch&);       \
     template cudaError_t forge::launch_tile<OPT, EPI, 256, 1>(const forge::TileLaunch&);       \
-    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2>(const forge::TileLaunch&);
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2>(const forge::TileLaunch&);       \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 4>(const forge::TileLaunch&);
 
 #define FORGE_INSTANTIATE_OPT(OPT)                    \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptFP32) \

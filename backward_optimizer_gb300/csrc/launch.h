@@ -16,15 +16,19 @@ struct TileLaunch {
     CUtensorMap tmap_dy;
     CUtensorMap tmap_x;
     const TileArgs* args;
-    int num_tiles;  // CTA tiles (CG = 1) or CTA-pair tiles (CG = 2)
+    int num_tiles;  // tiles of the launch's shape (per CTA, CTA pair or cluster of two pairs)
     int num_sms;
     cudaStream_t stream;
 };
 
 // EPI: 0 = store FP32 dW, 1 = fused optimizer with FP32 states, 2 = fused optimizer with INT8 states.
 // BN: tile columns (128, or 256 = two 128 x 128 tiles side by side).
-// CG: CTAs per tile (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair).
-template <int OPT, int EPI, int BN, int CG> cudaError_t launch_tile(const TileLaunch& l);
+// CL: CTAs per cluster (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair; 4: two pairs
+// on a 256 x 2BN tile sharing their dY slices by multicast).
+template <int OPT, int EPI, int BN, int CL> cudaError_t launch_tile(const TileLaunch& l);
+
+// CTAs a tile launch of the given shape would run (persistent grid size).
+cudaError_t tile_ctas(int bn, int cl, int num_tiles, int num_sms, int* ctas);
 template <int OPT, bool INT8> cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream);
 
 

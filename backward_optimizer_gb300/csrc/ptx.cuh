@@ -103,6 +103,17 @@ __device__ __forceinline__ void tma_load_2d_cg(void* dst, const CUtensorMap* map
     }
 }
 
+// Multicast form (CTA pairs only): the box lands at the same offset in every CTA of `mask`, and
+// each destination's bytes are counted on the barrier of that destination's pair.
+__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                                      int32_t c1, uint16_t mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -167,10 +178,11 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
             : "memory");
 }
 
-// Arrive once on `bar` -- in every CTA of the group, at the same shared-memory offset -- when
-// every tcgen05 operation issued so far by this thread has completed.
+// Arrive once on `bar` -- at the same shared-memory offset in every CTA of the cluster whose rank
+// bit is set in `mask` (CG = 2), or in this CTA (CG = 1) -- when every tcgen05 operation issued
+// so far by this thread has completed.
 template <int CG>
-__device__ __forceinline__ void tc_commit_all(uint64_t* bar) {
+__device__ __forceinline__ void tc_commit_mask(uint64_t* bar, uint16_t mask) {
     if constexpr (CG == 1)
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                          smem_addr(bar))
@@ -179,7 +191,7 @@ __device__ __forceinline__ void tc_commit_all(uint64_t* bar) {
         asm volatile(
             "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                 smem_addr(bar)),
-            "h"(static_cast<uint16_t>(0x3))
+            "h"(mask)
             : "memory");
 }
 

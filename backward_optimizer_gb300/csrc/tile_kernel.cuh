@@ -352,18 +352,25 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
 
 // ---------------------------------------------------------------- the kernel
 //
-// CG = 1: one CTA owns a 128 x BN tile (M = 128 MMA).
-// CG = 2: a cluster of two CTAs owns a 256 x BN tile.  Each CTA stages its own 128 rows of dY^T and
-//         its own BN/2 columns of X; the even CTA issues tcgen05.mma.cta_group::2 (M = 256), which
-//         reads both CTAs' shared memory and writes each CTA's 128 accumulator rows into that CTA's
-//         TMEM.  Both CTAs' TMA copies complete on the even CTA's stage barrier; the MMA commits
-//         are multicast to both CTAs; both epilogues release a TMEM buffer on the even CTA's
-//         barrier.  Per SM this halves the X bytes pulled from L2 for the same flops.
+// CL = 1: one CTA owns a 128 x BN tile (M = 128 MMA).
+// CL = 2: a cluster of two CTAs (a pair) owns a 256 x BN tile.  Each CTA stages its own 128 rows of
+//         dY^T and its own BN/2 columns of X; the pair's even CTA issues tcgen05.mma.cta_group::2
+//         (M = 256), which reads both CTAs' shared memory and writes each CTA's 128 accumulator
+//         rows into that CTA's TMEM.  Both CTAs' TMA copies complete on the even CTA's stage
+//         barrier; the MMA commits are multicast to both CTAs; both epilogues release a TMEM
+//         buffer on the even CTA's barrier.  Per SM this halves the X bytes pulled from L2.
+// CL = 4: two pairs side by side on a 256 x 2BN cluster tile share their dY^T slices: each pair
+//         loads one of the two 64-row boxes of every slice with a TMA multicast into both pairs,
+//         halving the dY bytes pulled from L2.  A stage slot is free again only when both pairs'
+//         MMAs have consumed it, so each pair's commit of a stage arrives in all four CTAs.
 
-template <int BN, int CG, int EPI, int OPT>
+template <int BN, int CL, int EPI, int OPT>
 __global__ void __launch_bounds__(kThreads, 1)
     forge_tile_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
                       const TileArgs a) {
+    static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
+    constexpr int CG = CL == 1 ? 1 : 2;       // CTAs per MMA (cta_group)
+    constexpr int kPairs = CL == 4 ? 2 : 1;   // MMA groups per cluster sharing dY
     using C = TileCfg<BN, CG, EPI>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -381,14 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // 0 = the CTA that issues the MMAs
-    const int first_tile = static_cast<int>(blockIdx.x) / CG;
-    const int tile_stride = static_cast<int>(gridDim.x) / CG;
+    const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
+    const uint32_t rank = crank & 1u;      // CTA within its pair; 0 issues the pair's MMAs
+    const uint32_t pair = crank >> 1;      // pair within the cluster
+    const uint32_t leader = crank & ~1u;   // cluster rank of this pair's MMA-issuing CTA
+    const int first_tile = static_cast<int>(blockIdx.x) / CL;
+    const int tile_stride = static_cast<int>(gridDim.x) / CL;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], kPairs);  // one commit per pair that reads this slot
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -406,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anything signals them
+    if constexpr (CL > 1) cluster_sync();  // other CTAs' barriers exist before anything signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const AbortCtx ab{abort_flag, a.status, a.wait_limit_ns};
@@ -423,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mb, nb;
                 tile_coords(tile, a, mb, nb);
                 const int row_a = mb * kBM * CG + static_cast<int>(rank) * kBM;
-                const int col_b = nb * BN + static_cast<int>(rank) * C::kBLoad;
+                const int col_b = (nb * kPairs + static_cast<int>(pair)) * BN + static_cast<int>(rank) * C::kBLoad;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, ab)) { ok = false; break; }
                     if (a.withhold_first_stage && rank == 0 && tile == first_tile && kb == 0) {
@@ -432,13 +442,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     }
                     uint32_t bar = smem_addr(&full[stage]);
-                    if constexpr (CG == 2) bar = map_to_rank(bar, 0);
+                    if constexpr (CG == 2) bar = map_to_rank(bar, leader);
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], CG * C::kStageBytes);
                     uint8_t* a_dst = sA + stage * C::kABytes;
                     uint8_t* b_dst = sB + stage * C::kBBytes;
                     const int k0 = kb * kBK;
-                    tma_load_2d_cg<CG>(a_dst, &tmap_dy, bar, row_a, k0, keep);
-                    tma_load_2d_cg<CG>(a_dst + kBK * 128, &tmap_dy, bar, row_a + 64, k0, keep);
+                    if constexpr (kPairs == 2) {
+                        // box `pair` of this CTA's 128 dY^T rows, for this CTA and its counterpart in
+                        // the other pair (cluster ranks rank and rank + 2)
+                        tma_load_2d_multicast(a_dst + pair * kBK * 128, &tmap_dy, bar, row_a + 64 * static_cast<int>(pair),
+                                              k0, static_cast<uint16_t>(0x5u << rank), keep);
+                    } else {
+                        tma_load_2d_cg<CG>(a_dst, &tmap_dy, bar, row_a, k0, keep);
+                        tma_load_2d_cg<CG>(a_dst + kBK * 128, &tmap_dy, bar, row_a + 64, k0, keep);
+                    }
 #pragma unroll
                     for (int j = 0; j < C::kBLoad / 64; ++j)
                         tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep);
@@ -486,11 +503,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
-                    tc_commit_all<CG>(&empty[stage]);
+                    // the slot is free once read: tell every CTA whose copies fill it
+                    tc_commit_mask<CG>(&empty[stage], kPairs == 2 ? 0xFu : 0x3u);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit_all<CG>(&acc_full[acc]);
+                tc_commit_mask<CG>(&acc_full[acc], static_cast<uint16_t>(0x3u << leader));
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
@@ -516,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int row0 = mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
-            const int col0 = nb * BN + half * kWidth;
+            const int col0 = (nb * kPairs + static_cast<int>(pair)) * BN + half * kWidth;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + half * kWidth);
             uint8_t* strip = strips + e * C::kStripBytes;
@@ -526,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if constexpr (CG == 2) mbar_arrive_remote(map_to_rank(smem_addr(&acc_empty[acc]), 0));
+                if constexpr (CG == 2) mbar_arrive_remote(map_to_rank(smem_addr(&acc_empty[acc]), leader));
                 else mbar_arrive(&acc_empty[acc]);
             }
             acc ^= 1;
@@ -536,9 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    // a pair tears down together: the even CTA's MMAs read the odd CTA's shared memory and write
-    // its TMEM, and commits land on both CTAs' barriers
-    if constexpr (CG == 2) cluster_sync();
+    // a cluster tears down together: a pair's MMAs read both CTAs' shared memory and write both
+    // TMEMs, multicast copies and commits land in other CTAs
+    if constexpr (CL > 1) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

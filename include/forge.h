@@ -172,6 +172,12 @@ FORGE_API void forge_set_wait_limit_ns(uint64_t ns);
  * CUDA context stays usable.  The outputs of that one call are unspecified.  No fault is raised. */
 FORGE_API void forge_debug_withhold_next_stage(void);
 
+/* The tile shape and persistent grid forge_fused_dw_step (and forge_dw_gemm) use for `shape`:
+ * rows x columns of W per tile (a group of the method's 128 x 128 tiles, §2 Methodology), CTAs per
+ * thread-block cluster, and CTAs launched on the current device.  Host-side query, no launch. */
+FORGE_API forge_status forge_launch_shape(const forge_shape *shape, int32_t *tile_rows, int32_t *tile_cols,
+                                          int32_t *cluster, int32_t *ctas);
+
 /* Number of the library's own kernel launches queued since load (all entry points). */
 FORGE_API uint64_t forge_launch_count(void);
 

@@ -11,7 +11,7 @@ import torch
 
 import backward_optimizer_gb300 as fg
 from oracle import bf16, int8_block, optim, step as ostep
-from tests.compare import assert_codes, assert_moments, assert_weights, moment_rtol
+from tests.compare import assert_codes, assert_moments, assert_weights, gradient_sensitivity, moment_rtol
 from tests.helpers import bits, f32
 from workloads import (OPTIMIZERS, WORKLOADS, Hparams, activations, default_hparams, layer_state,
                        sample_positions)
@@ -35,15 +35,10 @@ def _sampled_check(dy, x, w0, m0, v0, W, M, V, opt, hp, t, seed, n=2048, pos_see
                               None if v0 is None else f32(v0), hp, t, seed, rows, cols)
     T = dy.shape[0]
     rt = moment_rtol(T)
-    extra = None
-    if opt == "lion":
-        # where c = beta1 m + (1 - beta1) g lies within its own error of 0, either sign is correct
-        b1 = optim.binary32(hp.beta1)
-        c = b1 * f32(m0)[rows, cols].astype(np.float64) + (1 - b1) * ref["g"].astype(np.float64)
-        scale = np.maximum(np.abs(c), np.sqrt(np.mean(c * c)))
-        extra = np.where(np.abs(c) <= 2 * rt * scale, 2 * optim.binary32(hp.lr), 0.0)
-    assert_weights(bits(W)[rows, cols], ref["W"], "W", w_old_bits=bits(w0)[rows, cols], update_rtol=2 * rt,
-                   extra_tol=extra)
+    pick = lambda a: None if a is None else f32(a)[rows, cols]
+    e = (rows * d_in + cols).astype(np.uint64)
+    extra = gradient_sensitivity(opt, ref["g"], bits(w0)[rows, cols], pick(m0), pick(v0), hp, t, seed, e, rt)
+    assert_weights(bits(W)[rows, cols], ref["W"], "W", w_old_bits=bits(w0)[rows, cols], extra_tol=extra)
     if m0 is not None:
         assert_moments(f32(M)[rows, cols], ref["m"], "m", rtol=moment_rtol(T))
     if v0 is not None:

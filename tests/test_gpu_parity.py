@@ -5,7 +5,7 @@ import torch
 
 import backward_optimizer_gb300 as fg
 from oracle import int8_block, step as ostep
-from tests.compare import assert_codes, assert_moments, assert_weights
+from tests.compare import assert_codes, assert_moments, assert_weights, gradient_sensitivity, moment_rtol
 from tests.helpers import bits, f32
 from workloads import (OPTIMIZERS, WORKLOADS, Hparams, Layer, Workload, activations, default_hparams,
                        layer_state, moment_init, normal_bf16)
@@ -136,13 +136,13 @@ def test_tiny_workload_three_steps():
         rw, rm, rv = bits(W), f32(M), f32(V)  # continue from the GPU's state: per-step parity
 
 
-# (d_out, d_in) -> tile shape: (512, 512) a CTA pair on 256 x 256; (384, 256) one CTA on 128 x 256;
-# (384, 384) one CTA on 128 x 128.
-SHAPES = [(512, 512), (384, 256), (384, 384)]
+# (d_out, d_in) -> tile shape: (512, 512) two CTA pairs sharing dY on 256 x 512; (512, 768) a CTA
+# pair on 256 x 256; (384, 256) one CTA on 128 x 256; (384, 384) one CTA on 128 x 128.
+SHAPES = [(512, 512), (512, 768), (384, 256), (384, 384)]
 
 
 @pytest.mark.parametrize("opt, d_out, d_in", [(o, 512, 512) for o in OPTIMIZERS] + [(o, 384, 256) for o in OPTIMIZERS]
-                         + [(o, 384, 384) for o in ("adamw", "nadam", "sgd")])
+                         + [(o, d_out, d_in) for o in ("adamw", "nadam", "sgd") for d_out, d_in in ((384, 384), (512, 768))])
 def test_fused_matches_oracle_every_optimizer(opt, d_out, d_in):
     dy, x, w, m, v = _layer(d_out, d_in, 192, opt, seed=2)
     hp = default_hparams(opt, lr=1e-3)
@@ -201,10 +201,36 @@ def test_fused_equals_unfused_bitwise(opt, d_out, d_in):
         assert torch.equal(V1, V2)
 
 
-@pytest.mark.parametrize("d_out, d_in", [(2048, 2560), (2176, 2560), (2048, 1408)])
+@pytest.mark.parametrize("opt, d_out, d_in", [("adamw", 512, 512), ("lion", 512, 1024), ("adagrad", 2048, 2560)])
+def test_two_pairs_sharing_dy_slices(opt, d_out, d_in):
+    """T = 8192 selects clusters of two CTA pairs on 256 x 512 tiles, dY slices multicast between
+    the pairs; 2048 x 2560 has 40 cluster tiles, more than the resident clusters."""
+    T = 8192
+    assert fg.launch_shape(d_out, d_in, T)["cluster"] == 4
+    dy, x, w, m, v = _layer(d_out, d_in, T, opt, seed=13)
+    hp = default_hparams(opt, lr=1e-3)
+    W, M, V = dev(w), dev(m), dev(v)
+    fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, None, opt, hp, 3, seed=17)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    ref = ostep.fused_step(opt, bits(dy), bits(x), bits(w), None if m is None else f32(m),
+                           None if v is None else f32(v), hp, 3, 17)
+    rt = moment_rtol(T)
+    e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
+    extra = gradient_sensitivity(opt, ref["g"], bits(w), None if m is None else f32(m),
+                                 None if v is None else f32(v), hp, 3, 17, e, rt)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=extra)
+    if m is not None:
+        assert_moments(f32(M), ref["m"], "m", rtol=rt)
+    if v is not None:
+        assert_moments(f32(V), ref["v"], "v", rtol=moment_rtol(T, squared=True))
+
+
+@pytest.mark.parametrize("d_out, d_in", [(2048, 2560), (4096, 1280), (2176, 2560), (2048, 1408)])
 def test_many_tiles_with_a_ragged_persistent_tail(d_out, d_in):
-    """More tiles than resident CTAs (or CTA pairs), not a multiple of them: 80 pair tiles of
-    256 x 256; 170 tiles of 128 x 256 (d_out not a multiple of 256); 176 tiles of 128 x 128."""
+    """More tiles than resident clusters or CTAs, not a multiple of them: 80 pair tiles of 256 x 256
+    (2048 x 2560 and 4096 x 1280); 170 tiles of 128 x 256 (d_out not a multiple of 256); 176 tiles
+    of 128 x 128."""
     dy, x, w, m, v = _layer(d_out, d_in, 128, "adamw", seed=8)
     hp = default_hparams("adamw", lr=1e-3)
     W, M, V = dev(w), dev(m), dev(v)
@@ -242,3 +268,17 @@ def test_empty_layer_is_a_no_op():
 
 def test_status_word_clean_after_normal_runs():
     assert fg.sync_status() == 0
+
+
+@pytest.mark.parametrize("d_out, d_in, T, rows, cols, cluster", [
+    (512, 512, 8192, 256, 512, 4), (512, 512, 64, 256, 256, 2), (512, 768, 8192, 256, 256, 2),
+    (384, 256, 64, 128, 256, 1), (384, 384, 64, 128, 128, 1)])
+def test_launch_shape_query(d_out, d_in, T, rows, cols, cluster):
+    import ctypes
+    shape = fg.ForgeShape(T=T, d_out=d_out, d_in=d_in, state=0, reserved=0)
+    r, c, cl, n = (ctypes.c_int32() for _ in range(4))
+    assert fg.lib().forge_launch_shape(ctypes.byref(shape), ctypes.byref(r), ctypes.byref(c), ctypes.byref(cl),
+                                       ctypes.byref(n)) == 0
+    assert (r.value, c.value, cl.value) == (rows, cols, cluster)
+    tiles = (d_out // rows) * (d_in // cols)
+    assert n.value == tiles * cluster  # fewer tiles than resident clusters: one cluster per tile
