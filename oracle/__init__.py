@@ -18,11 +18,14 @@ Elimination for Memory-Efficient LLM Training" (gist.science technical summary):
   fidelity, "Low-precision fidelity", second point), with its own counter-based
   Philox4x32-10 generator -- ``bf16.py``, ``philox.py``;
 * INT8 optimizer states with one absmax scale per 64-element block (§2 Precision
-  and fidelity, third point) -- ``int8_block.py``.
+  and fidelity, third point) -- ``int8_block.py``;
+* the layer's input gradient dX = dY W from the weights before the step, and the
+  layer backward in that order (§5 Significance and claims, limitations: the
+  input gradient must be read before the weights are updated) -- ``backward.py``.
 
 Every function here is pinned by tests under ``tests/`` against closed forms,
 textbook or library routines (``torch.optim`` in float64), brute force on tiny
 inputs, or a published known-answer value; the one exception is listed as
 "parity unpinned" in its own docstring.
 """
-from . import bf16, int8_block, optim, philox, step  # noqa: F401
+from . import backward, bf16, int8_block, optim, philox, step  # noqa: F401
