@@ -8,6 +8,8 @@ fallback path.
 Entry points (same names as the C ABI in include/forge.h):
   fused_dw_step(dY, X, W, m, v, qscales, opt, hp, step, seed, stream=None)
   dw_gemm(dY, X, dW, stream=None)
+  dx_gemm(dY, W, dX, stream=None)
+  linear_backward(dY, X, W, m, v, qscales, dX, opt, hp, step, seed, stream=None)
   opt_step(dW, W, m, v, qscales, opt, hp, step, seed, stream=None)
   sync_status(stream=None), set_wait_limit_ns(ns), launch_count()
 """
@@ -19,7 +21,7 @@ from typing import Any, Optional
 
 __all__ = [
     "OPT_KINDS", "STATE_FP32", "STATE_INT8_B64", "ForgeError", "ForgeUnavailable", "lib", "library_path",
-    "fused_dw_step", "dw_gemm", "opt_step", "sync_status", "set_wait_limit_ns", "launch_count", "build",
+    "fused_dw_step", "dw_gemm", "dx_gemm", "linear_backward", "opt_step", "sync_status", "set_wait_limit_ns", "launch_count", "build",
     "ForgeShape", "ForgeHparams", "hparams_struct",
 ]
 
@@ -84,6 +86,11 @@ def lib() -> ctypes.CDLL:
     L.forge_fused_dw_step.restype = ctypes.c_int
     L.forge_dw_gemm.argtypes = [vp, vp, vp, ctypes.POINTER(ForgeShape), vp]
     L.forge_dw_gemm.restype = ctypes.c_int
+    L.forge_dx_gemm.argtypes = [vp, vp, vp, ctypes.POINTER(ForgeShape), vp]
+    L.forge_dx_gemm.restype = ctypes.c_int
+    L.forge_linear_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.POINTER(ForgeHparams),
+                                        ctypes.POINTER(ForgeShape), i64, u64, vp]
+    L.forge_linear_backward.restype = ctypes.c_int
     L.forge_opt_step.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.POINTER(ForgeHparams),
                                  ctypes.POINTER(ForgeShape), i64, u64, vp]
     L.forge_opt_step.restype = ctypes.c_int
@@ -96,6 +103,8 @@ def lib() -> ctypes.CDLL:
     i32p = ctypes.POINTER(ctypes.c_int32)
     L.forge_launch_shape.argtypes = [ctypes.POINTER(ForgeShape), i32p, i32p, i32p, i32p]
     L.forge_launch_shape.restype = ctypes.c_int
+    L.forge_dx_launch_shape.argtypes = [ctypes.POINTER(ForgeShape), i32p, i32p, i32p, i32p]
+    L.forge_dx_launch_shape.restype = ctypes.c_int
     L.forge_launch_count.argtypes = []
     L.forge_launch_count.restype = u64
     L.forge_status_string.argtypes = [ctypes.c_int]
@@ -174,6 +183,26 @@ def dw_gemm(dY, X, dW, stream=None) -> None:
     _check(lib().forge_dw_gemm(_ptr(dY), _ptr(X), _ptr(dW), ctypes.byref(shape), _stream(stream)), "forge_dw_gemm")
 
 
+def dx_gemm(dY, W, dX, stream=None) -> None:
+    """dX [T, d_in] bf16 = dY W, the layer's input gradient (read W before any step replaces it)."""
+    T, d_out = dY.shape
+    shape = _shape(T, d_out, W.shape[1], STATE_FP32)
+    _check(lib().forge_dx_gemm(_ptr(dY), _ptr(W), _ptr(dX), ctypes.byref(shape), _stream(stream)), "forge_dx_gemm")
+
+
+def linear_backward(dY, X, W, m=None, v=None, qscales=None, dX=None, opt: str = "adamw", hp: Any = None,
+                    step: int = 1, seed: int = 0, stream=None) -> None:
+    """The linear layer's backward with the fused weight step: dX = dY W from the weights before the
+    step, then the fused step, on one stream in that order."""
+    T, d_out = dY.shape
+    d_in = X.shape[1]
+    shape = _shape(T, d_out, d_in, _state_of(m, v))
+    st = lib().forge_linear_backward(_ptr(dY), _ptr(X), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), _ptr(dX),
+                                     OPT_KINDS[opt], ctypes.byref(hparams_struct(hp)), ctypes.byref(shape),
+                                     int(step), int(seed) & (2**64 - 1), _stream(stream))
+    _check(st, "forge_linear_backward")
+
+
 def opt_step(dW, W, m=None, v=None, qscales=None, opt: str = "adamw", hp: Any = None, step: int = 1, seed: int = 0,
              stream=None) -> None:
     """The unfused baseline's optimizer pass over a materialised FP32 gradient (None = zero gradient)."""
@@ -203,6 +232,14 @@ def launch_shape(d_out: int, d_in: int, T: int = 64) -> dict:
     vals = [ctypes.c_int32() for _ in range(4)]
     _check(lib().forge_launch_shape(ctypes.byref(_shape(T, d_out, d_in, STATE_FP32)), *[ctypes.byref(v) for v in vals]),
            "forge_launch_shape")
+    return dict(zip(("tile_rows", "tile_cols", "cluster", "ctas"), (v.value for v in vals)))
+
+
+def dx_launch_shape(T: int, d_out: int, d_in: int) -> dict:
+    """Tile tokens x columns, cluster size and CTA count dx_gemm uses for a layer."""
+    vals = [ctypes.c_int32() for _ in range(4)]
+    _check(lib().forge_dx_launch_shape(ctypes.byref(_shape(T, d_out, d_in, STATE_FP32)),
+                                       *[ctypes.byref(v) for v in vals]), "forge_dx_launch_shape")
     return dict(zip(("tile_rows", "tile_cols", "cluster", "ctas"), (v.value for v in vals)))
 
 

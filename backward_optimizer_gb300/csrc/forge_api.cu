@@ -232,8 +232,23 @@ TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t T) {
     return {128, 1, 1, 1};
 }
 
+// Input gradient dX = dY W: tile rows are tokens (M = T), columns d_in (N), reduction over d_out
+// (K).  A CTA pair needs 256 token rows per tile to be worth it; two pairs sharing dY slices pay
+// off only for a long reduction, as for the weight gradient.
+TileShape pick_dx_shape(int64_t T, int64_t d_out, int64_t d_in) {
+    if (T >= 256 && d_in % 512 == 0 && d_out >= 8192) return {256, 2, 4, 2};
+    if (T >= 256 && d_in % 256 == 0) return {256, 2, 2, 1};
+    if (d_in % 256 == 0) return {256, 1, 1, 1};
+    return {128, 1, 1, 1};
+}
+
 TileFn tile_fn(forge_opt_kind k, bool int8, int epi, TileShape t) {
     using namespace forge;
+    if (epi == kEpiDX) {
+        if (t.cl == 4) return launch_tile<0, kEpiDX, 256, 4>;
+        if (t.cl == 2) return launch_tile<0, kEpiDX, 256, 2>;
+        return t.bn == 256 ? launch_tile<0, kEpiDX, 256, 1> : launch_tile<0, kEpiDX, 128, 1>;
+    }
     if (epi == kEpiStoreGrad) {
         if (t.cl == 4) return launch_tile<0, kEpiStoreGrad, 256, 4>;
         if (t.cl == 2) return launch_tile<0, kEpiStoreGrad, 256, 2>;
@@ -298,6 +313,7 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.tiles_m = a.d_out / (forge::kBM * ts.cg);
     a.tiles_n = a.d_in / (ts.bn * ts.pairs);
     a.num_tiles = a.tiles_m * a.tiles_n;
+    a.k_blocks = a.T / forge::kBK;
     // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
     a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
     a.dW = dW;
@@ -328,6 +344,93 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     return cuda_status(fn(l));
 }
 
+forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* shape, cudaStream_t stream,
+                    const DeviceInfo& dev) {
+    forge::TileArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.d_out = static_cast<int>(shape->d_out);
+    a.d_in = static_cast<int>(shape->d_in);
+    a.T = static_cast<int>(shape->T);
+    const TileShape ts = pick_dx_shape(shape->T, shape->d_out, shape->d_in);
+    const int rows = forge::kBM * ts.cg;
+    a.tiles_m = (a.T + rows - 1) / rows;
+    a.tiles_n = a.d_in / (ts.bn * ts.pairs);
+    a.num_tiles = a.tiles_m * a.tiles_n;
+    a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
+    a.k_blocks = a.d_out / forge::kBK;
+    a.dX = static_cast<uint16_t*>(dX);
+    a.status = dev.status;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    a.withhold_first_stage = 0;
+
+    forge::TileLaunch l;
+    // A = dY [T, d_out] read K-major with the same box as the weight gradient's dY^T; B = W
+    // [d_out, d_in] read MN-major like X
+    forge_status st = make_operand_map(&l.tmap_dy, dY, shape->d_out, shape->T);
+    if (st != FORGE_OK) return st;
+    st = make_operand_map(&l.tmap_x, W, shape->d_in, shape->d_out);
+    if (st != FORGE_OK) return st;
+    l.args = &a;
+    l.num_tiles = a.num_tiles;
+    l.num_sms = dev.num_sms;
+    l.stream = stream;
+    TileFn fn = tile_fn(FORGE_SGD, false, forge::kEpiDX, ts);
+    if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
+    g_launches.fetch_add(1);
+    return cuda_status(fn(l));
+}
+
+// Argument checks of each entry point, separate from its launch so that forge_linear_backward can
+// check both calls before launching either.
+forge_status check_fused(const void* dY, const void* X, const void* W, const void* m, const void* v,
+                         const float* qscales, forge_opt_kind k, const forge_hparams* hp, const forge_shape* shape,
+                         int64_t step) {
+    forge_status st = check_shape(shape, true);
+    if (st != FORGE_OK) return st;
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;  // empty layer: nothing to read or write
+    st = check_opt_args(W, m, v, qscales, k, hp, shape, step);
+    if (st != FORGE_OK) return st;
+    if (shape->T > 0 && (dY == nullptr || X == nullptr)) return FORGE_ERR_INVALID_ARGUMENT;
+    if (shape->T > 0 && (!aligned32(dY) || !aligned32(X))) return FORGE_ERR_MISALIGNED;
+    return FORGE_OK;
+}
+
+forge_status launch_fused(const void* dY, const void* X, void* W, void* m, void* v, float* qscales,
+                          forge_opt_kind k, const forge_hparams* hp, const forge_shape* shape, int64_t step,
+                          uint64_t seed, cudaStream_t stream) {
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
+    DeviceInfo* dev = nullptr;
+    forge_status st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    if (shape->T == 0)  // no tokens: the gradient is exactly zero
+        return run_opt(nullptr, W, m, v, qscales, k, hp, shape, step, seed, stream, *dev);
+    return run_tile(dY, X, nullptr, W, m, v, qscales, k, forge::kEpiOptFP32, hp, shape, step, seed, stream, *dev);
+}
+
+forge_status check_dx(const void* dY, const void* W, const void* dX, const forge_shape* shape) {
+    forge_status st = check_shape(shape, false);
+    if (st != FORGE_OK) return st;
+    if (shape->T == 0 || shape->d_in == 0) return FORGE_OK;  // dX is empty
+    if ((shape->T / 128 + 1) * (shape->d_in / 128) > (1ll << 30)) return FORGE_ERR_INVALID_ARGUMENT;
+    if (dX == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    if (!aligned32(dX)) return FORGE_ERR_MISALIGNED;
+    if (shape->d_out == 0) return FORGE_OK;  // dX is zero; dY and W are empty
+    if (dY == nullptr || W == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    if (!aligned32(dY) || !aligned32(W)) return FORGE_ERR_MISALIGNED;
+    return FORGE_OK;
+}
+
+forge_status launch_dx(const void* dY, const void* W, void* dX, const forge_shape* shape, cudaStream_t stream) {
+    if (shape->T == 0 || shape->d_in == 0) return FORGE_OK;
+    DeviceInfo* dev = nullptr;
+    forge_status st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    if (shape->d_out == 0)
+        return cuda_status(
+            cudaMemsetAsync(dX, 0, static_cast<size_t>(shape->T) * static_cast<size_t>(shape->d_in) * 2, stream));
+    return run_dx(dY, W, dX, shape, stream, *dev);
+}
+
 }  // namespace
 
 extern "C" {
@@ -335,20 +438,30 @@ extern "C" {
 forge_status forge_fused_dw_step(const void* dY, const void* X, void* W, void* m, void* v, float* qscales,
                                  forge_opt_kind opt_kind, const forge_hparams* hp, const forge_shape* shape,
                                  int64_t step, uint64_t seed, struct CUstream_st* stream) {
-    forge_status st = check_shape(shape, true);
+    forge_status st = check_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step);
     if (st != FORGE_OK) return st;
-    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;  // empty layer: nothing to read or write
-    st = check_opt_args(W, m, v, qscales, opt_kind, hp, shape, step);
+    return launch_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream);
+}
+
+forge_status forge_dx_gemm(const void* dY, const void* W, void* dX, const forge_shape* shape,
+                           struct CUstream_st* stream) {
+    forge_status st = check_dx(dY, W, dX, shape);
     if (st != FORGE_OK) return st;
-    if (shape->T > 0 && (dY == nullptr || X == nullptr)) return FORGE_ERR_INVALID_ARGUMENT;
-    if (shape->T > 0 && (!aligned32(dY) || !aligned32(X))) return FORGE_ERR_MISALIGNED;
-    DeviceInfo* dev = nullptr;
-    st = device_info(&dev);
+    return launch_dx(dY, W, dX, shape, stream);
+}
+
+forge_status forge_linear_backward(const void* dY, const void* X, void* W, void* m, void* v, float* qscales,
+                                   void* dX, forge_opt_kind opt_kind, const forge_hparams* hp,
+                                   const forge_shape* shape, int64_t step, uint64_t seed,
+                                   struct CUstream_st* stream) {
+    forge_status st = check_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step);
     if (st != FORGE_OK) return st;
-    if (shape->T == 0)  // no tokens: the gradient is exactly zero
-        return run_opt(nullptr, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream, *dev);
-    return run_tile(dY, X, nullptr, W, m, v, qscales, opt_kind, forge::kEpiOptFP32, hp, shape, step, seed, stream,
-                    *dev);
+    st = check_dx(dY, W, dX, shape);
+    if (st != FORGE_OK) return st;
+    // dX reads W before the fused step replaces it: same stream, this order
+    st = launch_dx(dY, W, dX, shape, stream);
+    if (st != FORGE_OK) return st;
+    return launch_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream);
 }
 
 forge_status forge_dw_gemm(const void* dY, const void* X, float* dW, const forge_shape* shape,
@@ -418,6 +531,28 @@ forge_status forge_launch_shape(const forge_shape* shape, int32_t* tile_rows, in
     st = device_info(&dev);
     if (st != FORGE_OK) return st;
     const int64_t tiles = (shape->d_out / *tile_rows) * (shape->d_in / *tile_cols);
+    int n = 0;
+    if (forge::tile_ctas(ts.bn, ts.cl, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
+    *ctas = n;
+    return FORGE_OK;
+}
+
+forge_status forge_dx_launch_shape(const forge_shape* shape, int32_t* tile_rows, int32_t* tile_cols,
+                                   int32_t* cluster, int32_t* ctas) {
+    forge_status st = check_shape(shape, false);
+    if (st != FORGE_OK) return st;
+    if (tile_rows == nullptr || tile_cols == nullptr || cluster == nullptr || ctas == nullptr)
+        return FORGE_ERR_INVALID_ARGUMENT;
+    const TileShape ts = pick_dx_shape(shape->T, shape->d_out, shape->d_in);
+    *tile_rows = forge::kBM * ts.cg;
+    *tile_cols = ts.bn * ts.pairs;
+    *cluster = ts.cl;
+    *ctas = 0;
+    if (shape->T == 0 || shape->d_in == 0 || shape->d_out == 0) return FORGE_OK;
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    const int64_t tiles = ((shape->T + *tile_rows - 1) / *tile_rows) * (shape->d_in / *tile_cols);
     int n = 0;
     if (forge::tile_ctas(ts.bn, ts.cl, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
     *ctas = n;

@@ -1,0 +1,4 @@
+// Kernel instantiations of the input-gradient GEMM dX = dY W (bfloat16 dX to device memory).
+#include "instantiate.cuh"
+
+FORGE_INSTANTIATE_TILES(0, forge::kEpiDX)

@@ -21,7 +21,8 @@ struct TileLaunch {
     cudaStream_t stream;
 };
 
-// EPI: 0 = store FP32 dW, 1 = fused optimizer with FP32 states, 2 = fused optimizer with INT8 states.
+// EPI: 0 = store FP32 dW, 1 = fused optimizer with FP32 states, 2 = fused optimizer with INT8 states,
+// 3 = input gradient dX = dY W stored as bf16 (tile rows are tokens, columns d_in).
 // BN: tile columns (128, or 256 = two 128 x 128 tiles side by side).
 // CL: CTAs per cluster (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair; 4: two pairs
 // on a 256 x 2BN tile sharing their dY slices by multicast).

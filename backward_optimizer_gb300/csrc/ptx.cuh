@@ -253,16 +253,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor of kind::f16: D f32, A and B bf16, both operands MN-major
-// (A = dY^T and B = X are stored token-major), shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn_major(int M, int N) {
-    return (1u << 4)                                    // D format: f32
-           | (1u << 7)                                  // A format: bf16
-           | (1u << 10)                                 // B format: bf16
-           | (1u << 15)                                 // A is MN-major
-           | (1u << 16)                                 // B is MN-major
-           | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
-           | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
+// Instruction descriptor of kind::f16: D f32, A and B bf16, shape M x N.  An operand is
+// MN-major when its M (or N) index runs along memory (dY^T and X for the weight gradient, W for
+// the input gradient), K-major when K does (dY for the input gradient).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                                          // D format: f32
+           | (1u << 7)                                        // A format: bf16
+           | (1u << 10)                                       // B format: bf16
+           | (static_cast<uint32_t>(a_mn_major) << 15)        // A major-ness
+           | (static_cast<uint32_t>(b_mn_major) << 16)        // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)            // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);           // M / 16
 }
 
 // ---------------------------------------------------------------- shared memory
@@ -312,6 +313,20 @@ __device__ __forceinline__ void ld_cs_v2(const void* p, uint32_t (&r)[2]) {
 
 __device__ __forceinline__ void st_cs_v2(void* p, const uint32_t (&r)[2]) {
     asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(r[0]), "r"(r[1]) : "memory");
+}
+
+// Plain (default-cached) 256-bit store, for outputs the next kernel reads back.
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&r)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// Two binary32 values -> a packed bfloat16 pair (lo in bits 0-15), each rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(uint32_t lo, uint32_t hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return r;
 }
 
 }  // namespace forge

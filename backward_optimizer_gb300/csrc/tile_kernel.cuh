@@ -20,6 +20,11 @@
 // Tiles are visited by a static persistent schedule (tile = blockIdx.x + k * gridDim.x) in
 // grouped order so that concurrently running CTAs share dY and X slices in L2.
 //
+// The same pipeline also computes the layer's input gradient dX = dY W (EPI = kEpiDX), which the
+// fused step's ordering requires before W is overwritten: there the tile rows are tokens, the
+// columns d_in and the reduction runs over d_out; A = dY is K-major (d_out runs along memory),
+// B = W is MN-major like X, and the epilogue rounds each row to bfloat16.
+//
 // Every wait is bounded in time: on expiry the kernel records FORGE_ERR_TIMEOUT in the device
 // status word, raises a CTA-wide abort flag that every other wait observes, waits (bounded)
 // for its own copies and MMAs in flight, frees TMEM and returns.
@@ -39,19 +44,20 @@ constexpr int kNumEpiWarps = 8;  // two warps per TMEM lane quarter, each owning
 constexpr int kThreads = 64 + 32 * kNumEpiWarps;
 constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
 
-enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2 };
+enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3 };
 
 template <int BN, int CG, int EPI>
 struct TileCfg {
     static_assert(BN == 128 || BN == 256, "tile width");
     static_assert(CG == 1 || CG == 2, "CTA group");
     static constexpr int kBLoad = BN / CG;         // X columns staged by this CTA
-    static constexpr int kABytes = kBM * kBK * 2;  // one stage of dY^T: 2 boxes of [64 tokens][64 rows]
+    static constexpr int kABytes = kBM * kBK * 2;  // one stage of A: 2 boxes of 64 x 64 (dY^T, or dY for dX)
     static constexpr int kBBytes = kBLoad * kBK * 2;  // one stage of X: kBLoad/64 boxes of [64 tokens][64 cols]
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator (128 lanes x BN)
-    // one warp's 32 x 32 FP32 transpose strip; the INT8 epilogue stages two (a 64-column block)
-    static constexpr int kStripBytes = (EPI == kEpiOptINT8 ? 2 : 1) * 32 * 32 * 4;
+    // one warp's 32 x 32 FP32 transpose strip; the INT8 epilogue stages two (a 64-column block);
+    // the input-gradient epilogue stores rows as they come out of TMEM and needs none
+    static constexpr int kStripBytes = EPI == kEpiDX ? 0 : (EPI == kEpiOptINT8 ? 2 : 1) * 32 * 32 * 4;
     static constexpr int kEpiBytes = kNumEpiWarps * kStripBytes;
     static constexpr int kBarrierBytes = 256;
     static constexpr int kMaxSmem = 232448;
@@ -66,7 +72,9 @@ struct TileCfg {
 struct TileArgs {
     int d_out, d_in, T;
     int tiles_m, tiles_n, num_tiles, group_m;
+    int k_blocks;                 // 64-wide reduction slices per tile: T / 64 (dW), d_out / 64 (dX)
     float* dW;                    // kEpiStoreGrad: [d_out, d_in] FP32
+    uint16_t* dX;                 // kEpiDX: [T, d_in] bf16; token rows >= T are not stored
     uint16_t* W;                  // bf16 [d_out, d_in]
     void* m;                      // FP32 or int8 [d_out, d_in]
     void* v;
@@ -245,6 +253,28 @@ __device__ __forceinline__ void epi_opt_fp32(const TileArgs& a, int row0, int co
     }
 }
 
+// Input gradient: TMEM lane = token row, so each thread rounds its own row's 32-column runs to
+// bfloat16 and stores them as two 32-byte pieces.  Rows past the last token (the tail tile when T is
+// not a multiple of the tile height) are computed on TMA's zero fill and not stored.
+template <int WIDTH>
+__device__ __forceinline__ void epi_store_dx(const TileArgs& a, int row0, int col0, uint32_t taddr) {
+    const int row = row0 + static_cast<int>(threadIdx.x & 31u);
+    uint16_t* out = a.dX + static_cast<size_t>(row) * a.d_in + col0;
+#pragma unroll 1
+    for (int c = 0; c < WIDTH; c += 32) {
+        uint32_t g[32];
+        tmem_ld_32x32b_x32(taddr + c, g);  // warp-wide: every lane takes part, stored or not
+        tmem_ld_wait(g);
+        uint32_t p[2][8];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) p[j >> 3][j & 7] = pack_bf16x2_rn(g[2 * j], g[2 * j + 1]);
+        if (row < a.T) {
+            st_v8(out + c, p[0]);
+            st_v8(out + c + 16, p[1]);
+        }
+    }
+}
+
 // INT8 moments, on the transposed ownership of strip_transpose.  For each group of 64 columns (one
 // quantisation block per row) the warp stages both 32-column gradient strips; lane l then owns 8
 // consecutive columns in each half of rows (l div 4) + 8k, and the 4 lanes 4q .. 4q+3 together
@@ -372,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int CG = CL == 1 ? 1 : 2;       // CTAs per MMA (cta_group)
     constexpr int kPairs = CL == 4 ? 2 : 1;   // MMA groups per cluster sharing dY
     using C = TileCfg<BN, CG, EPI>;
+    constexpr bool kAKMajor = EPI == kEpiDX;  // A = dY with d_out (= K) along memory
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 128B-swizzle atoms need 1024B alignment
@@ -420,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const AbortCtx ab{abort_flag, a.status, a.wait_limit_ns};
-    const int kblocks = a.T / kBK;
+    const int kblocks = a.k_blocks;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -447,14 +478,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* a_dst = sA + stage * C::kABytes;
                     uint8_t* b_dst = sB + stage * C::kBBytes;
                     const int k0 = kb * kBK;
+                    // A box j holds rows row_a + 64j .. +63 of this CTA's 128 A rows; dY's tensor map
+                    // has d_out innermost, so its coordinates are (row, token) for dY^T and
+                    // (d_out slice, token row) for the K-major dY of dX
                     if constexpr (kPairs == 2) {
-                        // box `pair` of this CTA's 128 dY^T rows, for this CTA and its counterpart in
-                        // the other pair (cluster ranks rank and rank + 2)
-                        tma_load_2d_multicast(a_dst + pair * kBK * 128, &tmap_dy, bar, row_a + 64 * static_cast<int>(pair),
-                                              k0, static_cast<uint16_t>(0x5u << rank), keep);
+                        // box `pair`, for this CTA and its counterpart in the other pair (cluster
+                        // ranks rank and rank + 2)
+                        const int r = row_a + 64 * static_cast<int>(pair);
+                        tma_load_2d_multicast(a_dst + pair * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
+                                              kAKMajor ? r : k0, static_cast<uint16_t>(0x5u << rank), keep);
                     } else {
-                        tma_load_2d_cg<CG>(a_dst, &tmap_dy, bar, row_a, k0, keep);
-                        tma_load_2d_cg<CG>(a_dst + kBK * 128, &tmap_dy, bar, row_a + 64, k0, keep);
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int r = row_a + 64 * j;
+                            tma_load_2d_cg<CG>(a_dst + j * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
+                                               kAKMajor ? r : k0, keep);
+                        }
                     }
 #pragma unroll
                     for (int j = 0; j < C::kBLoad / 64; ++j)
@@ -480,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ------------------------------------------------ MMA issuer (the even CTA of a pair)
-            constexpr uint32_t idesc = idesc_bf16_f32_mn_major(kBM * CG, BN);
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM * CG, BN, !kAKMajor, true);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued_any = false;
@@ -495,10 +534,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_base = smem_addr(sB + stage * C::kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                        // 16 tokens = 16 rows of 128 bytes: advance 2048 bytes per MMA.  Within a
-                        // stage, the MN-direction 64-element column blocks are kBK*128 bytes apart
-                        // (leading byte offset) and 8-token row groups 1024 bytes apart (stride).
-                        const uint64_t ad = smem_desc_sw128(a_base + kk * 2048, kBK * 128, 1024);
+                        // MN-major: 16 K = 16 rows of 128 bytes, so advance 2048 bytes per MMA.
+                        // Within a stage, the MN-direction 64-element column blocks are kBK*128
+                        // bytes apart (leading byte offset) and 8-row groups 1024 bytes apart
+                        // (stride).  K-major (dY for dX): 16 K = 32 bytes within each 128-byte
+                        // swizzled row, 8-row groups 1024 bytes apart; the leading offset is unused.
+                        const uint64_t ad = kAKMajor ? smem_desc_sw128(a_base + kk * 32, 16, 1024)
+                                                     : smem_desc_sw128(a_base + kk * 2048, kBK * 128, 1024);
                         const uint64_t bd = smem_desc_sw128(b_base + kk * 2048, kBK * 128, 1024);
                         tc_mma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
@@ -538,7 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + half * kWidth);
             uint8_t* strip = strips + e * C::kStripBytes;
-            if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth>(a, row0, col0, taddr, strip);
+            if constexpr (EPI == kEpiDX) epi_store_dx<kWidth>(a, row0, col0, taddr);
+            else if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth>(a, row0, col0, taddr, strip);
             else if constexpr (EPI == kEpiOptFP32) epi_opt_fp32<OPT, kWidth>(a, row0, col0, taddr, strip);
             else epi_opt_int8<OPT, kWidth>(a, row0, col0, taddr, strip);
             tc_fence_before();

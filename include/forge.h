@@ -37,9 +37,10 @@
  *    out sets a device status word and the kernel returns early; the word is
  *    read and cleared by forge_sync_status().
  *  - Ordering (§5 Significance and claims, limitations: the input gradient must
- *    be read before the weights are updated): any dX = dY W that needs the old W
- *    must be enqueued before forge_fused_dw_step on the same stream.  The library
- *    does not compute dX.
+ *    be read before the weights are updated): the layer's input gradient
+ *    dX = dY W needs the old W, so it must be enqueued before forge_fused_dw_step
+ *    on the same stream.  forge_dx_gemm computes it; forge_linear_backward
+ *    enqueues both in that order.
  */
 #ifndef FORGE_H_
 #define FORGE_H_
@@ -155,6 +156,34 @@ FORGE_API forge_status forge_opt_step(const float *dW, void *W, void *m, void *v
                             const forge_shape *shape, int64_t step, uint64_t seed,
                             struct CUstream_st *stream);
 
+/*
+ * forge_dx_gemm -- the layer's input gradient dX = dY W (the read of W that §5
+ * Significance and claims, limitations, requires before the update), on the
+ * tensor cores: dX[t, i] = sum_o dY[t, o] W[o, i], accumulated in FP32 on chip
+ * and stored once, rounded to nearest even, as bfloat16.
+ *
+ *   dY [T, d_out] and W [d_out, d_in] bfloat16 row-major, as for the fused step;
+ *   dX [T, d_in] bfloat16 row-major, written (not accumulated); it must not
+ *   overlap dY or W.  Any T >= 0 is accepted (a tail of fewer than 128 or 256
+ *   tokens is computed on zero fill and not stored).  d_out == 0 writes zeros;
+ *   T == 0 or d_in == 0 writes nothing.  shape->state is ignored.
+ */
+FORGE_API forge_status forge_dx_gemm(const void *dY, const void *W, void *dX, const forge_shape *shape,
+                                     struct CUstream_st *stream);
+
+/*
+ * forge_linear_backward -- the whole backward of the linear layer Y = X W^T with
+ * the fused weight step, in the order §5 Significance and claims, limitations,
+ * requires: forge_dx_gemm (dX from the weights before the step), then
+ * forge_fused_dw_step, both on `stream`.  Arguments are those of the two calls;
+ * all of them are checked before either is launched, so an argument error
+ * launches nothing.  dX must not overlap any other buffer.
+ */
+FORGE_API forge_status forge_linear_backward(const void *dY, const void *X, void *W, void *m, void *v,
+                                             float *qscales, void *dX, forge_opt_kind opt_kind,
+                                             const forge_hparams *hp, const forge_shape *shape, int64_t step,
+                                             uint64_t seed, struct CUstream_st *stream);
+
 /* Waits for `stream`, then reads and clears the device status word of the current
  * device: FORGE_ERR_TIMEOUT if a bounded wait ran out in a kernel since the last
  * call, FORGE_ERR_CUDA if the stream reported an error, FORGE_OK otherwise. */
@@ -177,6 +206,10 @@ FORGE_API void forge_debug_withhold_next_stage(void);
  * thread-block cluster, and CTAs launched on the current device.  Host-side query, no launch. */
 FORGE_API forge_status forge_launch_shape(const forge_shape *shape, int32_t *tile_rows, int32_t *tile_cols,
                                           int32_t *cluster, int32_t *ctas);
+
+/* The same for forge_dx_gemm: tokens x d_in columns of dX per tile, CTAs per cluster, CTAs. */
+FORGE_API forge_status forge_dx_launch_shape(const forge_shape *shape, int32_t *tile_rows, int32_t *tile_cols,
+                                             int32_t *cluster, int32_t *ctas);
 
 /* Number of the library's own kernel launches queued since load (all entry points). */
 FORGE_API uint64_t forge_launch_count(void);

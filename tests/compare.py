@@ -88,6 +88,33 @@ def gradient_sensitivity(opt, g, w_bits, m, v, hp, t, seed, e, rtol, state="fp32
     return out
 
 
+DX_IDENTICAL_FRACTION = 0.99
+
+
+def assert_bf16_sum(gpu_bits, ref_f32, K, what="dX"):
+    """A K-term sum accumulated in FP32 and rounded once, to nearest even, to bfloat16.
+
+    ref_f32 is the exact sum rounded to binary32; its round-to-nearest-even bfloat16 is the
+    expected value.  The GPU's FP32 sum may differ from it by the accumulator's allowed deviation
+    rt * max(|ref|, rms(ref)), rt = moment_rtol(K) (the same reading as for dW), which moves the
+    bfloat16 result across a rounding boundary where the sum lies within that distance of one:
+    tolerance = one bfloat16 ULP + that deviation, and at least 99 % of elements bit-identical."""
+    g = np.asarray(gpu_bits, np.uint16).ravel()
+    r32 = np.asarray(ref_f32, np.float32).ravel()
+    r = bf16.round_nearest_even(r32)
+    same = g == r
+    frac = float(same.mean()) if same.size else 1.0
+    rv = r32.astype(np.float64)
+    scale = np.maximum(np.abs(rv), np.sqrt(np.mean(rv * rv)) if rv.size else 0.0)
+    ulp = np.where(r & 0x7FFF == 0, bf16.to_f64(np.uint16(1)), bf16.ulp(r))
+    tol = ulp + moment_rtol(K) * scale
+    bad = ~same & ~(np.abs(bf16.to_f64(g) - rv) <= tol)
+    assert not bad.any(), f"{what}: {bad.sum()} of {g.size} beyond tolerance, e.g. idx {np.flatnonzero(bad)[:5]} " \
+                          f"gpu {bf16.to_f64(g)[bad][:5]} ref {rv[bad][:5]}"
+    assert frac >= DX_IDENTICAL_FRACTION, f"{what}: only {frac:.6f} bit-identical"
+    return frac
+
+
 def assert_codes(gpu, ref, what="codes"):
     d = np.abs(np.asarray(gpu, np.int64) - np.asarray(ref, np.int64))
     assert d.max(initial=0) <= 1, f"{what}: code difference {d.max()}"

@@ -103,6 +103,37 @@ def test_dw_gemm_and_opt_step_reject_bad_arguments(L):
     assert L.forge_opt_step(A, A, A, A, None, 0, ctypes.byref(hp), ctypes.byref(_shape()), 0, 0, None) == 1
 
 
+def test_dx_gemm_rejects_bad_arguments(L):
+    s = ctypes.byref(_shape(T=100))  # any token count is accepted for dX
+    assert L.forge_dx_gemm(A, A, None, s, None) == 1
+    assert L.forge_dx_gemm(A, A, A + 2, s, None) == 3
+    assert L.forge_dx_gemm(None, A, A, s, None) == 1
+    assert L.forge_dx_gemm(A, A + 16, A, s, None) == 3
+    assert L.forge_dx_gemm(A, A, A, ctypes.byref(_shape(d_in=200)), None) == 1
+    assert L.forge_dx_gemm(A, A, A, None, None) == 1
+    # empty dX: nothing is checked beyond the shape and nothing runs
+    assert L.forge_dx_gemm(None, None, None, ctypes.byref(_shape(T=0)), None) == 0
+    assert L.forge_dx_gemm(None, None, None, ctypes.byref(_shape(d_in=0)), None) == 0
+
+
+def _backward(L, shape, dX=A, **kw):
+    hp = fg.hparams_struct()
+    args = dict(dY=A, X=A, W=A, m=A, v=A, q=None, opt=0, step=1)
+    args.update(kw)
+    return L.forge_linear_backward(args["dY"], args["X"], args["W"], args["m"], args["v"], args["q"], dX,
+                                   args["opt"], ctypes.byref(hp), ctypes.byref(shape), args["step"], 0, None)
+
+
+def test_linear_backward_checks_both_calls_before_launching(L):
+    assert _backward(L, _shape(), dX=None) == 1        # dX missing: nothing launched
+    assert _backward(L, _shape(), dX=A + 8) == 3
+    assert _backward(L, _shape(T=100)) == 1            # the weight step needs T a multiple of 64
+    assert _backward(L, _shape(), step=0) == 1
+    assert _backward(L, _shape(), m=None) == 1
+    if not _cuda_available():
+        assert _backward(L, _shape()) == 4             # arguments pass; no device here
+
+
 def test_wait_limit_setter_and_launch_counter(L):
     L.forge_set_wait_limit_ns(5)
     L.forge_set_wait_limit_ns(2_000_000_000)
