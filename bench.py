@@ -281,11 +281,51 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
-    elapsed_ms, unfused_ms, e2e_ms = max_over_ranks([elapsed_ms, unfused_ms, e2e_ms], world, dev)
+    # ---- the layer's input gradient dX = dY W (which must read W before the step replaces it),
+    # alone and as the ordered layer backward (dX, then the fused step, per layer)
+    dxs = [torch.empty(wl.T, l.d_in, dtype=torch.bfloat16, device=dev) for l in wl.layers]
+    dx_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in layers] for _ in range(args.steps)]
+
+    def dx_pass(ev=None):
+        for i, (L, dX) in enumerate(zip(layers, dxs)):
+            if ev is not None:
+                ev[i][0].record(stream)
+            fg.dx_gemm(L["dy"], L["w"], dX, stream=stream)
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    def backward_pass():
+        for i, (L, dX) in enumerate(zip(layers, dxs)):
+            fg.linear_backward(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], dX, args.opt, hp, t_step,
+                               seed=0x5EED + i, stream=stream)
+
+    timed = {}
+    for name, fn in (("dx", dx_pass), ("backward", backward_pass)):
+        for _ in range(args.warmup):
+            fn()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        b0.record(stream)
+        for k in range(args.steps):
+            fn(dx_ev[k]) if name == "dx" else fn()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        timed[name] = b0.elapsed_time(b1) / args.steps
+    dx_launch_ms = [a.elapsed_time(b) for step_ev in dx_ev for (a, b) in step_ev]
+    status = fg.sync_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the dX / backward timing")
+    del dxs
+
+    elapsed_ms, unfused_ms, e2e_ms, dx_ms, bwd_ms = max_over_ranks(
+        [elapsed_ms, unfused_ms, e2e_ms, timed["dx"], timed["backward"]], world, dev)
     ms_step = elapsed_ms / args.steps
     return dict(ms_step=ms_step, flops_step=flops_step, launch_ms=launch_ms, launches=launches,
                 unfused_ms=unfused_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks.summary(),
-                grad_pool_unfused=grad_pool_unfused, mem_fused=mem0, wl=wl)
+                grad_pool_unfused=grad_pool_unfused, mem_fused=mem0, wl=wl, dx_ms=dx_ms, bwd_ms=bwd_ms,
+                dx_launch_ms=dx_launch_ms)
 
 
 # ------------------------------------------------------------------------------------ CPU oracle
@@ -428,6 +468,12 @@ def main():
                      "kernel": "forge_tile_kernel (fused)", "avg_launch_ms": avg_launch_ms,
                      "flops_per_launch": flops_launch, "peak_source": f"bf16_tflops of {peaks_src}"},
         "clocks": r["clocks"],
+        # the layer's input gradient dX = dY W (same flops as dW) and the ordered layer backward
+        "dx": {"ms_per_step": r["dx_ms"], "value": job_throughput(r["flops_step"], world, r["dx_ms"]),
+               "unit": "TFLOP/s", "avg_launch_ms": statistics.mean(r["dx_launch_ms"]),
+               "frac": flops_launch / (statistics.mean(r["dx_launch_ms"]) * 1e-3) / 1e12 / peak},
+        "layer_backward": {"ms_per_step": r["bwd_ms"], "value": job_throughput(2 * r["flops_step"], world, r["bwd_ms"]),
+                           "unit": "TFLOP/s", "what": "dX then the fused step, per layer, one stream"},
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args)
