@@ -48,21 +48,28 @@ def philox4x32(ctr, key, rounds: int = ROUNDS) -> np.ndarray:
     return np.stack([w.astype(np.uint32) for w in c])
 
 
-def sr_bits(seed: int, step: int, e) -> np.ndarray:
-    """16 random bits for weight element ``e`` (row-major flat index) at optimizer step ``step``.
+STREAM_W, STREAM_M, STREAM_V = 0, 1, 2
+
+
+def sr_bits(seed: int, step: int, e, stream: int = STREAM_W) -> np.ndarray:
+    """16 random bits for element ``e`` (row-major flat index) of tensor ``stream`` at optimizer
+    step ``step``.
 
     Reading of the summary's unspecified stream (stated in the design notes):
       key     = (seed mod 2^32, seed div 2^32)
-      counter = (j mod 2^32, j div 2^32, step mod 2^32, step div 2^32),  j = e div 8
+      counter = (j mod 2^32, (j div 2^32) + stream * 2^30, step mod 2^32, step div 2^32),
+                j = e div 8; stream 0 is the weight, 1 and 2 the BF16 first and second moments
+                (j div 2^32 < 2^30 for every layer the library accepts, so the streams never meet)
       element e takes output word (e div 2) mod 4, its low half when e is even and
       its high half when e is odd -- one Philox call serves 8 consecutive elements.
     """
+    assert stream in (STREAM_W, STREAM_M, STREAM_V)
     e = np.asarray(e, dtype=np.uint64)
     j = e >> np.uint64(3)
     step = np.uint64(step)
     seed = np.uint64(seed)
     n = e.shape[0]
-    ctr = np.stack([j & _MASK, j >> np.uint64(32),
+    ctr = np.stack([j & _MASK, (j >> np.uint64(32)) + np.uint64(stream << 30),
                     np.full(n, step & _MASK, dtype=np.uint64),
                     np.full(n, step >> np.uint64(32), dtype=np.uint64)])
     out = philox4x32(ctr, (seed & _MASK, seed >> np.uint64(32))).astype(np.uint64)

@@ -17,12 +17,14 @@ computes the full-gradient step by its plain definition, in this order:
   2. INT8 states are dequantised (int8_block.dequantize);
   3. the optimizer runs in float64 (optim.update);
   4. new moments are rounded to binary32, or requantised to INT8 with one absmax
-     scale per 64-block; the weight update itself uses the unquantised moments;
+     scale per 64-block, or rounded to binary32 and then stochastically to BF16
+     with their own Philox streams (§2 Precision and fidelity, "BF16 or INT8"
+     states); the weight update itself uses the unrounded moments;
   5. the new weight is rounded to binary32, then stochastically to bfloat16
      with 16 Philox bits keyed by (seed, step, element index) (bf16, philox).
 
 Layouts: dY [T, d_out] and X [T, d_in] row-major bfloat16 bit patterns (uint16);
-W [d_out, d_in] bfloat16 bits; m, v [d_out, d_in] binary32 or int8 codes; INT8
+W [d_out, d_in] bfloat16 bits; m, v [d_out, d_in] binary32, int8 codes or bfloat16 bits; INT8
 scales [d_out, d_in / 64] binary32 per moment.  dW[o, i] = sum_t dY[t, o] X[t, i]
 is the weight gradient of the linear layer Y = X W^T.
 """
@@ -73,13 +75,18 @@ def apply_update(opt: str, g, w_bits, m, v, hp, t: int, seed: int, e,
 
     For ``state == "int8"`` the last axis of every array is a whole number of
     64-element blocks and ``m_scales``/``v_scales`` hold one scale per block.
+    For ``state == "bf16"`` m and v are bfloat16 bit patterns.
     Returns W (bf16 bits), w_f32 (the binary32 weight before rounding), m, v and,
-    for INT8 states, m_scales and v_scales.
+    for INT8 states, m_scales and v_scales; for INT8 and BF16 states also m_f32
+    and v_f32, the binary32 moments before quantisation or rounding.
     """
     use_m, use_v = optim.USES[opt]
     if state == "int8":
         m32 = int8_block.dequantize(m, m_scales) if use_m else None
         v32 = int8_block.dequantize(v, v_scales) if use_v else None
+    elif state == "bf16":
+        m32 = bf16.to_f32(m) if use_m else None
+        v32 = bf16.to_f32(v) if use_v else None
     else:
         m32 = np.asarray(m, dtype=np.float32) if use_m else None
         v32 = np.asarray(v, dtype=np.float32) if use_v else None
@@ -102,6 +109,13 @@ def apply_update(opt: str, g, w_bits, m, v, hp, t: int, seed: int, e,
         if v1_32 is not None:
             out["v"], out["v_scales"] = int8_block.quantize(v1_32)
         out["m_f32"], out["v_f32"] = m1_32, v1_32
+    elif state == "bf16":
+        flat = e.reshape(-1)
+        if m1_32 is not None:
+            out["m"] = bf16.stochastic_round(m1_32, philox.sr_bits(seed, t, flat, philox.STREAM_M).reshape(e.shape))
+        if v1_32 is not None:
+            out["v"] = bf16.stochastic_round(v1_32, philox.sr_bits(seed, t, flat, philox.STREAM_V).reshape(e.shape))
+        out["m_f32"], out["v_f32"] = m1_32, v1_32
     else:
         out["m"], out["v"] = m1_32, v1_32
     return out
@@ -120,15 +134,16 @@ def fused_step(opt: str, dy_bits, x_bits, w_bits, m, v, hp, t: int, seed: int,
 
 
 def fused_step_at(opt: str, dy_bits, x_bits, w_bits, m, v, hp, t: int, seed: int,
-                  rows: Sequence[int], cols: Sequence[int]) -> Dict[str, Optional[np.ndarray]]:
-    """The step at sampled positions of a large layer (binary32 states only)."""
+                  rows: Sequence[int], cols: Sequence[int], state: str = "fp32") -> Dict[str, Optional[np.ndarray]]:
+    """The step at sampled positions of a large layer (binary32 or BF16 states)."""
+    assert state in ("fp32", "bf16")
     rows = np.asarray(rows, dtype=np.int64)
     cols = np.asarray(cols, dtype=np.int64)
     d_in = np.asarray(w_bits).shape[1]
     g = dw_at(dy_bits, x_bits, rows, cols)
     pick = lambda a: None if a is None else np.asarray(a)[rows, cols]
     e = (rows * d_in + cols).astype(np.uint64)
-    out = apply_update(opt, g, pick(w_bits), pick(m), pick(v), hp, t, seed, e)
+    out = apply_update(opt, g, pick(w_bits), pick(m), pick(v), hp, t, seed, e, state)
     out["g"] = g
     return out
 
