@@ -20,7 +20,7 @@ import os
 from typing import Any, Optional
 
 __all__ = [
-    "OPT_KINDS", "STATE_FP32", "STATE_INT8_B64", "ForgeError", "ForgeUnavailable", "lib", "library_path",
+    "OPT_KINDS", "STATE_FP32", "STATE_INT8_B64", "STATE_BF16", "ForgeError", "ForgeUnavailable", "lib", "library_path",
     "fused_dw_step", "dw_gemm", "dx_gemm", "linear_backward", "opt_step", "sync_status", "set_wait_limit_ns", "launch_count", "build",
     "ForgeShape", "ForgeHparams", "hparams_struct",
 ]
@@ -32,6 +32,7 @@ OPT_KINDS = {"adamw": 0, "nadam": 1, "radam": 2, "lion": 3, "rmsprop": 4, "adagr
              "sgd_momentum": 7}
 STATE_FP32 = 0
 STATE_INT8_B64 = 1
+STATE_BF16 = 2
 STATUS = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARGUMENT", 2: "FORGE_ERR_UNSUPPORTED", 3: "FORGE_ERR_MISALIGNED",
           4: "FORGE_ERR_CUDA", 5: "FORGE_ERR_NOT_SM103", 6: "FORGE_ERR_TIMEOUT"}
 
@@ -159,14 +160,17 @@ def _state_of(m, v) -> int:
     import torch
     for t in (m, v):
         if t is not None:
-            return STATE_INT8_B64 if t.dtype == torch.int8 else STATE_FP32
+            if t.dtype == torch.int8:
+                return STATE_INT8_B64
+            return STATE_BF16 if t.dtype == torch.bfloat16 else STATE_FP32
     return STATE_FP32
 
 
 def fused_dw_step(dY, X, W, m=None, v=None, qscales=None, opt: str = "adamw", hp: Any = None, step: int = 1,
                   seed: int = 0, stream=None) -> None:
     """One fused step on torch tensors: dY [T, d_out] bf16, X [T, d_in] bf16, W [d_out, d_in] bf16,
-    m/v FP32 or int8 [d_out, d_in], qscales FP32 [2 * d_out * d_in / 64] for int8 states."""
+    m/v FP32, int8 or bf16 [d_out, d_in] (the dtype picks the state format), qscales FP32
+    [2 * d_out * d_in / 64] for int8 states."""
     T, d_out = dY.shape
     d_in = X.shape[1]
     shape = _shape(T, d_out, d_in, _state_of(m, v))

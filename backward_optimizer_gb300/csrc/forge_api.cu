@@ -164,7 +164,8 @@ forge_status check_shape(const forge_shape* shape, bool need_T) {
     if (shape->d_out > (1ll << 30) || shape->d_in > (1ll << 30) || shape->T > (1ll << 30))
         return FORGE_ERR_INVALID_ARGUMENT;
     if ((shape->d_out / 128) * (shape->d_in / 128) > (1ll << 30)) return FORGE_ERR_INVALID_ARGUMENT;
-    if (shape->state != FORGE_STATE_FP32 && shape->state != FORGE_STATE_INT8_B64) return FORGE_ERR_INVALID_ARGUMENT;
+    if (shape->state != FORGE_STATE_FP32 && shape->state != FORGE_STATE_INT8_B64 && shape->state != FORGE_STATE_BF16)
+        return FORGE_ERR_INVALID_ARGUMENT;
     return FORGE_OK;
 }
 
@@ -176,7 +177,7 @@ forge_status check_opt_args(const void* W, const void* m, const void* v, const f
     if (uses_m(k) && m == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
     if (uses_v(k) && v == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
     const bool int8 = shape->state == FORGE_STATE_INT8_B64;
-    if (int8 && k == FORGE_SGD) return FORGE_ERR_UNSUPPORTED;
+    if (shape->state != FORGE_STATE_FP32 && k == FORGE_SGD) return FORGE_ERR_UNSUPPORTED;  // no states to store
     if (int8 && qscales == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
     if (!aligned32(W) || (uses_m(k) && !aligned32(m)) || (uses_v(k) && !aligned32(v)) ||
         (int8 && (reinterpret_cast<uintptr_t>(qscales) & 3u)))
@@ -190,26 +191,26 @@ forge_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : F
 using TileFn = cudaError_t (*)(const forge::TileLaunch&);
 using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
 
+template <int OPT, int BN, int CL>
+TileFn tile_fn_state(int state) {
+    using namespace forge;
+    if (state == FORGE_STATE_INT8_B64) return launch_tile<OPT, kEpiOptINT8, BN, CL>;
+    if (state == FORGE_STATE_BF16) return launch_tile<OPT, kEpiOptBF16, BN, CL>;
+    return launch_tile<OPT, kEpiOptFP32, BN, CL>;
+}
+
 template <int BN, int CL>
-TileFn tile_fn_v(forge_opt_kind k, bool int8) {
+TileFn tile_fn_v(forge_opt_kind k, int state) {
     using namespace forge;
     switch (k) {
-        case FORGE_ADAMW:
-            return int8 ? launch_tile<kAdamW, kEpiOptINT8, BN, CL> : launch_tile<kAdamW, kEpiOptFP32, BN, CL>;
-        case FORGE_NADAM:
-            return int8 ? launch_tile<kNAdam, kEpiOptINT8, BN, CL> : launch_tile<kNAdam, kEpiOptFP32, BN, CL>;
-        case FORGE_RADAM:
-            return int8 ? launch_tile<kRAdam, kEpiOptINT8, BN, CL> : launch_tile<kRAdam, kEpiOptFP32, BN, CL>;
-        case FORGE_LION:
-            return int8 ? launch_tile<kLion, kEpiOptINT8, BN, CL> : launch_tile<kLion, kEpiOptFP32, BN, CL>;
-        case FORGE_RMSPROP:
-            return int8 ? launch_tile<kRMSprop, kEpiOptINT8, BN, CL> : launch_tile<kRMSprop, kEpiOptFP32, BN, CL>;
-        case FORGE_ADAGRAD:
-            return int8 ? launch_tile<kAdaGrad, kEpiOptINT8, BN, CL> : launch_tile<kAdaGrad, kEpiOptFP32, BN, CL>;
-        case FORGE_SGD: return int8 ? nullptr : launch_tile<kSGD, kEpiOptFP32, BN, CL>;
-        case FORGE_SGD_MOMENTUM:
-            return int8 ? launch_tile<kSGDMomentum, kEpiOptINT8, BN, CL>
-                        : launch_tile<kSGDMomentum, kEpiOptFP32, BN, CL>;
+        case FORGE_ADAMW: return tile_fn_state<kAdamW, BN, CL>(state);
+        case FORGE_NADAM: return tile_fn_state<kNAdam, BN, CL>(state);
+        case FORGE_RADAM: return tile_fn_state<kRAdam, BN, CL>(state);
+        case FORGE_LION: return tile_fn_state<kLion, BN, CL>(state);
+        case FORGE_RMSPROP: return tile_fn_state<kRMSprop, BN, CL>(state);
+        case FORGE_ADAGRAD: return tile_fn_state<kAdaGrad, BN, CL>(state);
+        case FORGE_SGD: return state == FORGE_STATE_FP32 ? launch_tile<kSGD, kEpiOptFP32, BN, CL> : nullptr;
+        case FORGE_SGD_MOMENTUM: return tile_fn_state<kSGDMomentum, BN, CL>(state);
     }
     return nullptr;
 }
@@ -242,7 +243,7 @@ TileShape pick_dx_shape(int64_t T, int64_t d_out, int64_t d_in) {
     return {128, 1, 1, 1};
 }
 
-TileFn tile_fn(forge_opt_kind k, bool int8, int epi, TileShape t) {
+TileFn tile_fn(forge_opt_kind k, int state, int epi, TileShape t) {
     using namespace forge;
     if (epi == kEpiDX) {
         if (t.cl == 4) return launch_tile<0, kEpiDX, 256, 4>;
@@ -254,22 +255,30 @@ TileFn tile_fn(forge_opt_kind k, bool int8, int epi, TileShape t) {
         if (t.cl == 2) return launch_tile<0, kEpiStoreGrad, 256, 2>;
         return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1> : launch_tile<0, kEpiStoreGrad, 128, 1>;
     }
-    if (t.cl == 4) return tile_fn_v<256, 4>(k, int8);
-    if (t.cl == 2) return tile_fn_v<256, 2>(k, int8);
-    return t.bn == 256 ? tile_fn_v<256, 1>(k, int8) : tile_fn_v<128, 1>(k, int8);
+    if (t.cl == 4) return tile_fn_v<256, 4>(k, state);
+    if (t.cl == 2) return tile_fn_v<256, 2>(k, state);
+    return t.bn == 256 ? tile_fn_v<256, 1>(k, state) : tile_fn_v<128, 1>(k, state);
 }
 
-OptFn opt_fn(forge_opt_kind k, bool int8) {
+template <int OPT>
+OptFn opt_fn_state(int state) {
+    using namespace forge;
+    if (state == FORGE_STATE_INT8_B64) return launch_opt<OPT, 1>;
+    if (state == FORGE_STATE_BF16) return launch_opt<OPT, 2>;
+    return launch_opt<OPT, 0>;
+}
+
+OptFn opt_fn(forge_opt_kind k, int state) {
     using namespace forge;
     switch (k) {
-        case FORGE_ADAMW: return int8 ? launch_opt<kAdamW, true> : launch_opt<kAdamW, false>;
-        case FORGE_NADAM: return int8 ? launch_opt<kNAdam, true> : launch_opt<kNAdam, false>;
-        case FORGE_RADAM: return int8 ? launch_opt<kRAdam, true> : launch_opt<kRAdam, false>;
-        case FORGE_LION: return int8 ? launch_opt<kLion, true> : launch_opt<kLion, false>;
-        case FORGE_RMSPROP: return int8 ? launch_opt<kRMSprop, true> : launch_opt<kRMSprop, false>;
-        case FORGE_ADAGRAD: return int8 ? launch_opt<kAdaGrad, true> : launch_opt<kAdaGrad, false>;
-        case FORGE_SGD: return int8 ? nullptr : launch_opt<kSGD, false>;
-        case FORGE_SGD_MOMENTUM: return int8 ? launch_opt<kSGDMomentum, true> : launch_opt<kSGDMomentum, false>;
+        case FORGE_ADAMW: return opt_fn_state<kAdamW>(state);
+        case FORGE_NADAM: return opt_fn_state<kNAdam>(state);
+        case FORGE_RADAM: return opt_fn_state<kRAdam>(state);
+        case FORGE_LION: return opt_fn_state<kLion>(state);
+        case FORGE_RMSPROP: return opt_fn_state<kRMSprop>(state);
+        case FORGE_ADAGRAD: return opt_fn_state<kAdaGrad>(state);
+        case FORGE_SGD: return state == FORGE_STATE_FP32 ? launch_opt<kSGD, 0> : nullptr;
+        case FORGE_SGD_MOMENTUM: return opt_fn_state<kSGDMomentum>(state);
     }
     return nullptr;
 }
@@ -293,7 +302,7 @@ forge_status run_opt(const float* dW, void* W, void* m, void* v, float* qscales,
     const uint64_t blocks = (a.n8 + 255) / 256;
     const uint64_t cap = static_cast<uint64_t>(dev.num_sms) * 8;
     const int grid = static_cast<int>(blocks < cap ? blocks : cap);
-    OptFn fn = opt_fn(k, int8);
+    OptFn fn = opt_fn(k, shape->state);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(a, grid, stream));
@@ -338,7 +347,8 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     l.num_tiles = a.num_tiles;
     l.num_sms = dev.num_sms;
     l.stream = stream;
-    TileFn fn = tile_fn(k, int8, epi, ts);
+    // epi is kEpiStoreGrad (dW to memory) or kEpiOptFP32 (the fused step, whose epilogue follows the state dtype)
+    TileFn fn = tile_fn(k, shape->state, epi, ts);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(l));
@@ -374,7 +384,7 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
     l.num_tiles = a.num_tiles;
     l.num_sms = dev.num_sms;
     l.stream = stream;
-    TileFn fn = tile_fn(FORGE_SGD, false, forge::kEpiDX, ts);
+    TileFn fn = tile_fn(FORGE_SGD, FORGE_STATE_FP32, forge::kEpiDX, ts);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(l));

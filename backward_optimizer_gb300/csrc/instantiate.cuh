@@ -79,9 +79,9 @@ cudaError_t tile_grid(int num_tiles, int num_sms, int* ctas) {
     return cudaSuccess;
 }
 
-template <int OPT, bool INT8>
+template <int OPT, int STATE>
 cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
-    forge_opt_kernel<OPT, INT8><<<grid, 256, 0, stream>>>(a);
+    forge_opt_kernel<OPT, STATE><<<grid, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -95,8 +95,12 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 
 #define FORGE_INSTANTIATE_OPT(OPT)                    \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptFP32) \
-    template cudaError_t forge::launch_opt<OPT, false>(const forge::OptArgs&, int, cudaStream_t);
+    template cudaError_t forge::launch_opt<OPT, 0>(const forge::OptArgs&, int, cudaStream_t);
 
 #define FORGE_INSTANTIATE_OPT_INT8(OPT)               \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptINT8) \
-    template cudaError_t forge::launch_opt<OPT, true>(const forge::OptArgs&, int, cudaStream_t);
+    template cudaError_t forge::launch_opt<OPT, 1>(const forge::OptArgs&, int, cudaStream_t);
+
+#define FORGE_INSTANTIATE_OPT_BF16(OPT)               \
+    FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptBF16) \
+    template cudaError_t forge::launch_opt<OPT, 2>(const forge::OptArgs&, int, cudaStream_t);

@@ -22,7 +22,8 @@ struct TileLaunch {
 };
 
 // EPI: 0 = store FP32 dW, 1 = fused optimizer with FP32 states, 2 = fused optimizer with INT8 states,
-// 3 = input gradient dX = dY W stored as bf16 (tile rows are tokens, columns d_in).
+// 3 = input gradient dX = dY W stored as bf16 (tile rows are tokens, columns d_in), 4 = fused optimizer
+// with bfloat16 states.
 // BN: tile columns (128, or 256 = two 128 x 128 tiles side by side).
 // CL: CTAs per cluster (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair; 4: two pairs
 // on a 256 x 2BN tile sharing their dY slices by multicast).
@@ -30,7 +31,8 @@ template <int OPT, int EPI, int BN, int CL> cudaError_t launch_tile(const TileLa
 
 // CTAs a tile launch of the given shape would run (persistent grid size).
 cudaError_t tile_ctas(int bn, int cl, int num_tiles, int num_sms, int* ctas);
-template <int OPT, bool INT8> cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream);
+// STATE: 0 = binary32 moments, 1 = INT8 with per-64 scales, 2 = bfloat16.
+template <int OPT, int STATE> cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream);
 
 
 }  // namespace forge

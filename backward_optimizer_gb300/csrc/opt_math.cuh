@@ -83,10 +83,15 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
     return Philox4{c0, c1, c2, c3};
 }
 
-// 16-bit random values for the 8 elements e8*8 .. e8*8+7 of the weight at step `step`:
+// Stochastic-rounding streams: the weight, and the first and second moments when they are stored
+// as BF16.  The stream index goes into the top two bits of the high counter word, which the
+// element index never reaches (at most 2^41 groups of 8 elements per layer).
+enum SrStream : uint32_t { kStreamW = 0, kStreamM = 1, kStreamV = 2 };
+
+// 16-bit random values for the 8 elements e8*8 .. e8*8+7 of tensor `stream` at step `step`:
 // element 2k takes the low half of word k, element 2k+1 its high half.
-__device__ __forceinline__ Philox4 sr_words(uint64_t e8, uint64_t seed, uint64_t step) {
-    return philox4x32_10(static_cast<uint32_t>(e8), static_cast<uint32_t>(e8 >> 32),
+__device__ __forceinline__ Philox4 sr_words(uint64_t e8, uint64_t seed, uint64_t step, uint32_t stream = kStreamW) {
+    return philox4x32_10(static_cast<uint32_t>(e8), static_cast<uint32_t>(e8 >> 32) + (stream << 30),
                          static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32),
                          static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
 }

@@ -9,7 +9,8 @@
 // Each thread owns 8 consecutive elements (one Philox call).  With INT8 states, the 8 lanes
 // l = 8k .. 8k+7 of a warp hold one 64-element block and reduce its absmax with shuffles;
 // the element count is a multiple of 128 * 128, so every warp is either fully in range or
-// fully out of it and the shuffles always see all 32 lanes.
+// fully out of it and the shuffles always see all 32 lanes.  With BF16 states the moments are
+// rounded stochastically with their own Philox streams, exactly as in the fused kernel.
 #pragma once
 
 #include <cstdint>
@@ -31,9 +32,12 @@ struct OptArgs {
     uint64_t seed, step;
 };
 
-template <int OPT, bool INT8>
+// STATE: 0 = binary32 moments, 1 = INT8 with per-64 scales, 2 = bfloat16 (the forge_state_dtype values).
+template <int OPT, int STATE>
 __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
     using Tr = OptTraits<OPT>;
+    constexpr bool INT8 = STATE == 1;
+    constexpr bool BF16S = STATE == 2;
     const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
     for (uint64_t gi = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < a.n8; gi += stride) {
         const uint64_t e0 = gi * 8;
@@ -57,6 +61,26 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
             for (int j = 0; j < 8; ++j) {
                 mf[j] = Tr::kM ? __fmul_rn(int8_at(mq[j >> 2], j & 3), ms) : 0.f;
                 vf[j] = Tr::kV ? __fmul_rn(int8_at(vq[j >> 2], j & 3), vs) : 0.f;
+            }
+        } else if constexpr (BF16S) {
+            uint32_t t[4];
+            if constexpr (Tr::kM) {
+                ld_cs_v4(static_cast<uint16_t*>(a.m) + e0, t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mf[j] = (j & 1) ? bf16_hi(t[j >> 1]) : bf16_lo(t[j >> 1]);
+            }
+            if constexpr (Tr::kV) {
+                ld_cs_v4(static_cast<uint16_t*>(a.v) + e0, t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vf[j] = (j & 1) ? bf16_hi(t[j >> 1]) : bf16_lo(t[j >> 1]);
+            }
+            if constexpr (!Tr::kM) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mf[j] = 0.f;
+            }
+            if constexpr (!Tr::kV) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vf[j] = 0.f;
             }
         } else {
             uint32_t t[8];
@@ -117,6 +141,22 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
             if constexpr (Tr::kV) {
                 st_cs_v2(static_cast<int8_t*>(a.v) + e0, vo);
                 if (leader) a.v_scales[e0 >> 6] = nvs;
+            }
+        } else if constexpr (BF16S) {
+            uint32_t t[4];
+            if constexpr (Tr::kM) {
+                const Philox4 pm = sr_words(gi, a.seed, a.step, kStreamM);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    t[k] = sr_bf16(mf[2 * k], sr_r16(pm, 2 * k)) | (sr_bf16(mf[2 * k + 1], sr_r16(pm, 2 * k + 1)) << 16);
+                st_cs_v4(static_cast<uint16_t*>(a.m) + e0, t);
+            }
+            if constexpr (Tr::kV) {
+                const Philox4 pv = sr_words(gi, a.seed, a.step, kStreamV);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    t[k] = sr_bf16(vf[2 * k], sr_r16(pv, 2 * k)) | (sr_bf16(vf[2 * k + 1], sr_r16(pv, 2 * k + 1)) << 16);
+                st_cs_v4(static_cast<uint16_t*>(a.v) + e0, t);
             }
         } else {
             uint32_t t[8];

@@ -44,7 +44,7 @@ constexpr int kNumEpiWarps = 8;  // two warps per TMEM lane quarter, each owning
 constexpr int kThreads = 64 + 32 * kNumEpiWarps;
 constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
 
-enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3 };
+enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3, kEpiOptBF16 = 4 };
 
 template <int BN, int CG, int EPI>
 struct TileCfg {
@@ -76,7 +76,7 @@ struct TileArgs {
     float* dW;                    // kEpiStoreGrad: [d_out, d_in] FP32
     uint16_t* dX;                 // kEpiDX: [T, d_in] bf16; token rows >= T are not stored
     uint16_t* W;                  // bf16 [d_out, d_in]
-    void* m;                      // FP32 or int8 [d_out, d_in]
+    void* m;                      // FP32, int8 or bf16 [d_out, d_in]
     void* v;
     float* m_scales;              // INT8: [d_out, d_in/64]
     float* v_scales;
@@ -208,26 +208,32 @@ __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int 
     }
 }
 
-template <int OPT, int WIDTH>
-__device__ __forceinline__ void epi_opt_fp32(const TileArgs& a, int row0, int col0, uint32_t taddr,
-                                             uint8_t* strip) {
+// Dense states: binary32 (BF16S = false) or bfloat16 rounded stochastically with their own Philox
+// streams (BF16S = true).  The update always runs on binary32 moments; only their storage differs.
+template <int OPT, int WIDTH, bool BF16S>
+__device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int col0, uint32_t taddr,
+                                              uint8_t* strip) {
     using Tr = OptTraits<OPT>;
+    constexpr int kSW = BF16S ? 4 : 8;  // 32-bit words holding a lane's 8 moment values
     const int lane = threadIdx.x & 31;
     // first element of this lane's 8-column run in row (row0 + lane/4); rows k = 1..3 follow at +8 rows
     const size_t lane_base = static_cast<size_t>(row0 + (lane >> 2)) * a.d_in + col0 + 8 * (lane & 3);
     const size_t row_step = static_cast<size_t>(8) * a.d_in;
-    float* mp = static_cast<float*>(a.m);
-    float* vp = static_cast<float*>(a.v);
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 32) {
-        uint32_t w[4][4], m[4][8], v[4][8];
+        uint32_t w[4][4], m[4][kSW], v[4][kSW];
         // the W/m/v loads do not depend on the gradient: issue them before the TMEM read
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const size_t e = lane_base + k * row_step + c;
             ld_cs_v4(a.W + e, w[k]);
-            if constexpr (Tr::kM) ld_cs_v8(mp + e, m[k]);
-            if constexpr (Tr::kV) ld_cs_v8(vp + e, v[k]);
+            if constexpr (BF16S) {
+                if constexpr (Tr::kM) ld_cs_v4(static_cast<uint16_t*>(a.m) + e, m[k]);
+                if constexpr (Tr::kV) ld_cs_v4(static_cast<uint16_t*>(a.v) + e, v[k]);
+            } else {
+                if constexpr (Tr::kM) ld_cs_v8(static_cast<float*>(a.m) + e, m[k]);
+                if constexpr (Tr::kV) ld_cs_v8(static_cast<float*>(a.v) + e, v[k]);
+            }
         }
         uint32_t g[4][8];
         strip_transpose(taddr + c, strip, g);
@@ -235,20 +241,39 @@ __device__ __forceinline__ void epi_opt_fp32(const TileArgs& a, int row0, int co
         for (int k = 0; k < 4; ++k) {
             const size_t e = lane_base + k * row_step + c;
             const Philox4 p = sr_words(e >> 3, a.seed, a.step);
+            Philox4 pm{}, pv{};
+            if constexpr (BF16S && Tr::kM) pm = sr_words(e >> 3, a.seed, a.step, kStreamM);
+            if constexpr (BF16S && Tr::kV) pv = sr_words(e >> 3, a.seed, a.step, kStreamV);
 #pragma unroll
             for (int j = 0; j < 8; j += 2) {
                 const uint32_t wp = w[k][j >> 1];
-                float m0 = Tr::kM ? __uint_as_float(m[k][j]) : 0.f, m1 = Tr::kM ? __uint_as_float(m[k][j + 1]) : 0.f;
-                float v0 = Tr::kV ? __uint_as_float(v[k][j]) : 0.f, v1 = Tr::kV ? __uint_as_float(v[k][j + 1]) : 0.f;
+                float m0 = 0.f, m1 = 0.f, v0 = 0.f, v1 = 0.f;
+                if constexpr (BF16S) {
+                    if constexpr (Tr::kM) { m0 = bf16_lo(m[k][j >> 1]); m1 = bf16_hi(m[k][j >> 1]); }
+                    if constexpr (Tr::kV) { v0 = bf16_lo(v[k][j >> 1]); v1 = bf16_hi(v[k][j >> 1]); }
+                } else {
+                    if constexpr (Tr::kM) { m0 = __uint_as_float(m[k][j]); m1 = __uint_as_float(m[k][j + 1]); }
+                    if constexpr (Tr::kV) { v0 = __uint_as_float(v[k][j]); v1 = __uint_as_float(v[k][j + 1]); }
+                }
                 const float w0 = opt_update<OPT>(__uint_as_float(g[k][j]), bf16_lo(wp), m0, v0, a.s);
                 const float w1 = opt_update<OPT>(__uint_as_float(g[k][j + 1]), bf16_hi(wp), m1, v1, a.s);
                 w[k][j >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
-                if constexpr (Tr::kM) { m[k][j] = __float_as_uint(m0); m[k][j + 1] = __float_as_uint(m1); }
-                if constexpr (Tr::kV) { v[k][j] = __float_as_uint(v0); v[k][j + 1] = __float_as_uint(v1); }
+                if constexpr (BF16S) {
+                    if constexpr (Tr::kM) m[k][j >> 1] = sr_bf16(m0, sr_r16(pm, j)) | (sr_bf16(m1, sr_r16(pm, j + 1)) << 16);
+                    if constexpr (Tr::kV) v[k][j >> 1] = sr_bf16(v0, sr_r16(pv, j)) | (sr_bf16(v1, sr_r16(pv, j + 1)) << 16);
+                } else {
+                    if constexpr (Tr::kM) { m[k][j] = __float_as_uint(m0); m[k][j + 1] = __float_as_uint(m1); }
+                    if constexpr (Tr::kV) { v[k][j] = __float_as_uint(v0); v[k][j + 1] = __float_as_uint(v1); }
+                }
             }
             st_cs_v4(a.W + e, w[k]);
-            if constexpr (Tr::kM) st_cs_v8(mp + e, m[k]);
-            if constexpr (Tr::kV) st_cs_v8(vp + e, v[k]);
+            if constexpr (BF16S) {
+                if constexpr (Tr::kM) st_cs_v4(static_cast<uint16_t*>(a.m) + e, m[k]);
+                if constexpr (Tr::kV) st_cs_v4(static_cast<uint16_t*>(a.v) + e, v[k]);
+            } else {
+                if constexpr (Tr::kM) st_cs_v8(static_cast<float*>(a.m) + e, m[k]);
+                if constexpr (Tr::kV) st_cs_v8(static_cast<float*>(a.v) + e, v[k]);
+            }
         }
     }
 }
@@ -582,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* strip = strips + e * C::kStripBytes;
             if constexpr (EPI == kEpiDX) epi_store_dx<kWidth>(a, row0, col0, taddr);
             else if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth>(a, row0, col0, taddr, strip);
-            else if constexpr (EPI == kEpiOptFP32) epi_opt_fp32<OPT, kWidth>(a, row0, col0, taddr, strip);
+            else if constexpr (EPI == kEpiOptFP32) epi_opt_dense<OPT, kWidth, false>(a, row0, col0, taddr, strip);
+            else if constexpr (EPI == kEpiOptBF16) epi_opt_dense<OPT, kWidth, true>(a, row0, col0, taddr, strip);
             else epi_opt_int8<OPT, kWidth>(a, row0, col0, taddr, strip);
             tc_fence_before();
             __syncwarp();

@@ -165,6 +165,9 @@ def _make_layer(wl, i, opt, state, device, seed, act_cache):
         m = None if m is None else torch.randint(-127, 128, (l.d_out, l.d_in), dtype=torch.int8, device=device)
         v = None if v is None else torch.randint(0, 128, (l.d_out, l.d_in), dtype=torch.int8, device=device)
         q = torch.rand(2 * n // 64, device=device) * 1e-5
+    elif state == "bf16":
+        m = None if m is None else m.to(torch.bfloat16)
+        v = None if v is None else v.to(torch.bfloat16)
     return dict(dy=dy, x=x, w=w, m=m, v=v, q=q)
 
 
@@ -388,7 +391,7 @@ def main():
     ap.add_argument("--impl", default="forge", choices=["forge", "reference"])
     ap.add_argument("--workload", default="llama8b-mlp")
     ap.add_argument("--opt", default="adamw")
-    ap.add_argument("--state", default="fp32", choices=["fp32", "int8"])
+    ap.add_argument("--state", default="fp32", choices=["fp32", "int8", "bf16"])
     ap.add_argument("--oracle-rows", type=int, default=0, help="rows per layer of the oracle sample (0: sized by time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -16,7 +16,13 @@
  *  - dY is [T, d_out] and X is [T, d_in]: bfloat16, row-major (token-major), as
  *    the forward and backward passes of a linear layer leave them.
  *  - W is [d_out, d_in] bfloat16, row-major.  m and v are [d_out, d_in] row-major,
- *    binary32 (FORGE_STATE_FP32) or int8 codes (FORGE_STATE_INT8_B64).
+ *    binary32 (FORGE_STATE_FP32), int8 codes (FORGE_STATE_INT8_B64) or bfloat16
+ *    (FORGE_STATE_BF16).
+ *  - BF16 states: the update reads the stored moments as binary32 and computes the
+ *    new ones in binary32 (the weight update uses these); they are then stored by
+ *    stochastic rounding to bfloat16 with 16 Philox bits each, like the weight,
+ *    from separate streams: the high counter word of the weight's stream gains
+ *    1 << 30 for m and 2 << 30 for v.
  *  - INT8 states (§2 Precision and fidelity, third low-precision point: blocks
  *    of 64): each run of 64 consecutive elements of a row shares one binary32
  *    scale s = absmax / 127; code q = clamp(round_half_even(x / s), -127, 127);
@@ -83,7 +89,8 @@ typedef enum forge_opt_kind {
 
 typedef enum forge_state_dtype {
     FORGE_STATE_FP32 = 0,
-    FORGE_STATE_INT8_B64 = 1
+    FORGE_STATE_INT8_B64 = 1,
+    FORGE_STATE_BF16 = 2  /* §2 Precision and fidelity, "BF16 or INT8" states: see below */
 } forge_state_dtype;
 
 typedef struct forge_shape {
@@ -126,7 +133,8 @@ typedef struct forge_hparams {
  *
  *   m: required for ADAMW, NADAM, RADAM, LION, SGD_MOMENTUM; ignored otherwise.
  *   v: required for ADAMW, NADAM, RADAM, RMSPROP, ADAGRAD; ignored otherwise.
- *   qscales: required iff shape->state == FORGE_STATE_INT8_B64 (not allowed for SGD).
+ *   qscales: required iff shape->state == FORGE_STATE_INT8_B64.  SGD has no
+ *   states: it takes FORGE_STATE_FP32 only.
  *   step: the 1-based optimizer step t.  seed: the layer's SR seed.
  *   T == 0 applies the update with a zero gradient.
  */

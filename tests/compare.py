@@ -22,6 +22,10 @@
   T <= 1344 this is the 1e-5 of the specification.  v, which squares g, gets twice
   the bound.
 * INT8 codes within +-1; their scales within the moment tolerance.
+* bfloat16 moments (BF16 states) are rounded stochastically like the weight: the weight's
+  criterion applies, with the moment before the step in place of W_old and the moment's own
+  gradient sensitivity.  The bit-identical fraction required of either is 99.9 % less the
+  expected share of rounding flips that sensitivity causes (assert_weights).
 """
 import numpy as np
 
@@ -39,7 +43,13 @@ def moment_rtol(T: int, squared: bool = False) -> float:
 
 def assert_weights(gpu_bits, ref_bits, what="W", w_old_bits=None, extra_tol=None):
     """extra_tol: per-element absolute allowance for the movement of the binary32 weight that the
-    gradient's allowed summation deviation causes (gradient_sensitivity)."""
+    gradient's allowed summation deviation causes (gradient_sensitivity).
+
+    Stochastic rounding with the same 16 random bits sends two binary32 values that are d apart to
+    different bfloat16 neighbours with probability d / ulp.  So where the allowed movement is a
+    sizeable part of an ULP (BF16 moments at long token runs, whose value moves in proportion to
+    g), the bit-identical fraction is lowered by its expected cost, mean(min(1, extra_tol / ulp)),
+    below the 99.9 %."""
     g = np.asarray(gpu_bits, np.uint16).ravel()
     r = np.asarray(ref_bits, np.uint16).ravel()
     assert g.shape == r.shape
@@ -56,7 +66,10 @@ def assert_weights(gpu_bits, ref_bits, what="W", w_old_bits=None, extra_tol=None
     bad = ~same & ~(np.abs(gv - rv) <= tol)
     assert not bad.any(), f"{what}: {bad.sum()} elements beyond 1 ULP, e.g. idx {np.flatnonzero(bad)[:5]} " \
                           f"gpu {gv[bad][:5]} ref {rv[bad][:5]}"
-    assert frac >= W_IDENTICAL_FRACTION, f"{what}: only {frac:.6f} bit-identical"
+    need = W_IDENTICAL_FRACTION
+    if extra_tol is not None and g.size:
+        need -= float(np.mean(np.minimum(1.0, np.asarray(extra_tol, np.float64).ravel() / ulp)))
+    assert frac >= need, f"{what}: only {frac:.6f} bit-identical (at least {need:.6f} required)"
     return frac
 
 
@@ -71,19 +84,21 @@ def assert_moments(gpu, ref, what="m", rtol=MOMENT_RTOL):
     return float((err / np.where(scale > 0, scale, 1)).max()) if r.size else 0.0
 
 
-def gradient_sensitivity(opt, g, w_bits, m, v, hp, t, seed, e, rtol, state="fp32", m_scales=None, v_scales=None):
-    """Per element, how far the oracle's binary32 weight moves when its gradient moves by the
-    summation deviation the summary allows, rtol * max(|g|, rms(g)), in either direction.  Used
-    as an extra weight tolerance: the GPU must agree, within one bfloat16 ULP, with the oracle
-    evaluated at some gradient inside that band.  (For Lion this includes a sign flip of c.)"""
+def gradient_sensitivity(opt, g, w_bits, m, v, hp, t, seed, e, rtol, state="fp32", m_scales=None, v_scales=None,
+                         what="w_f32"):
+    """Per element, how far the oracle's binary32 output `what` (the weight, or m_f32 / v_f32 for
+    rounded states) moves when its gradient moves by the summation deviation the summary allows,
+    rtol * max(|g|, rms(g)), in either direction.  Used as an extra tolerance: the GPU must agree,
+    within one bfloat16 ULP, with the oracle evaluated at some gradient inside that band.  (For
+    Lion this includes a sign flip of c.)"""
     from oracle import step as ostep
     g64 = np.asarray(g, np.float64)
     band = rtol * np.maximum(np.abs(g64), np.sqrt(np.mean(g64 * g64)))
-    base = ostep.apply_update(opt, g, w_bits, m, v, hp, t, seed, e, state, m_scales, v_scales)["w_f32"]
+    base = ostep.apply_update(opt, g, w_bits, m, v, hp, t, seed, e, state, m_scales, v_scales)[what]
     out = np.zeros(g64.shape)
     for sign in (-1.0, 1.0):
         moved = ostep.apply_update(opt, (g64 + sign * band).astype(np.float32), w_bits, m, v, hp, t, seed, e,
-                                   state, m_scales, v_scales)["w_f32"]
+                                   state, m_scales, v_scales)[what]
         out = np.maximum(out, np.abs(moved.astype(np.float64) - base.astype(np.float64)))
     return out
 

@@ -75,6 +75,8 @@ def _fused(L, shape, opt=0, step=1, W=A, m=A, v=A, q=None, dY=A, X=A, hp=True):
     (dict(shape=_shape(), v=None), 1),
     (dict(shape=_shape(state=1), q=None), 1),
     (dict(shape=_shape(state=1), opt=6, q=A), 2),
+    (dict(shape=_shape(state=2), opt=6), 2),
+    (dict(shape=_shape(state=3)), 1),
     (dict(shape=_shape(), W=A + 8), 3),
     (dict(shape=_shape(), m=A + 16), 3),
     (dict(shape=_shape(), dY=A + 2), 3),
