@@ -155,15 +155,17 @@ forge_status make_operand_map(CUtensorMap* map, const void* base, int64_t cols, 
     return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_CUDA;
 }
 
-forge_status check_shape(const forge_shape* shape, bool need_T) {
+// Sizes: any T >= 0 (the last 64-token slice is zero-filled past T); d_out and d_in multiples of 8,
+// which a TMA row stride (16 bytes) and the epilogue's 16- and 32-byte accesses need.  Tiles that
+// reach past the last row or column compute on zero fill and store nothing there.
+forge_status check_shape(const forge_shape* shape) {
     if (shape == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
     if (shape->d_out < 0 || shape->d_in < 0 || shape->T < 0 || shape->reserved != 0) return FORGE_ERR_INVALID_ARGUMENT;
-    if (shape->d_out % 128 != 0 || shape->d_in % 128 != 0) return FORGE_ERR_INVALID_ARGUMENT;
-    if (need_T && shape->T % forge::kBK != 0) return FORGE_ERR_INVALID_ARGUMENT;
+    if (shape->d_out % 8 != 0 || shape->d_in % 8 != 0) return FORGE_ERR_INVALID_ARGUMENT;
     // TMA coordinates are 32-bit; the tile scheduler counts tiles in int.
     if (shape->d_out > (1ll << 30) || shape->d_in > (1ll << 30) || shape->T > (1ll << 30))
         return FORGE_ERR_INVALID_ARGUMENT;
-    if ((shape->d_out / 128) * (shape->d_in / 128) > (1ll << 30)) return FORGE_ERR_INVALID_ARGUMENT;
+    if ((shape->d_out / 128 + 1) * (shape->d_in / 128 + 1) > (1ll << 30)) return FORGE_ERR_INVALID_ARGUMENT;
     if (shape->state != FORGE_STATE_FP32 && shape->state != FORGE_STATE_INT8_B64 && shape->state != FORGE_STATE_BF16)
         return FORGE_ERR_INVALID_ARGUMENT;
     return FORGE_OK;
@@ -179,6 +181,7 @@ forge_status check_opt_args(const void* W, const void* m, const void* v, const f
     const bool int8 = shape->state == FORGE_STATE_INT8_B64;
     if (shape->state != FORGE_STATE_FP32 && k == FORGE_SGD) return FORGE_ERR_UNSUPPORTED;  // no states to store
     if (int8 && qscales == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    if (int8 && shape->d_in % 64 != 0) return FORGE_ERR_INVALID_ARGUMENT;  // a 64-block never spans two rows
     if (!aligned32(W) || (uses_m(k) && !aligned32(m)) || (uses_v(k) && !aligned32(v)) ||
         (int8 && (reinterpret_cast<uintptr_t>(qscales) & 3u)))
         return FORGE_ERR_MISALIGNED;
@@ -226,10 +229,14 @@ struct TileShape {
     int cl;     // CTAs per cluster
     int pairs;  // MMA groups per cluster
 };
+// A ragged dimension (not a multiple of the tile) takes the wide shape once it is large enough that
+// the zero-filled tail costs little (over 1024).
 TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t T) {
+    const bool rows256 = d_out % 256 == 0 || (d_out % 128 != 0 && d_out > 1024);
+    const bool cols256 = d_in % 256 == 0 || (d_in % 128 != 0 && d_in > 1024);
     if (d_out % 256 == 0 && d_in % 512 == 0 && T >= 8192) return {256, 2, 4, 2};
-    if (d_out % 256 == 0 && d_in % 256 == 0) return {256, 2, 2, 1};
-    if (d_in % 256 == 0) return {256, 1, 1, 1};
+    if (rows256 && cols256) return {256, 2, 2, 1};
+    if (cols256) return {256, 1, 1, 1};
     return {128, 1, 1, 1};
 }
 
@@ -237,11 +244,14 @@ TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t T) {
 // (K).  A CTA pair needs 256 token rows per tile to be worth it; two pairs sharing dY slices pay
 // off only for a long reduction, as for the weight gradient.
 TileShape pick_dx_shape(int64_t T, int64_t d_out, int64_t d_in) {
+    const bool cols256 = d_in % 256 == 0 || (d_in % 128 != 0 && d_in > 1024);
     if (T >= 256 && d_in % 512 == 0 && d_out >= 8192) return {256, 2, 4, 2};
-    if (T >= 256 && d_in % 256 == 0) return {256, 2, 2, 1};
-    if (d_in % 256 == 0) return {256, 1, 1, 1};
+    if (T >= 256 && cols256) return {256, 2, 2, 1};
+    if (cols256) return {256, 1, 1, 1};
     return {128, 1, 1, 1};
 }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 TileFn tile_fn(forge_opt_kind k, int state, int epi, TileShape t) {
     using namespace forge;
@@ -319,10 +329,10 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.d_in = static_cast<int>(shape->d_in);
     a.T = static_cast<int>(shape->T);
     const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T);
-    a.tiles_m = a.d_out / (forge::kBM * ts.cg);
-    a.tiles_n = a.d_in / (ts.bn * ts.pairs);
+    a.tiles_m = static_cast<int>(ceil_div(a.d_out, forge::kBM * ts.cg));
+    a.tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn * ts.pairs));
     a.num_tiles = a.tiles_m * a.tiles_n;
-    a.k_blocks = a.T / forge::kBK;
+    a.k_blocks = static_cast<int>(ceil_div(a.T, forge::kBK));
     // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
     a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
     a.dW = dW;
@@ -363,11 +373,11 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
     a.T = static_cast<int>(shape->T);
     const TileShape ts = pick_dx_shape(shape->T, shape->d_out, shape->d_in);
     const int rows = forge::kBM * ts.cg;
-    a.tiles_m = (a.T + rows - 1) / rows;
-    a.tiles_n = a.d_in / (ts.bn * ts.pairs);
+    a.tiles_m = static_cast<int>(ceil_div(a.T, rows));
+    a.tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn * ts.pairs));
     a.num_tiles = a.tiles_m * a.tiles_n;
     a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
-    a.k_blocks = a.d_out / forge::kBK;
+    a.k_blocks = static_cast<int>(ceil_div(a.d_out, forge::kBK));
     a.dX = static_cast<uint16_t*>(dX);
     a.status = dev.status;
     a.wait_limit_ns = g_wait_limit_ns.load();
@@ -395,7 +405,7 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
 forge_status check_fused(const void* dY, const void* X, const void* W, const void* m, const void* v,
                          const float* qscales, forge_opt_kind k, const forge_hparams* hp, const forge_shape* shape,
                          int64_t step) {
-    forge_status st = check_shape(shape, true);
+    forge_status st = check_shape(shape);
     if (st != FORGE_OK) return st;
     if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;  // empty layer: nothing to read or write
     st = check_opt_args(W, m, v, qscales, k, hp, shape, step);
@@ -418,7 +428,7 @@ forge_status launch_fused(const void* dY, const void* X, void* W, void* m, void*
 }
 
 forge_status check_dx(const void* dY, const void* W, const void* dX, const forge_shape* shape) {
-    forge_status st = check_shape(shape, false);
+    forge_status st = check_shape(shape);
     if (st != FORGE_OK) return st;
     if (shape->T == 0 || shape->d_in == 0) return FORGE_OK;  // dX is empty
     if ((shape->T / 128 + 1) * (shape->d_in / 128) > (1ll << 30)) return FORGE_ERR_INVALID_ARGUMENT;
@@ -476,7 +486,7 @@ forge_status forge_linear_backward(const void* dY, const void* X, void* W, void*
 
 forge_status forge_dw_gemm(const void* dY, const void* X, float* dW, const forge_shape* shape,
                            struct CUstream_st* stream) {
-    forge_status st = check_shape(shape, true);
+    forge_status st = check_shape(shape);
     if (st != FORGE_OK) return st;
     if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
     if (dW == nullptr || (shape->T > 0 && (dY == nullptr || X == nullptr))) return FORGE_ERR_INVALID_ARGUMENT;
@@ -494,7 +504,7 @@ forge_status forge_dw_gemm(const void* dY, const void* X, float* dW, const forge
 forge_status forge_opt_step(const float* dW, void* W, void* m, void* v, float* qscales, forge_opt_kind opt_kind,
                             const forge_hparams* hp, const forge_shape* shape, int64_t step, uint64_t seed,
                             struct CUstream_st* stream) {
-    forge_status st = check_shape(shape, false);
+    forge_status st = check_shape(shape);
     if (st != FORGE_OK) return st;
     if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
     st = check_opt_args(W, m, v, qscales, opt_kind, hp, shape, step);
@@ -527,7 +537,7 @@ void forge_debug_withhold_next_stage(void) { g_withhold_next.store(1); }
 
 forge_status forge_launch_shape(const forge_shape* shape, int32_t* tile_rows, int32_t* tile_cols,
                                 int32_t* cluster, int32_t* ctas) {
-    forge_status st = check_shape(shape, false);
+    forge_status st = check_shape(shape);
     if (st != FORGE_OK) return st;
     if (tile_rows == nullptr || tile_cols == nullptr || cluster == nullptr || ctas == nullptr)
         return FORGE_ERR_INVALID_ARGUMENT;
@@ -540,7 +550,7 @@ forge_status forge_launch_shape(const forge_shape* shape, int32_t* tile_rows, in
     DeviceInfo* dev = nullptr;
     st = device_info(&dev);
     if (st != FORGE_OK) return st;
-    const int64_t tiles = (shape->d_out / *tile_rows) * (shape->d_in / *tile_cols);
+    const int64_t tiles = ceil_div(shape->d_out, *tile_rows) * ceil_div(shape->d_in, *tile_cols);
     int n = 0;
     if (forge::tile_ctas(ts.bn, ts.cl, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
     *ctas = n;
@@ -549,7 +559,7 @@ forge_status forge_launch_shape(const forge_shape* shape, int32_t* tile_rows, in
 
 forge_status forge_dx_launch_shape(const forge_shape* shape, int32_t* tile_rows, int32_t* tile_cols,
                                    int32_t* cluster, int32_t* ctas) {
-    forge_status st = check_shape(shape, false);
+    forge_status st = check_shape(shape);
     if (st != FORGE_OK) return st;
     if (tile_rows == nullptr || tile_cols == nullptr || cluster == nullptr || ctas == nullptr)
         return FORGE_ERR_INVALID_ARGUMENT;
@@ -562,7 +572,7 @@ forge_status forge_dx_launch_shape(const forge_shape* shape, int32_t* tile_rows,
     DeviceInfo* dev = nullptr;
     st = device_info(&dev);
     if (st != FORGE_OK) return st;
-    const int64_t tiles = ((shape->T + *tile_rows - 1) / *tile_rows) * (shape->d_in / *tile_cols);
+    const int64_t tiles = ceil_div(shape->T, *tile_rows) * ceil_div(shape->d_in, *tile_cols);
     int n = 0;
     if (forge::tile_ctas(ts.bn, ts.cl, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
     *ctas = n;

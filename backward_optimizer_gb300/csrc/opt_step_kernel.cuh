@@ -7,9 +7,10 @@
 // ablation baseline and for T == 0 (zero gradient, dW == nullptr).
 //
 // Each thread owns 8 consecutive elements (one Philox call).  With INT8 states, the 8 lanes
-// l = 8k .. 8k+7 of a warp hold one 64-element block and reduce its absmax with shuffles;
-// the element count is a multiple of 128 * 128, so every warp is either fully in range or
-// fully out of it and the shuffles always see all 32 lanes.  With BF16 states the moments are
+// l = 8k .. 8k+7 of a warp hold one 64-element block and reduce its absmax with shuffles.  Whole
+// warps iterate together (a lane past the last element only skips its loads and stores), so the
+// shuffles always see all 32 lanes; the element count is a multiple of 64 with INT8 states, so
+// each 8-lane block group is wholly in or out of range.  With BF16 states the moments are
 // rounded stochastically with their own Philox streams, exactly as in the fused kernel.
 #pragma once
 
@@ -39,23 +40,31 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
     constexpr bool INT8 = STATE == 1;
     constexpr bool BF16S = STATE == 2;
     const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-    for (uint64_t gi = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < a.n8; gi += stride) {
-        const uint64_t e0 = gi * 8;
+    const uint64_t lane = threadIdx.x & 31u;
+    for (uint64_t gi = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi - lane < a.n8; gi += stride) {
+        const bool valid = gi < a.n8;
+        const uint64_t e0 = (valid ? gi : 0) * 8;  // lanes past the end read (and store) nothing
         uint32_t g[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (a.dW != nullptr) ld_cs_v8(a.dW + e0, g);
-        uint32_t w[4];
-        ld_cs_v4(a.W + e0, w);
+        uint32_t w[4] = {0, 0, 0, 0};
+        if (valid) {
+            if (a.dW != nullptr) ld_cs_v8(a.dW + e0, g);
+            ld_cs_v4(a.W + e0, w);
+        }
         float mf[8], vf[8];
         float ms = 0.f, vs = 0.f;
         uint32_t mq[2] = {0, 0}, vq[2] = {0, 0};
         if constexpr (INT8) {
             if constexpr (Tr::kM) {
-                ld_cs_v2(static_cast<int8_t*>(a.m) + e0, mq);
-                ms = a.m_scales[e0 >> 6];
+                if (valid) {
+                    ld_cs_v2(static_cast<int8_t*>(a.m) + e0, mq);
+                    ms = a.m_scales[e0 >> 6];
+                }
             }
             if constexpr (Tr::kV) {
-                ld_cs_v2(static_cast<int8_t*>(a.v) + e0, vq);
-                vs = a.v_scales[e0 >> 6];
+                if (valid) {
+                    ld_cs_v2(static_cast<int8_t*>(a.v) + e0, vq);
+                    vs = a.v_scales[e0 >> 6];
+                }
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -63,14 +72,14 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
                 vf[j] = Tr::kV ? __fmul_rn(int8_at(vq[j >> 2], j & 3), vs) : 0.f;
             }
         } else if constexpr (BF16S) {
-            uint32_t t[4];
+            uint32_t t[4] = {0, 0, 0, 0};
             if constexpr (Tr::kM) {
-                ld_cs_v4(static_cast<uint16_t*>(a.m) + e0, t);
+                if (valid) ld_cs_v4(static_cast<uint16_t*>(a.m) + e0, t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mf[j] = (j & 1) ? bf16_hi(t[j >> 1]) : bf16_lo(t[j >> 1]);
             }
             if constexpr (Tr::kV) {
-                ld_cs_v4(static_cast<uint16_t*>(a.v) + e0, t);
+                if (valid) ld_cs_v4(static_cast<uint16_t*>(a.v) + e0, t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) vf[j] = (j & 1) ? bf16_hi(t[j >> 1]) : bf16_lo(t[j >> 1]);
             }
@@ -83,14 +92,14 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
                 for (int j = 0; j < 8; ++j) vf[j] = 0.f;
             }
         } else {
-            uint32_t t[8];
+            uint32_t t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
             if constexpr (Tr::kM) {
-                ld_cs_v8(static_cast<float*>(a.m) + e0, t);
+                if (valid) ld_cs_v8(static_cast<float*>(a.m) + e0, t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mf[j] = __uint_as_float(t[j]);
             }
             if constexpr (Tr::kV) {
-                ld_cs_v8(static_cast<float*>(a.v) + e0, t);
+                if (valid) ld_cs_v8(static_cast<float*>(a.v) + e0, t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) vf[j] = __uint_as_float(t[j]);
             }
@@ -113,7 +122,7 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             w[k] = sr_bf16(wn[2 * k], sr_r16(p, 2 * k)) | (sr_bf16(wn[2 * k + 1], sr_r16(p, 2 * k + 1)) << 16);
-        st_cs_v4(a.W + e0, w);
+        if (valid) st_cs_v4(a.W + e0, w);
         if constexpr (INT8) {
             float am = 0.f, av = 0.f;
 #pragma unroll
@@ -134,13 +143,15 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
                 if constexpr (Tr::kV) vo[j >> 2] |= int8_code(vf[j], nvs) << (8 * (j & 3));
             }
             const bool leader = (threadIdx.x & 7) == 0;
-            if constexpr (Tr::kM) {
-                st_cs_v2(static_cast<int8_t*>(a.m) + e0, mo);
-                if (leader) a.m_scales[e0 >> 6] = nms;
-            }
-            if constexpr (Tr::kV) {
-                st_cs_v2(static_cast<int8_t*>(a.v) + e0, vo);
-                if (leader) a.v_scales[e0 >> 6] = nvs;
+            if (valid) {
+                if constexpr (Tr::kM) {
+                    st_cs_v2(static_cast<int8_t*>(a.m) + e0, mo);
+                    if (leader) a.m_scales[e0 >> 6] = nms;
+                }
+                if constexpr (Tr::kV) {
+                    st_cs_v2(static_cast<int8_t*>(a.v) + e0, vo);
+                    if (leader) a.v_scales[e0 >> 6] = nvs;
+                }
             }
         } else if constexpr (BF16S) {
             uint32_t t[4];
@@ -149,26 +160,26 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     t[k] = sr_bf16(mf[2 * k], sr_r16(pm, 2 * k)) | (sr_bf16(mf[2 * k + 1], sr_r16(pm, 2 * k + 1)) << 16);
-                st_cs_v4(static_cast<uint16_t*>(a.m) + e0, t);
+                if (valid) st_cs_v4(static_cast<uint16_t*>(a.m) + e0, t);
             }
             if constexpr (Tr::kV) {
                 const Philox4 pv = sr_words(gi, a.seed, a.step, kStreamV);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     t[k] = sr_bf16(vf[2 * k], sr_r16(pv, 2 * k)) | (sr_bf16(vf[2 * k + 1], sr_r16(pv, 2 * k + 1)) << 16);
-                st_cs_v4(static_cast<uint16_t*>(a.v) + e0, t);
+                if (valid) st_cs_v4(static_cast<uint16_t*>(a.v) + e0, t);
             }
         } else {
             uint32_t t[8];
             if constexpr (Tr::kM) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) t[j] = __float_as_uint(mf[j]);
-                st_cs_v8(static_cast<float*>(a.m) + e0, t);
+                if (valid) st_cs_v8(static_cast<float*>(a.m) + e0, t);
             }
             if constexpr (Tr::kV) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) t[j] = __float_as_uint(vf[j]);
-                st_cs_v8(static_cast<float*>(a.v) + e0, t);
+                if (valid) st_cs_v8(static_cast<float*>(a.v) + e0, t);
             }
         }
     }

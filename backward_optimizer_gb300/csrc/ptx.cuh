@@ -322,6 +322,11 @@ __device__ __forceinline__ void st_v8(void* p, const uint32_t (&r)[8]) {
                  : "memory");
 }
 
+__device__ __forceinline__ void st_v4(void* p, const uint32_t (&r)[4]) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 // Two binary32 values -> a packed bfloat16 pair (lo in bits 0-15), each rounded to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(uint32_t lo, uint32_t hi) {
     uint32_t r;

@@ -130,7 +130,10 @@ __device__ __forceinline__ void tile_coords(int tile, const TileArgs& a, int& mb
 // ---------------------------------------------------------------- epilogues
 // Each is called by one warp for one tile.  The warp owns weight rows row0 .. row0+31 (its TMEM
 // lane quarter) and columns col0 .. col0+WIDTH-1; `taddr` is the TMEM address of (row0, col0);
-// `strip` is the warp's private 4 KiB shared-memory transpose buffer.
+// `strip` is the warp's private 4 KiB shared-memory transpose buffer.  A tile may reach past the
+// last row or column of a ragged layer (its operands were zero-filled there): device-memory
+// accesses are then skipped per 8-column run and per row, while TMEM reads and shuffles, which
+// are warp-wide, still run on every lane.
 
 __device__ __forceinline__ void st_v8_f32(float* p, const uint32_t (&r)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
@@ -198,13 +201,17 @@ template <int WIDTH>
 __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int col0, uint32_t taddr,
                                                uint8_t* strip) {
     const int lane = threadIdx.x & 31;
-    float* base = a.dW + static_cast<size_t>(row0 + (lane >> 2)) * a.d_in + col0 + 8 * (lane & 3);
+    const int row = row0 + (lane >> 2), col = col0 + 8 * (lane & 3);
+    float* base = a.dW + static_cast<size_t>(row) * a.d_in + col;
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 32) {
         uint32_t t[4][8];
         strip_transpose(taddr + c, strip, t);
+        if (col + c < a.d_in) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) st_v8_f32(base + static_cast<size_t>(8 * k) * a.d_in + c, t[k]);
+            for (int k = 0; k < 4; ++k)
+                if (row + 8 * k < a.d_out) st_v8_f32(base + static_cast<size_t>(8 * k) * a.d_in + c, t[k]);
+        }
     }
 }
 
@@ -216,23 +223,28 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
     using Tr = OptTraits<OPT>;
     constexpr int kSW = BF16S ? 4 : 8;  // 32-bit words holding a lane's 8 moment values
     const int lane = threadIdx.x & 31;
+    const int row = row0 + (lane >> 2), col = col0 + 8 * (lane & 3);
     // first element of this lane's 8-column run in row (row0 + lane/4); rows k = 1..3 follow at +8 rows
-    const size_t lane_base = static_cast<size_t>(row0 + (lane >> 2)) * a.d_in + col0 + 8 * (lane & 3);
+    const size_t lane_base = static_cast<size_t>(row) * a.d_in + col;
     const size_t row_step = static_cast<size_t>(8) * a.d_in;
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 32) {
         uint32_t w[4][4], m[4][kSW], v[4][kSW];
+        bool ok[4];
         // the W/m/v loads do not depend on the gradient: issue them before the TMEM read
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const size_t e = lane_base + k * row_step + c;
-            ld_cs_v4(a.W + e, w[k]);
+            ok[k] = col + c < a.d_in && row + 8 * k < a.d_out;
+            // a run outside the layer loads the layer's first run instead (always valid) and
+            // stores nothing, so the loads stay unconditional
+            const size_t el = ok[k] ? lane_base + k * row_step + c : 0;
+            ld_cs_v4(a.W + el, w[k]);
             if constexpr (BF16S) {
-                if constexpr (Tr::kM) ld_cs_v4(static_cast<uint16_t*>(a.m) + e, m[k]);
-                if constexpr (Tr::kV) ld_cs_v4(static_cast<uint16_t*>(a.v) + e, v[k]);
+                if constexpr (Tr::kM) ld_cs_v4(static_cast<uint16_t*>(a.m) + el, m[k]);
+                if constexpr (Tr::kV) ld_cs_v4(static_cast<uint16_t*>(a.v) + el, v[k]);
             } else {
-                if constexpr (Tr::kM) ld_cs_v8(static_cast<float*>(a.m) + e, m[k]);
-                if constexpr (Tr::kV) ld_cs_v8(static_cast<float*>(a.v) + e, v[k]);
+                if constexpr (Tr::kM) ld_cs_v8(static_cast<float*>(a.m) + el, m[k]);
+                if constexpr (Tr::kV) ld_cs_v8(static_cast<float*>(a.v) + el, v[k]);
             }
         }
         uint32_t g[4][8];
@@ -266,13 +278,15 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                     if constexpr (Tr::kV) { v[k][j] = __float_as_uint(v0); v[k][j + 1] = __float_as_uint(v1); }
                 }
             }
-            st_cs_v4(a.W + e, w[k]);
-            if constexpr (BF16S) {
-                if constexpr (Tr::kM) st_cs_v4(static_cast<uint16_t*>(a.m) + e, m[k]);
-                if constexpr (Tr::kV) st_cs_v4(static_cast<uint16_t*>(a.v) + e, v[k]);
-            } else {
-                if constexpr (Tr::kM) st_cs_v8(static_cast<float*>(a.m) + e, m[k]);
-                if constexpr (Tr::kV) st_cs_v8(static_cast<float*>(a.v) + e, v[k]);
+            if (ok[k]) {
+                st_cs_v4(a.W + e, w[k]);
+                if constexpr (BF16S) {
+                    if constexpr (Tr::kM) st_cs_v4(static_cast<uint16_t*>(a.m) + e, m[k]);
+                    if constexpr (Tr::kV) st_cs_v4(static_cast<uint16_t*>(a.v) + e, v[k]);
+                } else {
+                    if constexpr (Tr::kM) st_cs_v8(static_cast<float*>(a.m) + e, m[k]);
+                    if constexpr (Tr::kV) st_cs_v8(static_cast<float*>(a.v) + e, v[k]);
+                }
             }
         }
     }
@@ -280,7 +294,8 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
 
 // Input gradient: TMEM lane = token row, so each thread rounds its own row's 32-column runs to
 // bfloat16 and stores them as two 32-byte pieces.  Rows past the last token (the tail tile when T is
-// not a multiple of the tile height) are computed on TMA's zero fill and not stored.
+// not a multiple of the tile height) are computed on TMA's zero fill and not stored; past the last
+// column (d_in a multiple of 8 only) a 16-column piece shrinks to its first 8 or is skipped.
 template <int WIDTH>
 __device__ __forceinline__ void epi_store_dx(const TileArgs& a, int row0, int col0, uint32_t taddr) {
     const int row = row0 + static_cast<int>(threadIdx.x & 31u);
@@ -294,8 +309,23 @@ __device__ __forceinline__ void epi_store_dx(const TileArgs& a, int row0, int co
 #pragma unroll
         for (int j = 0; j < 16; ++j) p[j >> 3][j & 7] = pack_bf16x2_rn(g[2 * j], g[2 * j + 1]);
         if (row < a.T) {
-            st_v8(out + c, p[0]);
-            st_v8(out + c + 16, p[1]);
+            // rows start 32-byte aligned only when d_in is a multiple of 16; else 16-byte stores
+            const bool wide = (a.d_in & 15) == 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int left = a.d_in - (col0 + c + 16 * h);  // columns of this 16-run inside the layer
+                if (wide && left >= 16) {
+                    st_v8(out + c + 16 * h, p[h]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        if (left >= 8 * (q + 1)) {
+                            const uint32_t r4[4] = {p[h][4 * q], p[h][4 * q + 1], p[h][4 * q + 2], p[h][4 * q + 3]};
+                            st_v4(out + c + 16 * h + 8 * q, r4);
+                        }
+                    }
+                }
+            }
         }
     }
 }
@@ -317,8 +347,9 @@ struct Int8RowIn {
 };
 
 template <int OPT>
-__device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e_row, Int8RowIn<OPT>& in) {
+__device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e_row, bool ok, Int8RowIn<OPT>& in) {
     using Tr = OptTraits<OPT>;
+    if (!ok) e_row = 0;  // a row past the layer's last reads the first (always valid) and stores nothing
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         ld_cs_v4(a.W + e_row + 32 * h, in.w[h]);
@@ -330,8 +361,8 @@ __device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e_row, I
 }
 
 template <int OPT>
-__device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row, const uint8_t* strip, int k,
-                                                Int8RowIn<OPT>& in) {
+__device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row, bool ok, const uint8_t* strip,
+                                                int k, Int8RowIn<OPT>& in) {
     using Tr = OptTraits<OPT>;
     // pass 1: absmax of the row block's new moments
     float am = 0.f, av = 0.f;
@@ -374,11 +405,13 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
             if constexpr (Tr::kM) mo[j >> 2] |= int8_code(mm, nms) << (8 * (j & 3));
             if constexpr (Tr::kV) vo[j >> 2] |= int8_code(vv, nvs) << (8 * (j & 3));
         }
-        st_cs_v4(a.W + e, in.w[h]);
-        if constexpr (Tr::kM) st_cs_v2(static_cast<int8_t*>(a.m) + e, mo);
-        if constexpr (Tr::kV) st_cs_v2(static_cast<int8_t*>(a.v) + e, vo);
+        if (ok) {
+            st_cs_v4(a.W + e, in.w[h]);
+            if constexpr (Tr::kM) st_cs_v2(static_cast<int8_t*>(a.m) + e, mo);
+            if constexpr (Tr::kV) st_cs_v2(static_cast<int8_t*>(a.v) + e, vo);
+        }
     }
-    if ((threadIdx.x & 3u) == 0) {
+    if (ok && (threadIdx.x & 3u) == 0) {
         if constexpr (Tr::kM) a.m_scales[e_row >> 6] = nms;
         if constexpr (Tr::kV) a.v_scales[e_row >> 6] = nvs;
     }
@@ -389,18 +422,23 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
                                              uint8_t* strip) {
     static_assert(WIDTH % 64 == 0, "whole quantisation blocks");
     const int lane = threadIdx.x & 31;
-    const size_t lane_base = static_cast<size_t>(row0 + (lane >> 2)) * a.d_in + col0 + 8 * (lane & 3);
+    const int row = row0 + (lane >> 2);
+    const size_t lane_base = static_cast<size_t>(row) * a.d_in + col0 + 8 * (lane & 3);
     const size_t row_step = static_cast<size_t>(8) * a.d_in;
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 64) {
+        // d_in is a multiple of 64, so a 64-column block lies wholly inside or outside the layer:
+        // the same for every lane of the warp
+        if (col0 + c >= a.d_in) break;
         Int8RowIn<OPT> in[2];
-        int8_row_load<OPT>(a, lane_base + c, in[0]);
+        int8_row_load<OPT>(a, lane_base + c, row < a.d_out, in[0]);
         strip_store(taddr + c, strip);
         strip_store(taddr + c + 32, strip + 4096);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            if (k < 3) int8_row_load<OPT>(a, lane_base + (k + 1) * row_step + c, in[(k + 1) & 1]);
-            int8_row_update<OPT>(a, lane_base + k * row_step + c, strip, k, in[k & 1]);
+            if (k < 3)
+                int8_row_load<OPT>(a, lane_base + (k + 1) * row_step + c, row + 8 * (k + 1) < a.d_out, in[(k + 1) & 1]);
+            int8_row_update<OPT>(a, lane_base + k * row_step + c, row + 8 * k < a.d_out, strip, k, in[k & 1]);
         }
     }
 }

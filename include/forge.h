@@ -32,9 +32,12 @@
  *    aligned, owned by the caller.  The library allocates no device memory and
  *    keeps no pointer after a call returns.  W, m, v and qscales are updated in
  *    place.
- *  - Sizes: d_out and d_in multiples of 128 (the tile, §2 Methodology), T a
- *    multiple of 64 (the token slice of one pipeline stage) or T == 0; d_out or
- *    d_in == 0 is an empty layer and a no-op.
+ *  - Sizes: d_out and d_in multiples of 8 (a TMA row stride is a multiple of 16
+ *    bytes; with INT8 states d_in is a multiple of 64, so that a block of 64
+ *    never spans two rows) and any T >= 0.  The method's 128 x 128 tile (§2
+ *    Methodology) need not divide the layer: a tile reaching past the last row,
+ *    column or token computes on zero fill and writes nothing outside the layer.
+ *    T == 0 is a zero gradient; d_out or d_in == 0 is an empty layer and a no-op.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream) and return after the launch is queued.  Argument errors
  *    are detected on the host before anything is launched and are returned

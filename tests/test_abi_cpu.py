@@ -62,8 +62,8 @@ def _fused(L, shape, opt=0, step=1, W=A, m=A, v=A, q=None, dY=A, X=A, hp=True):
 @pytest.mark.parametrize("kw, code", [
     (dict(shape=None), 1),
     (dict(shape=_shape(d_out=500)), 1),
-    (dict(shape=_shape(d_in=200)), 1),
-    (dict(shape=_shape(T=100)), 1),
+    (dict(shape=_shape(d_in=204)), 1),               # d_out and d_in: multiples of 8
+    (dict(shape=_shape(state=1, d_in=200), q=A), 1),  # INT8 blocks of 64 may not span rows
     (dict(shape=_shape(T=-64)), 1),
     (dict(shape=_shape(reserved=1)), 1),
     (dict(shape=_shape(state=5)), 1),
@@ -98,7 +98,7 @@ def test_unused_moments_may_be_null(L):
 def test_dw_gemm_and_opt_step_reject_bad_arguments(L):
     assert L.forge_dw_gemm(A, A, None, ctypes.byref(_shape()), None) == 1
     assert L.forge_dw_gemm(A, A, A + 4, ctypes.byref(_shape()), None) == 3
-    assert L.forge_dw_gemm(A, A, A, ctypes.byref(_shape(d_in=64)), None) == 1
+    assert L.forge_dw_gemm(A, A, A, ctypes.byref(_shape(d_in=60)), None) == 1
     hp = fg.hparams_struct()
     assert L.forge_opt_step(A, None, A, A, None, 0, ctypes.byref(hp), ctypes.byref(_shape()), 1, 0, None) == 1
     assert L.forge_opt_step(A + 4, A, A, A, None, 0, ctypes.byref(hp), ctypes.byref(_shape()), 1, 0, None) == 3
@@ -111,7 +111,7 @@ def test_dx_gemm_rejects_bad_arguments(L):
     assert L.forge_dx_gemm(A, A, A + 2, s, None) == 3
     assert L.forge_dx_gemm(None, A, A, s, None) == 1
     assert L.forge_dx_gemm(A, A + 16, A, s, None) == 3
-    assert L.forge_dx_gemm(A, A, A, ctypes.byref(_shape(d_in=200)), None) == 1
+    assert L.forge_dx_gemm(A, A, A, ctypes.byref(_shape(d_in=204)), None) == 1
     assert L.forge_dx_gemm(A, A, A, None, None) == 1
     # empty dX: nothing is checked beyond the shape and nothing runs
     assert L.forge_dx_gemm(None, None, None, ctypes.byref(_shape(T=0)), None) == 0
@@ -129,7 +129,7 @@ def _backward(L, shape, dX=A, **kw):
 def test_linear_backward_checks_both_calls_before_launching(L):
     assert _backward(L, _shape(), dX=None) == 1        # dX missing: nothing launched
     assert _backward(L, _shape(), dX=A + 8) == 3
-    assert _backward(L, _shape(T=100)) == 1            # the weight step needs T a multiple of 64
+    assert _backward(L, _shape(d_out=100)) == 1        # d_out a multiple of 8
     assert _backward(L, _shape(), step=0) == 1
     assert _backward(L, _shape(), m=None) == 1
     if not _cuda_available():
