@@ -190,3 +190,27 @@ def sample_positions(d_out: int, d_in: int, n: int, seed: int, block: int = 1) -
     rows = (flat // (d_in // block)).tolist()
     cols = ((flat % (d_in // block)) * block).tolist()
     return rows, cols
+
+
+def fp8_e4m3(t: torch.Tensor) -> Tuple[torch.Tensor, float]:
+    """Per-tensor E4M3 codes of a float32 tensor, as an FP8 training recipe hands them over:
+    scale = amax / 448 (the largest E4M3 magnitude), codes = PyTorch's float8_e4m3fn cast of t / scale.
+    Returns (uint8 codes, scale)."""
+    t = t.float()
+    amax = float(t.abs().max()) if t.numel() else 0.0
+    scale = float(torch.tensor(amax / 448.0 if amax > 0 else 1.0, dtype=torch.float32))
+    codes = (t / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
+
+
+def activations_fp8(wl: Workload, layer_index: int, step: int, seed: int = 0, device="cpu"):
+    """(dY codes [T, d_out], s_dY, X codes [T, d_in], s_X): the layer's activations drawn as for
+    ``activations`` (float32, same seeds) and quantised per tensor to E4M3."""
+    l = wl.layers[layer_index]
+    dy = torch.randn(wl.T, l.d_out, generator=_gen(layer_seed(seed, layer_index, "dy", step), device),
+                     device=device) * wl.dy_std
+    x = torch.randn(wl.T, l.d_in, generator=_gen(layer_seed(seed, layer_index, "x", step), device),
+                    device=device) * wl.x_std
+    dyq, s_dy = fp8_e4m3(dy)
+    xq, s_x = fp8_e4m3(x)
+    return dyq, s_dy, xq, s_x
