@@ -9,6 +9,8 @@ Entry points (same names as the C ABI in include/forge.h):
   fused_dw_step(dY, X, W, m, v, qscales, opt, hp, step, seed, stream=None)
   dw_gemm(dY, X, dW, stream=None)
   dx_gemm(dY, W, dX, stream=None)
+  fused_dw_step_e4m3(dY8, X8, dy_scale, x_scale, W, m, v, qscales, opt, hp, step, seed, stream=None)
+  dw_gemm_e4m3(dY8, X8, dy_scale, x_scale, dW, stream=None)
   linear_backward(dY, X, W, m, v, qscales, dX, opt, hp, step, seed, stream=None)
   opt_step(dW, W, m, v, qscales, opt, hp, step, seed, stream=None)
   sync_status(stream=None), set_wait_limit_ns(ns), launch_count()
@@ -21,7 +23,7 @@ from typing import Any, Optional
 
 __all__ = [
     "OPT_KINDS", "STATE_FP32", "STATE_INT8_B64", "STATE_BF16", "ForgeError", "ForgeUnavailable", "lib", "library_path",
-    "fused_dw_step", "dw_gemm", "dx_gemm", "linear_backward", "opt_step", "sync_status", "set_wait_limit_ns", "launch_count", "build",
+    "fused_dw_step", "dw_gemm", "dx_gemm", "linear_backward", "opt_step", "fused_dw_step_e4m3", "dw_gemm_e4m3", "sync_status", "set_wait_limit_ns", "launch_count", "build",
     "ForgeShape", "ForgeHparams", "hparams_struct",
 ]
 
@@ -87,6 +89,12 @@ def lib() -> ctypes.CDLL:
     L.forge_fused_dw_step.restype = ctypes.c_int
     L.forge_dw_gemm.argtypes = [vp, vp, vp, ctypes.POINTER(ForgeShape), vp]
     L.forge_dw_gemm.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    L.forge_fused_dw_step_e4m3.argtypes = [vp, vp, f32, f32, vp, vp, vp, vp, ctypes.c_int,
+                                           ctypes.POINTER(ForgeHparams), ctypes.POINTER(ForgeShape), i64, u64, vp]
+    L.forge_fused_dw_step_e4m3.restype = ctypes.c_int
+    L.forge_dw_gemm_e4m3.argtypes = [vp, vp, f32, f32, vp, ctypes.POINTER(ForgeShape), vp]
+    L.forge_dw_gemm_e4m3.restype = ctypes.c_int
     L.forge_dx_gemm.argtypes = [vp, vp, vp, ctypes.POINTER(ForgeShape), vp]
     L.forge_dx_gemm.restype = ctypes.c_int
     L.forge_linear_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.POINTER(ForgeHparams),
@@ -185,6 +193,27 @@ def dw_gemm(dY, X, dW, stream=None) -> None:
     T, d_out = dY.shape
     shape = _shape(T, d_out, X.shape[1], STATE_FP32)
     _check(lib().forge_dw_gemm(_ptr(dY), _ptr(X), _ptr(dW), ctypes.byref(shape), _stream(stream)), "forge_dw_gemm")
+
+
+def fused_dw_step_e4m3(dY, X, dy_scale: float, x_scale: float, W, m=None, v=None, qscales=None, opt: str = "adamw",
+                       hp: Any = None, step: int = 1, seed: int = 0, stream=None) -> None:
+    """The fused step with E4M3 operands: dY [T, d_out] and X [T, d_in] one-byte codes (uint8 or
+    float8_e4m3fn tensors) with per-tensor scales; everything else as fused_dw_step."""
+    T, d_out = dY.shape
+    d_in = X.shape[1]
+    shape = _shape(T, d_out, d_in, _state_of(m, v))
+    st = lib().forge_fused_dw_step_e4m3(_ptr(dY), _ptr(X), float(dy_scale), float(x_scale), _ptr(W), _ptr(m),
+                                        _ptr(v), _ptr(qscales), OPT_KINDS[opt], ctypes.byref(hparams_struct(hp)),
+                                        ctypes.byref(shape), int(step), int(seed) & (2**64 - 1), _stream(stream))
+    _check(st, "forge_fused_dw_step_e4m3")
+
+
+def dw_gemm_e4m3(dY, X, dy_scale: float, x_scale: float, dW, stream=None) -> None:
+    """dW [d_out, d_in] FP32 = dy_scale * x_scale * (dY^T X) from E4M3 codes."""
+    T, d_out = dY.shape
+    shape = _shape(T, d_out, X.shape[1], STATE_FP32)
+    _check(lib().forge_dw_gemm_e4m3(_ptr(dY), _ptr(X), float(dy_scale), float(x_scale), _ptr(dW), ctypes.byref(shape),
+                                    _stream(stream)), "forge_dw_gemm_e4m3")
 
 
 def dx_gemm(dY, W, dX, stream=None) -> None:

@@ -142,16 +142,18 @@ OptScalars derive_scalars(forge_opt_kind k, const forge_hparams& hp, int64_t ste
     return s;
 }
 
-forge_status make_operand_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows) {
-    // A [rows, cols] bf16 row-major operand, read in boxes of 64 columns x 64 rows with the
-    // 128-byte swizzle (each box row is exactly one 128-byte swizzle span).
+forge_status make_operand_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, bool e4m3 = false) {
+    // A [rows, cols] row-major operand, bf16 or E4M3, read in boxes of 64 rows whose rows are
+    // exactly one 128-byte swizzle span (64 bf16 or 128 E4M3 columns).
+    const int64_t esize = e4m3 ? 1 : 2;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(forge::kBK)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esize)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 64};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_CUDA;
 }
 
@@ -194,26 +196,26 @@ forge_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : F
 using TileFn = cudaError_t (*)(const forge::TileLaunch&);
 using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
 
-template <int OPT, int BN, int CL>
+template <int OPT, int BN, int CL, int OPS>
 TileFn tile_fn_state(int state) {
     using namespace forge;
-    if (state == FORGE_STATE_INT8_B64) return launch_tile<OPT, kEpiOptINT8, BN, CL>;
-    if (state == FORGE_STATE_BF16) return launch_tile<OPT, kEpiOptBF16, BN, CL>;
-    return launch_tile<OPT, kEpiOptFP32, BN, CL>;
+    if (state == FORGE_STATE_INT8_B64) return launch_tile<OPT, kEpiOptINT8, BN, CL, OPS>;
+    if (state == FORGE_STATE_BF16) return launch_tile<OPT, kEpiOptBF16, BN, CL, OPS>;
+    return launch_tile<OPT, kEpiOptFP32, BN, CL, OPS>;
 }
 
-template <int BN, int CL>
+template <int BN, int CL, int OPS>
 TileFn tile_fn_v(forge_opt_kind k, int state) {
     using namespace forge;
     switch (k) {
-        case FORGE_ADAMW: return tile_fn_state<kAdamW, BN, CL>(state);
-        case FORGE_NADAM: return tile_fn_state<kNAdam, BN, CL>(state);
-        case FORGE_RADAM: return tile_fn_state<kRAdam, BN, CL>(state);
-        case FORGE_LION: return tile_fn_state<kLion, BN, CL>(state);
-        case FORGE_RMSPROP: return tile_fn_state<kRMSprop, BN, CL>(state);
-        case FORGE_ADAGRAD: return tile_fn_state<kAdaGrad, BN, CL>(state);
-        case FORGE_SGD: return state == FORGE_STATE_FP32 ? launch_tile<kSGD, kEpiOptFP32, BN, CL> : nullptr;
-        case FORGE_SGD_MOMENTUM: return tile_fn_state<kSGDMomentum, BN, CL>(state);
+        case FORGE_ADAMW: return tile_fn_state<kAdamW, BN, CL, OPS>(state);
+        case FORGE_NADAM: return tile_fn_state<kNAdam, BN, CL, OPS>(state);
+        case FORGE_RADAM: return tile_fn_state<kRAdam, BN, CL, OPS>(state);
+        case FORGE_LION: return tile_fn_state<kLion, BN, CL, OPS>(state);
+        case FORGE_RMSPROP: return tile_fn_state<kRMSprop, BN, CL, OPS>(state);
+        case FORGE_ADAGRAD: return tile_fn_state<kAdaGrad, BN, CL, OPS>(state);
+        case FORGE_SGD: return state == FORGE_STATE_FP32 ? launch_tile<kSGD, kEpiOptFP32, BN, CL, OPS> : nullptr;
+        case FORGE_SGD_MOMENTUM: return tile_fn_state<kSGDMomentum, BN, CL, OPS>(state);
     }
     return nullptr;
 }
@@ -253,21 +255,27 @@ TileShape pick_dx_shape(int64_t T, int64_t d_out, int64_t d_in) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-TileFn tile_fn(forge_opt_kind k, int state, int epi, TileShape t) {
+template <int OPS>
+TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t) {
     using namespace forge;
     if (epi == kEpiDX) {
-        if (t.cl == 4) return launch_tile<0, kEpiDX, 256, 4>;
-        if (t.cl == 2) return launch_tile<0, kEpiDX, 256, 2>;
-        return t.bn == 256 ? launch_tile<0, kEpiDX, 256, 1> : launch_tile<0, kEpiDX, 128, 1>;
+        if constexpr (OPS != kOpsBF16) return nullptr;
+        if (t.cl == 4) return launch_tile<0, kEpiDX, 256, 4, kOpsBF16>;
+        if (t.cl == 2) return launch_tile<0, kEpiDX, 256, 2, kOpsBF16>;
+        return t.bn == 256 ? launch_tile<0, kEpiDX, 256, 1, kOpsBF16> : launch_tile<0, kEpiDX, 128, 1, kOpsBF16>;
     }
     if (epi == kEpiStoreGrad) {
-        if (t.cl == 4) return launch_tile<0, kEpiStoreGrad, 256, 4>;
-        if (t.cl == 2) return launch_tile<0, kEpiStoreGrad, 256, 2>;
-        return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1> : launch_tile<0, kEpiStoreGrad, 128, 1>;
+        if (t.cl == 4) return launch_tile<0, kEpiStoreGrad, 256, 4, OPS>;
+        if (t.cl == 2) return launch_tile<0, kEpiStoreGrad, 256, 2, OPS>;
+        return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1, OPS> : launch_tile<0, kEpiStoreGrad, 128, 1, OPS>;
     }
-    if (t.cl == 4) return tile_fn_v<256, 4>(k, state);
-    if (t.cl == 2) return tile_fn_v<256, 2>(k, state);
-    return t.bn == 256 ? tile_fn_v<256, 1>(k, state) : tile_fn_v<128, 1>(k, state);
+    if (t.cl == 4) return tile_fn_v<256, 4, OPS>(k, state);
+    if (t.cl == 2) return tile_fn_v<256, 2, OPS>(k, state);
+    return t.bn == 256 ? tile_fn_v<256, 1, OPS>(k, state) : tile_fn_v<128, 1, OPS>(k, state);
+}
+
+TileFn tile_fn(forge_opt_kind k, int state, int epi, TileShape t, bool e4m3) {
+    return e4m3 ? tile_fn_ops<forge::kOpsE4M3>(k, state, epi, t) : tile_fn_ops<forge::kOpsBF16>(k, state, epi, t);
 }
 
 template <int OPT>
@@ -318,9 +326,11 @@ forge_status run_opt(const float* dW, void* W, void* m, void* v, float* qscales,
     return cuda_status(fn(a, grid, stream));
 }
 
+// e4m3: dY and X are E4M3 codes and the gradient tile is scaled by g_scale = s_dY * s_X.
 forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m, void* v, float* qscales,
                       forge_opt_kind k, int epi, const forge_hparams* hp, const forge_shape* shape, int64_t step,
-                      uint64_t seed, cudaStream_t stream, const DeviceInfo& dev) {
+                      uint64_t seed, cudaStream_t stream, const DeviceInfo& dev, bool e4m3 = false,
+                      float g_scale = 1.0f) {
     const bool int8 = shape->state == FORGE_STATE_INT8_B64;
     const uint64_t n = static_cast<uint64_t>(shape->d_out) * static_cast<uint64_t>(shape->d_in);
     forge::TileArgs a;
@@ -332,7 +342,8 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.tiles_m = static_cast<int>(ceil_div(a.d_out, forge::kBM * ts.cg));
     a.tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn * ts.pairs));
     a.num_tiles = a.tiles_m * a.tiles_n;
-    a.k_blocks = static_cast<int>(ceil_div(a.T, forge::kBK));
+    a.k_blocks = static_cast<int>(ceil_div(a.T, e4m3 ? 128 : forge::kBK));
+    a.g_scale = g_scale;
     // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
     a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
     a.dW = dW;
@@ -349,16 +360,16 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.withhold_first_stage = epi == forge::kEpiStoreGrad ? 0 : g_withhold_next.exchange(0);
 
     forge::TileLaunch l;
-    forge_status st = make_operand_map(&l.tmap_dy, dY, shape->d_out, shape->T);
+    forge_status st = make_operand_map(&l.tmap_dy, dY, shape->d_out, shape->T, e4m3);
     if (st != FORGE_OK) return st;
-    st = make_operand_map(&l.tmap_x, X, shape->d_in, shape->T);
+    st = make_operand_map(&l.tmap_x, X, shape->d_in, shape->T, e4m3);
     if (st != FORGE_OK) return st;
     l.args = &a;
     l.num_tiles = a.num_tiles;
     l.num_sms = dev.num_sms;
     l.stream = stream;
     // epi is kEpiStoreGrad (dW to memory) or kEpiOptFP32 (the fused step, whose epilogue follows the state dtype)
-    TileFn fn = tile_fn(k, shape->state, epi, ts);
+    TileFn fn = tile_fn(k, shape->state, epi, ts, e4m3);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(l));
@@ -394,7 +405,7 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
     l.num_tiles = a.num_tiles;
     l.num_sms = dev.num_sms;
     l.stream = stream;
-    TileFn fn = tile_fn(FORGE_SGD, FORGE_STATE_FP32, forge::kEpiDX, ts);
+    TileFn fn = tile_fn(FORGE_SGD, FORGE_STATE_FP32, forge::kEpiDX, ts, false);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(l));
@@ -417,14 +428,24 @@ forge_status check_fused(const void* dY, const void* X, const void* W, const voi
 
 forge_status launch_fused(const void* dY, const void* X, void* W, void* m, void* v, float* qscales,
                           forge_opt_kind k, const forge_hparams* hp, const forge_shape* shape, int64_t step,
-                          uint64_t seed, cudaStream_t stream) {
+                          uint64_t seed, cudaStream_t stream, bool e4m3 = false, float g_scale = 1.0f) {
     if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
     DeviceInfo* dev = nullptr;
     forge_status st = device_info(&dev);
     if (st != FORGE_OK) return st;
     if (shape->T == 0)  // no tokens: the gradient is exactly zero
         return run_opt(nullptr, W, m, v, qscales, k, hp, shape, step, seed, stream, *dev);
-    return run_tile(dY, X, nullptr, W, m, v, qscales, k, forge::kEpiOptFP32, hp, shape, step, seed, stream, *dev);
+    return run_tile(dY, X, nullptr, W, m, v, qscales, k, forge::kEpiOptFP32, hp, shape, step, seed, stream, *dev,
+                    e4m3, g_scale);
+}
+
+// E4M3 operands: rows of dY and X are d_out and d_in bytes, a multiple of 16 for TMA; the scales are
+// finite and positive.
+forge_status check_e4m3(const forge_shape* shape, float dy_scale, float x_scale) {
+    if (shape->d_out % 16 != 0 || shape->d_in % 16 != 0) return FORGE_ERR_INVALID_ARGUMENT;
+    if (!(dy_scale > 0.0f && dy_scale < INFINITY) || !(x_scale > 0.0f && x_scale < INFINITY))
+        return FORGE_ERR_INVALID_ARGUMENT;
+    return FORGE_OK;
 }
 
 forge_status check_dx(const void* dY, const void* W, const void* dX, const forge_shape* shape) {
@@ -461,6 +482,37 @@ forge_status forge_fused_dw_step(const void* dY, const void* X, void* W, void* m
     forge_status st = check_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step);
     if (st != FORGE_OK) return st;
     return launch_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream);
+}
+
+forge_status forge_fused_dw_step_e4m3(const void* dY, const void* X, float dy_scale, float x_scale, void* W, void* m,
+                                      void* v, float* qscales, forge_opt_kind opt_kind, const forge_hparams* hp,
+                                      const forge_shape* shape, int64_t step, uint64_t seed,
+                                      struct CUstream_st* stream) {
+    forge_status st = check_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step);
+    if (st != FORGE_OK) return st;
+    st = check_e4m3(shape, dy_scale, x_scale);
+    if (st != FORGE_OK) return st;
+    const float g_scale = dy_scale * x_scale;  // one binary32 rounding
+    return launch_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream, true, g_scale);
+}
+
+forge_status forge_dw_gemm_e4m3(const void* dY, const void* X, float dy_scale, float x_scale, float* dW,
+                                const forge_shape* shape, struct CUstream_st* stream) {
+    forge_status st = check_shape(shape);
+    if (st != FORGE_OK) return st;
+    st = check_e4m3(shape, dy_scale, x_scale);
+    if (st != FORGE_OK) return st;
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
+    if (dW == nullptr || (shape->T > 0 && (dY == nullptr || X == nullptr))) return FORGE_ERR_INVALID_ARGUMENT;
+    if (!aligned32(dW) || (shape->T > 0 && (!aligned32(dY) || !aligned32(X)))) return FORGE_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    if (shape->T == 0)
+        return cuda_status(cudaMemsetAsync(dW, 0, static_cast<size_t>(shape->d_out) * shape->d_in * sizeof(float),
+                                           stream));
+    return run_tile(dY, X, dW, nullptr, nullptr, nullptr, nullptr, FORGE_SGD, forge::kEpiStoreGrad, nullptr, shape,
+                    1, 0, stream, *dev, true, dy_scale * x_scale);
 }
 
 forge_status forge_dx_gemm(const void* dY, const void* W, void* dX, const forge_shape* shape,

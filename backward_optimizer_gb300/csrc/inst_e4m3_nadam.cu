@@ -1,0 +1,3 @@
+// Kernel instantiations with E4M3 operands for one optimizer (nadam).
+#include "instantiate.cuh"
+FORGE_INSTANTIATE_OPT_E4M3(forge::kNAdam)

@@ -9,11 +9,11 @@
 
 namespace forge {
 
-template <int OPT, int EPI, int BN, int CL>
+template <int OPT, int EPI, int BN, int CL, int OPS>
 cudaError_t launch_tile(const TileLaunch& l) {
     constexpr int CG = CL == 1 ? 1 : 2;
     using C = TileCfg<BN, CG, EPI>;
-    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT>;
+    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT, OPS>;
     static std::atomic<uint64_t> configured{0};  // one bit per device ordinal
     static std::atomic<int> max_clusters[64];    // co-resident clusters per device
     int dev = 0;
@@ -56,7 +56,7 @@ template <int OPT, int EPI, int BN, int CL>
 cudaError_t tile_grid(int num_tiles, int num_sms, int* ctas) {
     constexpr int CG = CL == 1 ? 1 : 2;
     using C = TileCfg<BN, CG, EPI>;
-    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT>;
+    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT, kOpsBF16>;
     int cap = num_sms;
     if (CL > 1) {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -87,11 +87,19 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 
 }  // namespace forge
 
-#define FORGE_INSTANTIATE_TILES(OPT, EPI)                                                      \
-    template cudaError_t forge::launch_tile<OPT, EPI, 128, 1>(const forge::TileLaunch&);       \
-    template cudaError_t forge::launch_tile<OPT, EPI, 256, 1>(const forge::TileLaunch&);       \
-    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2>(const forge::TileLaunch&);       \
-    template cudaError_t forge::launch_tile<OPT, EPI, 256, 4>(const forge::TileLaunch&);
+#define FORGE_INSTANTIATE_TILES_OPS(OPT, EPI, OPS)                                               \
+    template cudaError_t forge::launch_tile<OPT, EPI, 128, 1, OPS>(const forge::TileLaunch&);       \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 1, OPS>(const forge::TileLaunch&);       \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2, OPS>(const forge::TileLaunch&);       \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 4, OPS>(const forge::TileLaunch&);
+
+#define FORGE_INSTANTIATE_TILES(OPT, EPI) FORGE_INSTANTIATE_TILES_OPS(OPT, EPI, forge::kOpsBF16)
+
+// E4M3 operands, every state format.
+#define FORGE_INSTANTIATE_OPT_E4M3(OPT)                                    \
+    FORGE_INSTANTIATE_TILES_OPS(OPT, forge::kEpiOptFP32, forge::kOpsE4M3) \
+    FORGE_INSTANTIATE_TILES_OPS(OPT, forge::kEpiOptINT8, forge::kOpsE4M3) \
+    FORGE_INSTANTIATE_TILES_OPS(OPT, forge::kEpiOptBF16, forge::kOpsE4M3)
 
 #define FORGE_INSTANTIATE_OPT(OPT)                    \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptFP32) \

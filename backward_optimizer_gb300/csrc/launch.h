@@ -27,7 +27,8 @@ struct TileLaunch {
 // BN: tile columns (128, or 256 = two 128 x 128 tiles side by side).
 // CL: CTAs per cluster (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair; 4: two pairs
 // on a 256 x 2BN tile sharing their dY slices by multicast).
-template <int OPT, int EPI, int BN, int CL> cudaError_t launch_tile(const TileLaunch& l);
+// OPS: operand format of dY and X, 0 = bf16, 1 = E4M3 (the gradient tile is scaled by s_dY * s_X).
+template <int OPT, int EPI, int BN, int CL, int OPS> cudaError_t launch_tile(const TileLaunch& l);
 
 // CTAs a tile launch of the given shape would run (persistent grid size).
 cudaError_t tile_ctas(int bn, int cl, int num_tiles, int num_sms, int* ctas);

@@ -178,6 +178,26 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
             : "memory");
 }
 
+// The same for two E4M3 operands (kind::f8f6f4, K = 32 per instruction).
+template <int CG>
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
 // Arrive once on `bar` -- at the same shared-memory offset in every CTA of the cluster whose rank
 // bit is set in `mask` (CG = 2), or in this CTA (CG = 1) -- when every tcgen05 operation issued
 // so far by this thread has completed.
@@ -313,6 +333,16 @@ __device__ __forceinline__ void ld_cs_v2(const void* p, uint32_t (&r)[2]) {
 
 __device__ __forceinline__ void st_cs_v2(void* p, const uint32_t (&r)[2]) {
     asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(r[0]), "r"(r[1]) : "memory");
+}
+
+// Instruction descriptor of kind::f8f6f4 with A and B both E4M3 (format code 0), D f32.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                                          // D format: f32
+           | (0u << 7) | (0u << 10)                           // A, B format: E4M3
+           | (static_cast<uint32_t>(a_mn_major) << 15)
+           | (static_cast<uint32_t>(b_mn_major) << 16)
+           | (static_cast<uint32_t>(N >> 3) << 17)
+           | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Plain (default-cached) 256-bit store, for outputs the next kernel reads back.

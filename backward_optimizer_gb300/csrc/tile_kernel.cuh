@@ -46,6 +46,19 @@ constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
 
 enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3, kEpiOptBF16 = 4 };
 
+// Operand formats.  Either way a stage row is 128 bytes (the swizzle span) and a stage of one
+// operand is 16 KiB per 128 MN rows: 64 tokens of bf16, or 128 tokens of E4M3, whose products the
+// tensor core takes 32 tokens at a time (kind::f8f6f4) instead of 16.
+enum OperandKind : int { kOpsBF16 = 0, kOpsE4M3 = 1 };
+
+template <int OPS>
+struct OperandTraits {
+    static constexpr int kTok = OPS == kOpsE4M3 ? 128 : 64;          // tokens per pipeline stage
+    static constexpr int kMNPerRow = OPS == kOpsE4M3 ? 128 : 64;     // MN elements per 128-byte row
+    static constexpr int kBlockBytes = kTok * 128;                   // one MN block of a stage
+    static constexpr int kStepBytes = OPS == kOpsE4M3 ? 4096 : 2048;  // rows one MMA consumes (K)
+};
+
 template <int BN, int CG, int EPI>
 struct TileCfg {
     static_assert(BN == 128 || BN == 256, "tile width");
@@ -72,7 +85,8 @@ struct TileCfg {
 struct TileArgs {
     int d_out, d_in, T;
     int tiles_m, tiles_n, num_tiles, group_m;
-    int k_blocks;                 // 64-wide reduction slices per tile: T / 64 (dW), d_out / 64 (dX)
+    int k_blocks;                 // reduction slices per tile: T / 64 (dW; T / 128 for E4M3), d_out / 64 (dX)
+    float g_scale;                // E4M3 operands: s_dY * s_X, applied to the FP32 gradient tile
     float* dW;                    // kEpiStoreGrad: [d_out, d_in] FP32
     uint16_t* dX;                 // kEpiDX: [T, d_in] bf16; token rows >= T are not stored
     uint16_t* W;                  // bf16 [d_out, d_in]
@@ -147,11 +161,22 @@ __device__ __forceinline__ void st_v8_f32(float* p, const uint32_t (&r)[8]) {
 // 32 columns, so every warp-wide access touches 8 rows x one contiguous span instead of 32 rows.
 // The strip is written with its 16-byte chunks XOR-swizzled by (row mod 8), which makes both the
 // row-wise writes and the column-wise reads free of bank conflicts.
-__device__ __forceinline__ void strip_transpose(uint32_t taddr, uint8_t* strip, uint32_t (&out)[4][8]) {
+template <bool SCALE>
+__device__ __forceinline__ void scale_strip(uint32_t (&g)[32], float scale) {
+    if constexpr (SCALE) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] = __float_as_uint(__fmul_rn(__uint_as_float(g[i]), scale));
+    }
+}
+
+template <bool SCALE = false>
+__device__ __forceinline__ void strip_transpose(uint32_t taddr, uint8_t* strip, uint32_t (&out)[4][8],
+                                                float scale = 1.0f) {
     const uint32_t lane = threadIdx.x & 31u;
     uint32_t g[32];
     tmem_ld_32x32b_x32(taddr, g);
     tmem_ld_wait(g);
+    scale_strip<SCALE>(g, scale);
     const uint32_t base = smem_addr(strip);
 #pragma unroll
     for (uint32_t j = 0; j < 8; ++j)
@@ -173,11 +198,13 @@ __device__ __forceinline__ void strip_transpose(uint32_t taddr, uint8_t* strip, 
 
 // The two halves of strip_transpose, for callers that consume one row group at a time: the strip
 // is written once, then lane l reads the 8 columns it owns of row (l div 4) + 8k.
-__device__ __forceinline__ void strip_store(uint32_t taddr, uint8_t* strip) {
+template <bool SCALE = false>
+__device__ __forceinline__ void strip_store(uint32_t taddr, uint8_t* strip, float scale = 1.0f) {
     const uint32_t lane = threadIdx.x & 31u;
     uint32_t g[32];
     tmem_ld_32x32b_x32(taddr, g);
     tmem_ld_wait(g);
+    scale_strip<SCALE>(g, scale);
     const uint32_t base = smem_addr(strip);
     __syncwarp();  // earlier reads of the strip are complete
 #pragma unroll
@@ -197,7 +224,7 @@ __device__ __forceinline__ void strip_load_row(const uint8_t* strip, int k, uint
         ld_shared_v4(base + r * 128u + (((2u * (lane & 3u) + h) ^ sub_row) << 4), &out[4 * h]);
 }
 
-template <int WIDTH>
+template <int WIDTH, bool SCALE>
 __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int col0, uint32_t taddr,
                                                uint8_t* strip) {
     const int lane = threadIdx.x & 31;
@@ -206,7 +233,7 @@ __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int 
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 32) {
         uint32_t t[4][8];
-        strip_transpose(taddr + c, strip, t);
+        strip_transpose<SCALE>(taddr + c, strip, t, a.g_scale);
         if (col + c < a.d_in) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -217,7 +244,7 @@ __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int 
 
 // Dense states: binary32 (BF16S = false) or bfloat16 rounded stochastically with their own Philox
 // streams (BF16S = true).  The update always runs on binary32 moments; only their storage differs.
-template <int OPT, int WIDTH, bool BF16S>
+template <int OPT, int WIDTH, bool BF16S, bool SCALE>
 __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int col0, uint32_t taddr,
                                               uint8_t* strip) {
     using Tr = OptTraits<OPT>;
@@ -248,7 +275,7 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
             }
         }
         uint32_t g[4][8];
-        strip_transpose(taddr + c, strip, g);
+        strip_transpose<SCALE>(taddr + c, strip, g, a.g_scale);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const size_t e = lane_base + k * row_step + c;
@@ -417,7 +444,7 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
     }
 }
 
-template <int OPT, int WIDTH>
+template <int OPT, int WIDTH, bool SCALE>
 __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int col0, uint32_t taddr,
                                              uint8_t* strip) {
     static_assert(WIDTH % 64 == 0, "whole quantisation blocks");
@@ -432,8 +459,8 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
         if (col0 + c >= a.d_in) break;
         Int8RowIn<OPT> in[2];
         int8_row_load<OPT>(a, lane_base + c, row < a.d_out, in[0]);
-        strip_store(taddr + c, strip);
-        strip_store(taddr + c + 32, strip + 4096);
+        strip_store<SCALE>(taddr + c, strip, a.g_scale);
+        strip_store<SCALE>(taddr + c + 32, strip + 4096, a.g_scale);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             if (k < 3)
@@ -457,11 +484,14 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
 //         halving the dY bytes pulled from L2.  A stage slot is free again only when both pairs'
 //         MMAs have consumed it, so each pair's commit of a stage arrives in all four CTAs.
 
-template <int BN, int CL, int EPI, int OPT>
+template <int BN, int CL, int EPI, int OPT, int OPS>
 __global__ void __launch_bounds__(kThreads, 1)
     forge_tile_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
                       const TileArgs a) {
     static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
+    static_assert(OPS == kOpsBF16 || EPI != kEpiDX, "the input gradient takes bf16 operands");
+    using O = OperandTraits<OPS>;
+    constexpr bool kScale = OPS == kOpsE4M3;
     constexpr int CG = CL == 1 ? 1 : 2;       // CTAs per MMA (cta_group)
     constexpr int kPairs = CL == 4 ? 2 : 1;   // MMA groups per cluster sharing dY
     using C = TileCfg<BN, CG, EPI>;
@@ -540,27 +570,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], CG * C::kStageBytes);
                     uint8_t* a_dst = sA + stage * C::kABytes;
                     uint8_t* b_dst = sB + stage * C::kBBytes;
-                    const int k0 = kb * kBK;
+                    const int k0 = kb * O::kTok;
                     // A box j holds rows row_a + 64j .. +63 of this CTA's 128 A rows; dY's tensor map
                     // has d_out innermost, so its coordinates are (row, token) for dY^T and
                     // (d_out slice, token row) for the K-major dY of dX
-                    if constexpr (kPairs == 2) {
-                        // box `pair`, for this CTA and its counterpart in the other pair (cluster
-                        // ranks rank and rank + 2)
-                        const int r = row_a + 64 * static_cast<int>(pair);
-                        tma_load_2d_multicast(a_dst + pair * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
-                                              kAKMajor ? r : k0, static_cast<uint16_t>(0x5u << rank), keep);
-                    } else {
+                    if constexpr (OPS == kOpsE4M3) {
+                        // E4M3: 128 rows of dY^T fill one 128-byte row; box j is token half j of the
+                        // stage (64 token rows at j * 8 KiB)
+                        if constexpr (kPairs == 2) {
+                            tma_load_2d_multicast(a_dst + pair * 8192, &tmap_dy, bar, row_a, k0 + 64 * static_cast<int>(pair),
+                                                  static_cast<uint16_t>(0x5u << rank), keep);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const int r = row_a + 64 * j;
-                            tma_load_2d_cg<CG>(a_dst + j * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
-                                               kAKMajor ? r : k0, keep);
+                            for (int j = 0; j < 2; ++j)
+                                tma_load_2d_cg<CG>(a_dst + j * 8192, &tmap_dy, bar, row_a, k0 + 64 * j, keep);
                         }
-                    }
 #pragma unroll
-                    for (int j = 0; j < C::kBLoad / 64; ++j)
-                        tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep);
+                        for (int j = 0; j < C::kBLoad / 128; ++j)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                tma_load_2d_cg<CG>(b_dst + j * O::kBlockBytes + h * 8192, &tmap_x, bar, col_b + 128 * j,
+                                                   k0 + 64 * h, keep);
+                    } else {
+                        if constexpr (kPairs == 2) {
+                            // box `pair`, for this CTA and its counterpart in the other pair (cluster
+                            // ranks rank and rank + 2)
+                            const int r = row_a + 64 * static_cast<int>(pair);
+                            tma_load_2d_multicast(a_dst + pair * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
+                                                  kAKMajor ? r : k0, static_cast<uint16_t>(0x5u << rank), keep);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const int r = row_a + 64 * j;
+                                tma_load_2d_cg<CG>(a_dst + j * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
+                                                   kAKMajor ? r : k0, keep);
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < C::kBLoad / 64; ++j)
+                            tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep);
+                    }
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -582,7 +631,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ------------------------------------------------ MMA issuer (the even CTA of a pair)
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM * CG, BN, !kAKMajor, true);
+            constexpr uint32_t idesc = OPS == kOpsE4M3 ? idesc_e4m3_f32(kBM * CG, BN, true, true)
+                                                       : idesc_bf16_f32(kBM * CG, BN, !kAKMajor, true);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued_any = false;
@@ -602,10 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // bytes apart (leading byte offset) and 8-row groups 1024 bytes apart
                         // (stride).  K-major (dY for dX): 16 K = 32 bytes within each 128-byte
                         // swizzled row, 8-row groups 1024 bytes apart; the leading offset is unused.
+                        // E4M3: 32 tokens per MMA, 4096 bytes; MN blocks of 128 elements 16 KiB apart
                         const uint64_t ad = kAKMajor ? smem_desc_sw128(a_base + kk * 32, 16, 1024)
-                                                     : smem_desc_sw128(a_base + kk * 2048, kBK * 128, 1024);
-                        const uint64_t bd = smem_desc_sw128(b_base + kk * 2048, kBK * 128, 1024);
-                        tc_mma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                                                     : smem_desc_sw128(a_base + kk * O::kStepBytes, O::kBlockBytes, 1024);
+                        const uint64_t bd = smem_desc_sw128(b_base + kk * O::kStepBytes, O::kBlockBytes, 1024);
+                        if constexpr (OPS == kOpsE4M3) tc_mma_e4m3<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        else tc_mma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
                     // the slot is free once read: tell every CTA whose copies fill it
@@ -644,10 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + half * kWidth);
             uint8_t* strip = strips + e * C::kStripBytes;
             if constexpr (EPI == kEpiDX) epi_store_dx<kWidth>(a, row0, col0, taddr);
-            else if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth>(a, row0, col0, taddr, strip);
-            else if constexpr (EPI == kEpiOptFP32) epi_opt_dense<OPT, kWidth, false>(a, row0, col0, taddr, strip);
-            else if constexpr (EPI == kEpiOptBF16) epi_opt_dense<OPT, kWidth, true>(a, row0, col0, taddr, strip);
-            else epi_opt_int8<OPT, kWidth>(a, row0, col0, taddr, strip);
+            else if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth, kScale>(a, row0, col0, taddr, strip);
+            else if constexpr (EPI == kEpiOptFP32) epi_opt_dense<OPT, kWidth, false, kScale>(a, row0, col0, taddr, strip);
+            else if constexpr (EPI == kEpiOptBF16) epi_opt_dense<OPT, kWidth, true, kScale>(a, row0, col0, taddr, strip);
+            else epi_opt_int8<OPT, kWidth, kScale>(a, row0, col0, taddr, strip);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {

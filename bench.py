@@ -149,14 +149,18 @@ def _act_key(wl, i):
     return (l.d_out, l.d_in) if len(wl.layers) > 8 else i
 
 
-def _make_layer(wl, i, opt, state, device, seed, act_cache):
-    """One layer's W/m/v (its own) and dY/X (see _act_key)."""
+def _make_layer(wl, i, opt, state, device, seed, act_cache, operands="bf16"):
+    """One layer's W/m/v (its own) and dY/X (see _act_key): bf16, or E4M3 codes with per-tensor scales."""
     import torch
-    from workloads import activations, layer_state
+    from workloads import activations, activations_fp8, layer_state
     key = _act_key(wl, i)
     if key not in act_cache:
-        act_cache[key] = activations(wl, i, 1, seed, device=device)
-    dy, x = act_cache[key]
+        if operands == "e4m3":
+            dyq, s_dy, xq, s_x = activations_fp8(wl, i, 1, seed, device=device)
+            act_cache[key] = (dyq, xq, s_dy, s_x)
+        else:
+            act_cache[key] = activations(wl, i, 1, seed, device=device) + (1.0, 1.0)
+    dy, x, s_dy, s_x = act_cache[key]
     w, m, v = layer_state(wl, i, opt, seed, device=device)
     q = None
     if state == "int8":
@@ -168,7 +172,7 @@ def _make_layer(wl, i, opt, state, device, seed, act_cache):
     elif state == "bf16":
         m = None if m is None else m.to(torch.bfloat16)
         v = None if v is None else v.to(torch.bfloat16)
-    return dict(dy=dy, x=x, w=w, m=m, v=v, q=q)
+    return dict(dy=dy, x=x, w=w, m=m, v=v, q=q, s_dy=s_dy, s_x=s_x)
 
 
 def run_gpu(args, rank, world):
@@ -183,16 +187,25 @@ def run_gpu(args, rank, world):
     hp = default_hparams(args.opt)
     t_step = wl.steps[-1]
     act_cache = {}
-    layers = [_make_layer(wl, i, args.opt, args.state, dev, 1000 * rank, act_cache) for i in range(len(wl.layers))]
+    e4m3 = args.operands == "e4m3"
+    layers = [_make_layer(wl, i, args.opt, args.state, dev, 1000 * rank, act_cache, args.operands)
+              for i in range(len(wl.layers))]
     stream = torch.cuda.current_stream()
     flops_step = wl.flops_per_step()
+
+    def fused(i, L):
+        if e4m3:
+            fg.fused_dw_step_e4m3(L["dy"], L["x"], L["s_dy"], L["s_x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp,
+                                  t_step, seed=0x5EED + i, stream=stream)
+        else:
+            fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step,
+                             seed=0x5EED + i, stream=stream)
 
     def fused_pass(ev=None):
         for i, L in enumerate(layers):
             if ev is not None:
                 ev[i][0].record(stream)
-            fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step,
-                             seed=0x5EED + i, stream=stream)
+            fused(i, L)
             if ev is not None:
                 ev[i][1].record(stream)
 
@@ -235,7 +248,10 @@ def run_gpu(args, rank, world):
 
     def unfused_pass():
         for L, dW in zip(layers, dws):
-            fg.dw_gemm(L["dy"], L["x"], dW, stream=stream)
+            if e4m3:
+                fg.dw_gemm_e4m3(L["dy"], L["x"], L["s_dy"], L["s_x"], dW, stream=stream)
+            else:
+                fg.dw_gemm(L["dy"], L["x"], dW, stream=stream)
         for i, (L, dW) in enumerate(zip(layers, dws)):
             fg.opt_step(dW, L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step, seed=0x5EED + i, stream=stream)
 
@@ -256,10 +272,10 @@ def run_gpu(args, rank, world):
 
     # ---- end to end: dY/X from pinned host memory each step, updated W copied back
     # (one pinned host copy per distinct layer shape; every layer's dY/X is copied in each step)
-    host_act = {k: (dy.cpu().pin_memory(), x.cpu().pin_memory()) for k, (dy, x) in act_cache.items()}
+    host_act = {k: (a[0].cpu().pin_memory(), a[1].cpu().pin_memory()) for k, a in act_cache.items()}
     host_in = [host_act[_act_key(wl, i)] for i in range(len(wl.layers))]
-    out_by_key = {k: torch.empty((dy.shape[1], x.shape[1]), dtype=torch.bfloat16).pin_memory()
-                  for k, (dy, x) in act_cache.items()}
+    out_by_key = {k: torch.empty((a[0].shape[1], a[1].shape[1]), dtype=torch.bfloat16).pin_memory()
+                  for k, a in act_cache.items()}
     host_out = [out_by_key[_act_key(wl, i)] for i in range(len(wl.layers))]
     h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
@@ -268,8 +284,7 @@ def run_gpu(args, rank, world):
         for i, L in enumerate(layers):
             L["dy"].copy_(host_in[i][0], non_blocking=True)
             L["x"].copy_(host_in[i][1], non_blocking=True)
-            fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step,
-                             seed=0x5EED + i, stream=stream)
+            fused(i, L)
             host_out[i].copy_(L["w"], non_blocking=True)
 
     for _ in range(args.warmup):
@@ -303,8 +318,8 @@ def run_gpu(args, rank, world):
             fg.linear_backward(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], dX, args.opt, hp, t_step,
                                seed=0x5EED + i, stream=stream)
 
-    timed = {}
-    for name, fn in (("dx", dx_pass), ("backward", backward_pass)):
+    timed = {"dx": float("nan"), "backward": float("nan")}
+    for name, fn in () if e4m3 else (("dx", dx_pass), ("backward", backward_pass)):
         for _ in range(args.warmup):
             fn()
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -316,7 +331,7 @@ def run_gpu(args, rank, world):
         b1.record(stream)
         torch.cuda.synchronize()
         timed[name] = b0.elapsed_time(b1) / args.steps
-    dx_launch_ms = [a.elapsed_time(b) for step_ev in dx_ev for (a, b) in step_ev]
+    dx_launch_ms = [] if e4m3 else [a.elapsed_time(b) for step_ev in dx_ev for (a, b) in step_ev]
     status = fg.sync_status()
     if status != 0:
         raise RuntimeError(f"device status {status} in the dX / backward timing")
@@ -392,6 +407,8 @@ def main():
     ap.add_argument("--workload", default="llama8b-mlp")
     ap.add_argument("--opt", default="adamw")
     ap.add_argument("--state", default="fp32", choices=["fp32", "int8", "bf16"])
+    ap.add_argument("--operands", default="bf16", choices=["bf16", "e4m3"],
+                    help="dY/X format: bf16, or E4M3 codes with per-tensor scales")
     ap.add_argument("--oracle-rows", type=int, default=0, help="rows per layer of the oracle sample (0: sized by time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -404,6 +421,7 @@ def main():
     wl = WORKLOADS[args.workload]
     metric = "fused dW+AdamW TFLOP/s & step ms per layer sweep vs unfused; % of BF16 tensor peak"
     config = {"workload": f"{wl.name}: {wl.description}", "opt": args.opt, "state": args.state,
+              "operands": args.operands,
               "T": wl.T, "layers": [f"{l.name} {l.d_out}x{l.d_in}" for l in wl.layers[:7]],
               "n_layers": len(wl.layers), "l2": "inputs larger than L2 (W/m/v/dY/X per step >> 129 MB)"}
 
@@ -449,7 +467,12 @@ def main():
         return
 
     peaks, peaks_src = _peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    e4m3 = args.operands == "e4m3"
+    # E4M3 contractions take the FP8 peak: the measured bf16 peak times the nominal ratio 4.5 / 2.25
+    peak = 2.0 * bf16_peak if e4m3 else bf16_peak
+    peak_source = (f"2 x bf16_tflops of {peaks_src} (nominal fp8/bf16 dense ratio 4.5/2.25)" if e4m3
+                   else f"bf16_tflops of {peaks_src}")
     n_layers = len(r["wl"].layers)
     avg_launch_ms = statistics.mean(r["launch_ms"])
     flops_launch = r["flops_step"] / n_layers
@@ -458,7 +481,7 @@ def main():
     line = {
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+        "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16", "data": "synthetic", "config": config,
         "unfused": {"ms_per_step": r["unfused_ms"], "value": job_throughput(r["flops_step"], world, r["unfused_ms"]),
                     "speedup_fused": r["unfused_ms"] / r["ms_step"]},
         "grad_pool_bytes": {"fused_hbm": 0, "unfused_hbm": r["grad_pool_unfused"],
@@ -469,15 +492,17 @@ def main():
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": _ncu_traffic(args.workload, args.opt, args.state),
                      "kernel": "forge_tile_kernel (fused)", "avg_launch_ms": avg_launch_ms,
-                     "flops_per_launch": flops_launch, "peak_source": f"bf16_tflops of {peaks_src}"},
+                     "flops_per_launch": flops_launch, "peak_source": peak_source},
         "clocks": r["clocks"],
         # the layer's input gradient dX = dY W (same flops as dW) and the ordered layer backward
-        "dx": {"ms_per_step": r["dx_ms"], "value": job_throughput(r["flops_step"], world, r["dx_ms"]),
-               "unit": "TFLOP/s", "avg_launch_ms": statistics.mean(r["dx_launch_ms"]),
-               "frac": flops_launch / (statistics.mean(r["dx_launch_ms"]) * 1e-3) / 1e12 / peak},
-        "layer_backward": {"ms_per_step": r["bwd_ms"], "value": job_throughput(2 * r["flops_step"], world, r["bwd_ms"]),
-                           "unit": "TFLOP/s", "what": "dX then the fused step, per layer, one stream"},
     }
+    if r["dx_launch_ms"]:  # bf16 operands only: dX = dY W needs dY in bf16
+        line["dx"] = {"ms_per_step": r["dx_ms"], "value": job_throughput(r["flops_step"], world, r["dx_ms"]),
+                      "unit": "TFLOP/s", "avg_launch_ms": statistics.mean(r["dx_launch_ms"]),
+                      "frac": flops_launch / (statistics.mean(r["dx_launch_ms"]) * 1e-3) / 1e12 / bf16_peak}
+        line["layer_backward"] = {"ms_per_step": r["bwd_ms"],
+                                  "value": job_throughput(2 * r["flops_step"], world, r["bwd_ms"]),
+                                  "unit": "TFLOP/s", "what": "dX then the fused step, per layer, one stream"}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(line))

@@ -168,6 +168,28 @@ FORGE_API forge_status forge_opt_step(const float *dW, void *W, void *m, void *v
                             struct CUstream_st *stream);
 
 /*
+ * forge_fused_dw_step_e4m3 -- forge_fused_dw_step with FP8 operands (§4 Experimental
+ * results, "Composability": FORGE composes with FP8 quantisation and absorbs the
+ * dequantisation cost).  dY [T, d_out] and X [T, d_in] are E4M3 codes (OCP 8-bit
+ * format: 4 exponent bits, bias 7, 3 mantissa bits, no infinities), row-major, one
+ * byte each, with one binary32 scale per tensor: value = scale * decode(code).  The
+ * tensor core sums the code products in FP32 (kind::f8f6f4); the finished gradient
+ * tile is then multiplied by s = dy_scale * x_scale (one binary32 product, formed
+ * on the host) and the step proceeds exactly as in forge_fused_dw_step, for every
+ * state format.  d_out and d_in must be multiples of 16 (row strides of 16 bytes);
+ * both scales finite and positive.
+ */
+FORGE_API forge_status forge_fused_dw_step_e4m3(const void *dY, const void *X, float dy_scale, float x_scale,
+                                                void *W, void *m, void *v, float *qscales, forge_opt_kind opt_kind,
+                                                const forge_hparams *hp, const forge_shape *shape, int64_t step,
+                                                uint64_t seed, struct CUstream_st *stream);
+
+/* The weight gradient alone from E4M3 operands: dW = s * (dY^T X) in binary32, as
+ * forge_dw_gemm; the unfused baseline of forge_fused_dw_step_e4m3. */
+FORGE_API forge_status forge_dw_gemm_e4m3(const void *dY, const void *X, float dy_scale, float x_scale, float *dW,
+                                          const forge_shape *shape, struct CUstream_st *stream);
+
+/*
  * forge_dx_gemm -- the layer's input gradient dX = dY W (the read of W that §5
  * Significance and claims, limitations, requires before the update), on the
  * tensor cores: dX[t, i] = sum_o dY[t, o] W[o, i], accumulated in FP32 on chip

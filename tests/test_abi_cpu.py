@@ -152,3 +152,21 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(fg, "_LIB_PATH", "/nonexistent/libforge.so")
     with pytest.raises(fg.ForgeUnavailable):
         fg.lib()
+
+
+def test_e4m3_entry_points_reject_bad_arguments(L):
+    hp = fg.hparams_struct()
+
+    def fused(shape, sdy=1.0, sx=1.0, opt=0):
+        return L.forge_fused_dw_step_e4m3(A, A, sdy, sx, A, A, A, None, opt, ctypes.byref(hp), ctypes.byref(shape),
+                                          1, 0, None)
+    assert fused(_shape(d_out=520)) == 1            # E4M3 rows must be multiples of 16 bytes
+    assert fused(_shape(d_in=264)) == 1
+    assert fused(_shape(), sdy=0.0) == 1            # scales finite and positive
+    assert fused(_shape(), sx=float("inf")) == 1
+    assert fused(_shape(), sdy=float("nan")) == 1
+    assert fused(_shape(), opt=9) == 1
+    assert L.forge_dw_gemm_e4m3(A, A, 1.0, -2.0, A, ctypes.byref(_shape()), None) == 1
+    assert L.forge_dw_gemm_e4m3(A, A, 1.0, 1.0, A + 4, ctypes.byref(_shape()), None) == 3
+    if not _cuda_available():
+        assert fused(_shape()) == 4                 # arguments pass; no device here

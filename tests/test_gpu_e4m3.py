@@ -1,0 +1,185 @@
+"""FP8 (E4M3) operands with per-tensor scales, CUDA path vs oracle (needs a GB300).
+
+The tensor core sums E4M3 code products (kind::f8f6f4, 128 tokens per pipeline stage) in FP32;
+the epilogue multiplies the finished gradient tile by s_dY * s_X before the optimizer.  The cases
+cover every tile shape (one CTA on 128 x 128 and 128 x 256, a CTA pair, two pairs sharing dY by
+multicast), a ragged token tail and ragged rows and columns, every optimizer and state format.
+"""
+import numpy as np
+import pytest
+import torch
+
+import backward_optimizer_gb300 as fg
+from oracle import fp8, int8_block
+from tests.compare import (assert_codes, assert_moments, assert_weights, gradient_sensitivity, moment_rtol)
+from tests.helpers import bits, f32
+from workloads import (OPTIMIZERS, WORKLOADS, Layer, Workload, activations_fp8, default_hparams, layer_state,
+                       moment_init, sample_positions)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fg.build()
+    fg.lib()
+
+
+def _layer(d_out, d_in, T, opt, seed):
+    wl = Workload("t", (Layer("w", d_out, d_in),), T, 1.0, 1e-3, m_init="absnormal:1e-4", v_init="uniform:1e-6")
+    dyq, s_dy, xq, s_x = activations_fp8(wl, 0, 1, seed)
+    w, m, v = layer_state(wl, 0, opt, seed)
+    return dyq, s_dy, xq, s_x, w, m, v
+
+
+def _np8(t):
+    return t.numpy().astype(np.uint8)
+
+
+# (d_out, d_in, T, tile): a pair; 128 x 256; 128 x 128 with a token tail; ragged rows and columns on
+# pairs (1104 and 1296 are multiples of 16, not of 128)
+CASES = [(512, 512, 256, (256, 256, 2)), (384, 256, 256, (128, 256, 1)), (384, 384, 192, (128, 128, 1)),
+         (1104, 1296, 100, (256, 256, 2))]
+
+
+@pytest.mark.parametrize("d_out, d_in, T, tile", CASES)
+def test_dw_gemm_e4m3_matches_oracle(d_out, d_in, T, tile):
+    got = fg.launch_shape(d_out, d_in, T)
+    assert (got["tile_rows"], got["tile_cols"], got["cluster"]) == tile
+    dyq, s_dy, xq, s_x, *_ = _layer(d_out, d_in, T, "sgd", seed=d_in + T)
+    dW = torch.empty(d_out, d_in, dtype=torch.float32, device="cuda")
+    fg.dw_gemm_e4m3(dyq.cuda(), xq.cuda(), s_dy, s_x, dW)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    assert_moments(dW.cpu().numpy(), fp8.dw_fp8(_np8(dyq), _np8(xq), s_dy, s_x), "dW", rtol=moment_rtol(T))
+
+
+def test_dw_gemm_e4m3_is_exact_on_integer_patterns():
+    """Small integer codes, one nonzero per token column pattern: every sum is exact in FP32, so any
+    index mix-up (transposed, shifted or swapped halves of a stage) shows bit for bit."""
+    T, d_out, d_in = 256, 256, 384
+    one_to_eight = np.array([0x38, 0x40, 0x44, 0x48, 0x4A, 0x4C, 0x4E, 0x50], np.uint8)  # 1 .. 8
+    dy = np.zeros((T, d_out), np.uint8)
+    x = np.zeros((T, d_in), np.uint8)
+    dy[np.arange(d_out) % T, np.arange(d_out)] = one_to_eight[np.arange(d_out) % 7]
+    x[(7 * np.arange(d_in)) % T, np.arange(d_in)] = one_to_eight[np.arange(d_in) % 5]
+    dW = torch.empty(d_out, d_in, dtype=torch.float32, device="cuda")
+    fg.dw_gemm_e4m3(torch.from_numpy(dy).cuda(), torch.from_numpy(x).cuda(), 0.5, 0.25, dW)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(dW.cpu().numpy(), fp8.dw_fp8(dy, x, 0.5, 0.25))
+
+
+@pytest.mark.parametrize("opt", OPTIMIZERS)
+@pytest.mark.parametrize("d_out, d_in", [(512, 512), (384, 256)])
+def test_fused_e4m3_fp32_states(opt, d_out, d_in):
+    T = 256
+    dyq, s_dy, xq, s_x, w, m, v = _layer(d_out, d_in, T, opt, seed=3)
+    hp = default_hparams(opt, lr=1e-3)
+    dev = lambda t: None if t is None else t.cuda()
+    W, M, V = dev(w), dev(m), dev(v)
+    fg.fused_dw_step_e4m3(dyq.cuda(), xq.cuda(), s_dy, s_x, W, M, V, None, opt, hp, 4, seed=11)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    ref = fp8.fused_step_fp8(opt, _np8(dyq), _np8(xq), s_dy, s_x, bits(w), None if m is None else f32(m),
+                             None if v is None else f32(v), hp, 4, 11)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    if m is not None:
+        assert_moments(f32(M), ref["m"], "m")
+    if v is not None:
+        assert_moments(f32(V), ref["v"], "v")
+
+
+def test_fused_e4m3_bf16_and_int8_states():
+    T, d_out, d_in = 192, 512, 768
+    dyq, s_dy, xq, s_x, w, m, v = _layer(d_out, d_in, T, "adamw", seed=4)
+    hp = default_hparams("adamw", lr=1e-3)
+    # BF16 states
+    mb, vb = m.to(torch.bfloat16), v.to(torch.bfloat16)
+    W, M, V = w.cuda(), mb.cuda(), vb.cuda()
+    fg.fused_dw_step_e4m3(dyq.cuda(), xq.cuda(), s_dy, s_x, W, M, V, None, "adamw", hp, 2, seed=5)
+    torch.cuda.synchronize()
+    ref = fp8.fused_step_fp8("adamw", _np8(dyq), _np8(xq), s_dy, s_x, bits(w), bits(mb), bits(vb), hp, 2, 5,
+                             state="bf16")
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    assert_weights(bits(M), ref["m"], "m", w_old_bits=bits(mb))
+    assert_weights(bits(V), ref["v"], "v", w_old_bits=bits(vb))
+    # INT8 states
+    rng = np.random.default_rng(4)
+    m32 = (f32(moment_init("absnormal:1e-4", w.shape, 6)) * np.sign(rng.standard_normal(w.shape))).astype(np.float32)
+    mq, ms = int8_block.quantize(m32)
+    vq, vs = int8_block.quantize(f32(moment_init("uniform:1e-6", w.shape, 7)))
+    W = w.cuda()
+    M, V = torch.from_numpy(mq).cuda(), torch.from_numpy(vq).cuda()
+    Q = torch.from_numpy(np.concatenate([ms.ravel(), vs.ravel()]).astype(np.float32)).cuda()
+    fg.fused_dw_step_e4m3(dyq.cuda(), xq.cuda(), s_dy, s_x, W, M, V, Q, "adamw", hp, 3, seed=8)
+    torch.cuda.synchronize()
+    ref = fp8.fused_step_fp8("adamw", _np8(dyq), _np8(xq), s_dy, s_x, bits(w), mq, vq, hp, 3, 8, "int8", ms, vs)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    assert_codes(M.cpu().numpy(), ref["m"], "m codes")
+    assert_codes(V.cpu().numpy(), ref["v"], "v codes")
+    n64 = w.numel() // 64
+    q = Q.cpu().numpy()
+    assert_moments(q[:n64], ref["m_scales"].ravel(), "m scales")
+    assert_moments(q[n64:], ref["v_scales"].ravel(), "v scales")
+
+
+@pytest.mark.parametrize("d_out, d_in, T", [(512, 768, 320), (1104, 1296, 100)])
+def test_fused_e4m3_equals_unfused_bitwise(d_out, d_in, T):
+    dyq, s_dy, xq, s_x, w, m, v = _layer(d_out, d_in, T, "adamw", seed=9)
+    hp = default_hparams("adamw", lr=1e-3)
+    D, X = dyq.cuda(), xq.cuda()
+    W1, M1, V1 = w.cuda(), m.cuda(), v.cuda()
+    W2, M2, V2 = w.cuda(), m.cuda(), v.cuda()
+    fg.fused_dw_step_e4m3(D, X, s_dy, s_x, W1, M1, V1, None, "adamw", hp, 6, seed=1)
+    dW = torch.empty(d_out, d_in, dtype=torch.float32, device="cuda")
+    fg.dw_gemm_e4m3(D, X, s_dy, s_x, dW)
+    fg.opt_step(dW, W2, M2, V2, None, "adamw", hp, 6, seed=1)
+    torch.cuda.synchronize()
+    assert torch.equal(W1.view(torch.int16), W2.view(torch.int16))
+    assert torch.equal(M1, M2) and torch.equal(V1, V2)
+
+
+@pytest.mark.parametrize("opt", ["adamw", "lion"])
+def test_two_pairs_sharing_dy_with_e4m3(opt):
+    """T = 8192: clusters of two CTA pairs, each loading one token half of every dY stage by multicast."""
+    T, d_out, d_in = 8192, 512, 1024
+    assert fg.launch_shape(d_out, d_in, T)["cluster"] == 4
+    dyq, s_dy, xq, s_x, w, m, v = _layer(d_out, d_in, T, opt, seed=10)
+    hp = default_hparams(opt, lr=1e-3)
+    W, M, V = w.cuda(), m.cuda(), None if v is None else v.cuda()
+    fg.fused_dw_step_e4m3(dyq.cuda(), xq.cuda(), s_dy, s_x, W, M, V, None, opt, hp, 3, seed=2)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    ref = fp8.fused_step_fp8(opt, _np8(dyq), _np8(xq), s_dy, s_x, bits(w), f32(m), None if v is None else f32(v),
+                             hp, 3, 2)
+    rt = moment_rtol(T)
+    e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
+    extra = gradient_sensitivity(opt, ref["g"], bits(w), f32(m), None if v is None else f32(v), hp, 3, 2, e, rt)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=extra)
+    assert_moments(f32(M), ref["m"], "m", rtol=rt)
+
+
+def test_llama8b_gate_e4m3_sampled():
+    """Llama-3.1-8B MLP gate (14336 x 4096), T = 4096, E4M3 operands, AdamW with FP32 states."""
+    wl = WORKLOADS["llama8b-mlp"]
+    hp = default_hparams("adamw")
+    dyq, s_dy, xq, s_x = activations_fp8(wl, 0, 1)
+    w, m, v = layer_state(wl, 0, "adamw")
+    W, M, V = w.cuda(), m.cuda(), v.cuda()
+    fg.fused_dw_step_e4m3(dyq.cuda(), xq.cuda(), s_dy, s_x, W, M, V, None, "adamw", hp, 10, seed=4)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    d_out, d_in = w.shape
+    rows, cols = (np.asarray(a) for a in sample_positions(d_out, d_in, 2048, 3))
+    g = fp8.dw_fp8_at(_np8(dyq), _np8(xq), s_dy, s_x, rows, cols)
+    from oracle import step as ostep
+    e = (rows * d_in + cols).astype(np.uint64)
+    ref = ostep.apply_update("adamw", g, bits(w)[rows, cols], f32(m)[rows, cols], f32(v)[rows, cols], hp, 10, 4, e)
+    rt = moment_rtol(wl.T)
+    extra = gradient_sensitivity("adamw", g, bits(w)[rows, cols], f32(m)[rows, cols], f32(v)[rows, cols], hp, 10, 4,
+                                 e, rt)
+    assert_weights(bits(W)[rows, cols], ref["W"], "W", w_old_bits=bits(w)[rows, cols], extra_tol=extra)
+    assert_moments(f32(M)[rows, cols], ref["m"], "m", rtol=rt)
+    assert_moments(f32(V)[rows, cols], ref["v"], "v", rtol=moment_rtol(wl.T, squared=True))
