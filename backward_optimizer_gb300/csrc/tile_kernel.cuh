@@ -274,11 +274,13 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                 if constexpr (Tr::kV) ld_cs_v8(static_cast<float*>(a.v) + el, v[k]);
             }
         }
-        uint32_t g[4][8];
-        strip_transpose<SCALE>(taddr + c, strip, g, a.g_scale);
+        // the gradient strip goes to shared memory once; each row group then reads its 8 values
+        strip_store<SCALE>(taddr + c, strip, a.g_scale);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const size_t e = lane_base + k * row_step + c;
+            uint32_t g[8];
+            strip_load_row(strip, k, g);
             const Philox4 p = sr_words(e >> 3, a.seed, a.step);
             Philox4 pm{}, pv{};
             if constexpr (BF16S && Tr::kM) pm = sr_words(e >> 3, a.seed, a.step, kStreamM);
@@ -294,8 +296,8 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                     if constexpr (Tr::kM) { m0 = __uint_as_float(m[k][j]); m1 = __uint_as_float(m[k][j + 1]); }
                     if constexpr (Tr::kV) { v0 = __uint_as_float(v[k][j]); v1 = __uint_as_float(v[k][j + 1]); }
                 }
-                const float w0 = opt_update<OPT>(__uint_as_float(g[k][j]), bf16_lo(wp), m0, v0, a.s);
-                const float w1 = opt_update<OPT>(__uint_as_float(g[k][j + 1]), bf16_hi(wp), m1, v1, a.s);
+                const float w0 = opt_update<OPT>(__uint_as_float(g[j]), bf16_lo(wp), m0, v0, a.s);
+                const float w1 = opt_update<OPT>(__uint_as_float(g[j + 1]), bf16_hi(wp), m1, v1, a.s);
                 w[k][j >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
                 if constexpr (BF16S) {
                     if constexpr (Tr::kM) m[k][j >> 1] = sr_bf16(m0, sr_r16(pm, j)) | (sr_bf16(m1, sr_r16(pm, j + 1)) << 16);
