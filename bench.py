@@ -490,7 +490,7 @@ def main():
                 "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": _ncu_traffic(args.workload, args.opt, args.state),
+                     "frac": achieved / peak, "traffic": _ncu_traffic(args.workload, args.opt, args.state) if not e4m3 else None,
                      "kernel": "forge_tile_kernel (fused)", "avg_launch_ms": avg_launch_ms,
                      "flops_per_launch": flops_launch, "peak_source": peak_source},
         "clocks": r["clocks"],
