@@ -193,13 +193,14 @@ def run_gpu(args, rank, world):
     stream = torch.cuda.current_stream()
     flops_step = wl.flops_per_step()
 
-    def fused(i, L):
+    def fused(i, L, on=None):
+        on = stream if on is None else on
         if e4m3:
             fg.fused_dw_step_e4m3(L["dy"], L["x"], L["s_dy"], L["s_x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp,
-                                  t_step, seed=0x5EED + i, stream=stream)
+                                  t_step, seed=0x5EED + i, stream=on)
         else:
             fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step,
-                             seed=0x5EED + i, stream=stream)
+                             seed=0x5EED + i, stream=on)
 
     def fused_pass(ev=None):
         for i, L in enumerate(layers):
@@ -240,6 +241,31 @@ def run_gpu(args, rank, world):
     status = fg.sync_status()
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
+
+    # ---- the same fused pass captured once in a CUDA graph and replayed: no host launch path per
+    # layer (it matters only for small layers, whose kernels are shorter than a launch)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side), torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream()
+        for i, L in enumerate(layers):
+            fused(i, L, on=cap)
+    stream.wait_stream(side)
+    for _ in range(args.warmup):
+        graph.replay()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1) / args.steps
+    del graph
+    if fg.sync_status() != 0:
+        raise RuntimeError("device status after the graph replays")
 
     # ---- unfused two-phase baseline on the same data: all dW to HBM, then every optimizer pass
     dws = [torch.empty(l.d_out, l.d_in, dtype=torch.float32, device=dev) for l in wl.layers]
@@ -366,12 +392,12 @@ def run_gpu(args, rank, world):
         raise RuntimeError(f"device status {status} in the dX / backward timing")
     del dxs
 
-    elapsed_ms, unfused_ms, e2e_ms, dx_ms, bwd_ms = max_over_ranks(
-        [elapsed_ms, unfused_ms, e2e_ms, timed["dx"], timed["backward"]], world, dev)
+    elapsed_ms, unfused_ms, e2e_ms, dx_ms, bwd_ms, graph_ms = max_over_ranks(
+        [elapsed_ms, unfused_ms, e2e_ms, timed["dx"], timed["backward"], graph_ms], world, dev)
     ms_step = elapsed_ms / args.steps
     return dict(ms_step=ms_step, flops_step=flops_step, launch_ms=launch_ms, launches=launches,
                 unfused_ms=unfused_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks.summary(),
-                grad_pool_unfused=grad_pool_unfused, mem_fused=mem0, wl=wl, dx_ms=dx_ms, bwd_ms=bwd_ms,
+                grad_pool_unfused=grad_pool_unfused, mem_fused=mem0, wl=wl, dx_ms=dx_ms, bwd_ms=bwd_ms, graph_ms=graph_ms,
                 dx_launch_ms=dx_launch_ms)
 
 
@@ -518,6 +544,8 @@ def main():
         "e2e": {"value": job_throughput(r["flops_step"], world, r["e2e_ms"]), "unit": "TFLOP/s",
                 "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
+        "graph": {"ms_per_step": r["graph_ms"], "value": job_throughput(r["flops_step"], world, r["graph_ms"]),
+                  "unit": "TFLOP/s", "what": "the fused pass captured once in a CUDA graph and replayed"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": _ncu_traffic(args.workload, args.opt, args.state) if not e4m3 else None,
                      "kernel": "forge_tile_kernel (fused)", "avg_launch_ms": avg_launch_ms,
