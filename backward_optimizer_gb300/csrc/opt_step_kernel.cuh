@@ -47,8 +47,8 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
         uint32_t g[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         uint32_t w[4] = {0, 0, 0, 0};
         if (valid) {
-            if (a.dW != nullptr) ld_cs_v8(a.dW + e0, g);
-            ld_cs_v4(a.W + e0, w);
+            if (a.dW != nullptr) ld_v8(a.dW + e0, g);
+            ld_v4(a.W + e0, w);
         }
         float mf[8], vf[8];
         float ms = 0.f, vs = 0.f;
@@ -56,13 +56,13 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
         if constexpr (INT8) {
             if constexpr (Tr::kM) {
                 if (valid) {
-                    ld_cs_v2(static_cast<int8_t*>(a.m) + e0, mq);
+                    ld_v2(static_cast<int8_t*>(a.m) + e0, mq);
                     ms = a.m_scales[e0 >> 6];
                 }
             }
             if constexpr (Tr::kV) {
                 if (valid) {
-                    ld_cs_v2(static_cast<int8_t*>(a.v) + e0, vq);
+                    ld_v2(static_cast<int8_t*>(a.v) + e0, vq);
                     vs = a.v_scales[e0 >> 6];
                 }
             }
@@ -74,12 +74,12 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
         } else if constexpr (BF16S) {
             uint32_t t[4] = {0, 0, 0, 0};
             if constexpr (Tr::kM) {
-                if (valid) ld_cs_v4(static_cast<uint16_t*>(a.m) + e0, t);
+                if (valid) ld_v4(static_cast<uint16_t*>(a.m) + e0, t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mf[j] = (j & 1) ? bf16_hi(t[j >> 1]) : bf16_lo(t[j >> 1]);
             }
             if constexpr (Tr::kV) {
-                if (valid) ld_cs_v4(static_cast<uint16_t*>(a.v) + e0, t);
+                if (valid) ld_v4(static_cast<uint16_t*>(a.v) + e0, t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) vf[j] = (j & 1) ? bf16_hi(t[j >> 1]) : bf16_lo(t[j >> 1]);
             }
@@ -94,12 +94,12 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
         } else {
             uint32_t t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
             if constexpr (Tr::kM) {
-                if (valid) ld_cs_v8(static_cast<float*>(a.m) + e0, t);
+                if (valid) ld_v8(static_cast<float*>(a.m) + e0, t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mf[j] = __uint_as_float(t[j]);
             }
             if constexpr (Tr::kV) {
-                if (valid) ld_cs_v8(static_cast<float*>(a.v) + e0, t);
+                if (valid) ld_v8(static_cast<float*>(a.v) + e0, t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) vf[j] = __uint_as_float(t[j]);
             }
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             w[k] = sr_bf16(wn[2 * k], sr_r16(p, 2 * k)) | (sr_bf16(wn[2 * k + 1], sr_r16(p, 2 * k + 1)) << 16);
-        if (valid) st_cs_v4(a.W + e0, w);
+        if (valid) st_v4(a.W + e0, w);
         if constexpr (INT8) {
             float am = 0.f, av = 0.f;
 #pragma unroll
@@ -145,11 +145,11 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
             const bool leader = (threadIdx.x & 7) == 0;
             if (valid) {
                 if constexpr (Tr::kM) {
-                    st_cs_v2(static_cast<int8_t*>(a.m) + e0, mo);
+                    st_v2(static_cast<int8_t*>(a.m) + e0, mo);
                     if (leader) a.m_scales[e0 >> 6] = nms;
                 }
                 if constexpr (Tr::kV) {
-                    st_cs_v2(static_cast<int8_t*>(a.v) + e0, vo);
+                    st_v2(static_cast<int8_t*>(a.v) + e0, vo);
                     if (leader) a.v_scales[e0 >> 6] = nvs;
                 }
             }
@@ -160,26 +160,26 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     t[k] = sr_bf16(mf[2 * k], sr_r16(pm, 2 * k)) | (sr_bf16(mf[2 * k + 1], sr_r16(pm, 2 * k + 1)) << 16);
-                if (valid) st_cs_v4(static_cast<uint16_t*>(a.m) + e0, t);
+                if (valid) st_v4(static_cast<uint16_t*>(a.m) + e0, t);
             }
             if constexpr (Tr::kV) {
                 const Philox4 pv = sr_words(gi, a.seed, a.step, kStreamV);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     t[k] = sr_bf16(vf[2 * k], sr_r16(pv, 2 * k)) | (sr_bf16(vf[2 * k + 1], sr_r16(pv, 2 * k + 1)) << 16);
-                if (valid) st_cs_v4(static_cast<uint16_t*>(a.v) + e0, t);
+                if (valid) st_v4(static_cast<uint16_t*>(a.v) + e0, t);
             }
         } else {
             uint32_t t[8];
             if constexpr (Tr::kM) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) t[j] = __float_as_uint(mf[j]);
-                if (valid) st_cs_v8(static_cast<float*>(a.m) + e0, t);
+                if (valid) st_v8(static_cast<float*>(a.m) + e0, t);
             }
             if constexpr (Tr::kV) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) t[j] = __float_as_uint(vf[j]);
-                if (valid) st_cs_v8(static_cast<float*>(a.v) + e0, t);
+                if (valid) st_v8(static_cast<float*>(a.v) + e0, t);
             }
         }
     }

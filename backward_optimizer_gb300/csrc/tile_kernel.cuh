@@ -265,13 +265,13 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
             // a run outside the layer loads the layer's first run instead (always valid) and
             // stores nothing, so the loads stay unconditional
             const size_t el = ok[k] ? lane_base + k * row_step + c : 0;
-            ld_cs_v4(a.W + el, w[k]);
+            ld_v4(a.W + el, w[k]);
             if constexpr (BF16S) {
-                if constexpr (Tr::kM) ld_cs_v4(static_cast<uint16_t*>(a.m) + el, m[k]);
-                if constexpr (Tr::kV) ld_cs_v4(static_cast<uint16_t*>(a.v) + el, v[k]);
+                if constexpr (Tr::kM) ld_v4(static_cast<uint16_t*>(a.m) + el, m[k]);
+                if constexpr (Tr::kV) ld_v4(static_cast<uint16_t*>(a.v) + el, v[k]);
             } else {
-                if constexpr (Tr::kM) ld_cs_v8(static_cast<float*>(a.m) + el, m[k]);
-                if constexpr (Tr::kV) ld_cs_v8(static_cast<float*>(a.v) + el, v[k]);
+                if constexpr (Tr::kM) ld_v8(static_cast<float*>(a.m) + el, m[k]);
+                if constexpr (Tr::kV) ld_v8(static_cast<float*>(a.v) + el, v[k]);
             }
         }
         // the gradient strip goes to shared memory once; each row group then reads its 8 values
@@ -308,13 +308,13 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                 }
             }
             if (ok[k]) {
-                st_cs_v4(a.W + e, w[k]);
+                st_v4(a.W + e, w[k]);
                 if constexpr (BF16S) {
-                    if constexpr (Tr::kM) st_cs_v4(static_cast<uint16_t*>(a.m) + e, m[k]);
-                    if constexpr (Tr::kV) st_cs_v4(static_cast<uint16_t*>(a.v) + e, v[k]);
+                    if constexpr (Tr::kM) st_v4(static_cast<uint16_t*>(a.m) + e, m[k]);
+                    if constexpr (Tr::kV) st_v4(static_cast<uint16_t*>(a.v) + e, v[k]);
                 } else {
-                    if constexpr (Tr::kM) st_cs_v8(static_cast<float*>(a.m) + e, m[k]);
-                    if constexpr (Tr::kV) st_cs_v8(static_cast<float*>(a.v) + e, v[k]);
+                    if constexpr (Tr::kM) st_v8(static_cast<float*>(a.m) + e, m[k]);
+                    if constexpr (Tr::kV) st_v8(static_cast<float*>(a.v) + e, v[k]);
                 }
             }
         }
@@ -381,9 +381,9 @@ __device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e_row, b
     if (!ok) e_row = 0;  // a row past the layer's last reads the first (always valid) and stores nothing
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        ld_cs_v4(a.W + e_row + 32 * h, in.w[h]);
-        if constexpr (Tr::kM) ld_cs_v2(static_cast<int8_t*>(a.m) + e_row + 32 * h, in.mq[h]);
-        if constexpr (Tr::kV) ld_cs_v2(static_cast<int8_t*>(a.v) + e_row + 32 * h, in.vq[h]);
+        ld_v4(a.W + e_row + 32 * h, in.w[h]);
+        if constexpr (Tr::kM) ld_v2(static_cast<int8_t*>(a.m) + e_row + 32 * h, in.mq[h]);
+        if constexpr (Tr::kV) ld_v2(static_cast<int8_t*>(a.v) + e_row + 32 * h, in.vq[h]);
     }
     in.ms = Tr::kM ? a.m_scales[e_row >> 6] : 0.f;
     in.vs = Tr::kV ? a.v_scales[e_row >> 6] : 0.f;
@@ -435,9 +435,9 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
             if constexpr (Tr::kV) vo[j >> 2] |= int8_code(vv, nvs) << (8 * (j & 3));
         }
         if (ok) {
-            st_cs_v4(a.W + e, in.w[h]);
-            if constexpr (Tr::kM) st_cs_v2(static_cast<int8_t*>(a.m) + e, mo);
-            if constexpr (Tr::kV) st_cs_v2(static_cast<int8_t*>(a.v) + e, vo);
+            st_v4(a.W + e, in.w[h]);
+            if constexpr (Tr::kM) st_v2(static_cast<int8_t*>(a.m) + e, mo);
+            if constexpr (Tr::kV) st_v2(static_cast<int8_t*>(a.v) + e, vo);
         }
     }
     if (ok && (threadIdx.x & 3u) == 0) {
