@@ -277,5 +277,5 @@ def dx_launch_shape(T: int, d_out: int, d_in: int) -> dict:
 
 
 def debug_withhold_next_stage() -> None:
-    """Test switch: the next fused launch withholds one pipeline stage so a bounded wait runs out."""
+    """Test switch: the next tile-kernel launch withholds one pipeline stage so a bounded wait runs out."""
     lib().forge_debug_withhold_next_stage()

@@ -26,7 +26,7 @@ using forge::OptScalars;
 constexpr int kMaxDevices = 64;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<uint64_t> g_launches{0};
-std::atomic<int> g_withhold_next{0};  // test switch, consumed by the next fused launch
+std::atomic<int> g_withhold_next{0};  // test switch, consumed by the next tile-kernel launch
 
 struct DeviceInfo {
     bool ready = false;
@@ -357,7 +357,7 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.step = static_cast<uint64_t>(step);
     a.status = dev.status;
     a.wait_limit_ns = g_wait_limit_ns.load();
-    a.withhold_first_stage = epi == forge::kEpiStoreGrad ? 0 : g_withhold_next.exchange(0);
+    a.withhold_first_stage = g_withhold_next.exchange(0);
 
     forge::TileLaunch l;
     forge_status st = make_operand_map(&l.tmap_dy, dY, shape->d_out, shape->T, e4m3);
@@ -392,7 +392,7 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
     a.dX = static_cast<uint16_t*>(dX);
     a.status = dev.status;
     a.wait_limit_ns = g_wait_limit_ns.load();
-    a.withhold_first_stage = 0;
+    a.withhold_first_stage = g_withhold_next.exchange(0);
 
     forge::TileLaunch l;
     // A = dY [T, d_out] read K-major with the same box as the weight gradient's dY^T; B = W

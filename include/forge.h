@@ -227,8 +227,9 @@ FORGE_API forge_status forge_sync_status(struct CUstream_st *stream);
 FORGE_API void forge_set_wait_limit_ns(uint64_t ns);
 
 /* Test switch for the failure-detection path (the method has no counterpart; it exists so that
- * the bounded waits can be exercised without a real fault).  The next forge_fused_dw_step launch
- * with T > 0 withholds the first pipeline stage of its first tile: the MMA thread's wait for that
+ * the bounded waits can be exercised without a real fault).  The next tile-kernel launch (of
+ * forge_fused_dw_step, forge_fused_dw_step_e4m3, forge_dw_gemm, forge_dw_gemm_e4m3 or
+ * forge_dx_gemm, with work to do) withholds the first pipeline stage of its first tile: the MMA thread's wait for that
  * stage runs out after the wait limit, the kernel records FORGE_ERR_TIMEOUT, stops every other
  * wait, frees its TMEM and returns; forge_sync_status() then reports FORGE_ERR_TIMEOUT and the
  * CUDA context stays usable.  The outputs of that one call are unspecified.  No fault is raised. */

@@ -58,3 +58,46 @@ def test_withheld_stage_times_out_and_context_survives(d_out, d_in, T):
     assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=extra)
     assert_moments(f32(M), ref["m"], "m", rtol=rt)
     assert_moments(f32(V), ref["v"], "v", rtol=moment_rtol(T, squared=True))
+
+
+def test_withheld_stage_in_the_e4m3_step():
+    from oracle import fp8
+    from workloads import activations_fp8
+    T, d_out, d_in = 512, 512, 768
+    wl = Workload("t", (Layer("w", d_out, d_in),), T, 1.0, 1e-3, m_init="absnormal:1e-4", v_init="uniform:1e-6")
+    dyq, s_dy, xq, s_x = activations_fp8(wl, 0, 1, 3)
+    w, m, v = layer_state(wl, 0, "adamw", 3)
+    hp = default_hparams("adamw", lr=1e-3)
+    D, X = dyq.cuda(), xq.cuda()
+    fg.debug_withhold_next_stage()
+    fg.fused_dw_step_e4m3(D, X, s_dy, s_x, w.cuda(), m.cuda(), v.cuda(), None, "adamw", hp, 2, seed=1)
+    assert fg.sync_status() == TIMEOUT
+    W, M, V = w.cuda(), m.cuda(), v.cuda()
+    fg.fused_dw_step_e4m3(D, X, s_dy, s_x, W, M, V, None, "adamw", hp, 2, seed=1)
+    assert fg.sync_status() == 0
+    ref = fp8.fused_step_fp8("adamw", dyq.numpy(), xq.numpy(), s_dy, s_x, bits(w), f32(m), f32(v), hp, 2, 1)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    assert_moments(f32(M), ref["m"], "m")
+
+
+@pytest.mark.parametrize("kind", ["dx", "dw"])
+def test_withheld_stage_in_the_gemms(kind):
+    """The input-gradient and weight-gradient GEMMs run the same pipeline and report the same way."""
+    from oracle import backward as obw
+    from tests.compare import assert_bf16_sum
+    dy, x, w, _, _ = _layer(512, 768, 512)
+    D, X, Wd = dy.cuda(), x.cuda(), w.cuda()
+    for attempt in range(2):
+        if attempt == 0:
+            fg.debug_withhold_next_stage()
+        if kind == "dx":
+            out = torch.empty(512, 768, dtype=torch.bfloat16, device="cuda")
+            fg.dx_gemm(D, Wd, out)
+        else:
+            out = torch.empty(512, 768, dtype=torch.float32, device="cuda")
+            fg.dw_gemm(D, X, out)
+        assert fg.sync_status() == (TIMEOUT if attempt == 0 else 0)
+    if kind == "dx":
+        assert_bf16_sum(bits(out), obw.dx_f32(bits(dy), bits(w)), 512)
+    else:
+        assert_moments(out.cpu().numpy(), ostep.dw(bits(dy), bits(x)), "dW")
