@@ -124,6 +124,17 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------ ranks
 
+def algorithmic_bytes(wl, opt: str, state: str, operands: str) -> int:
+    """Least HBM bytes of one fused pass: per weight element W read and written (2 + 2) and each
+    moment the optimizer keeps read and written (binary32 4 + 4, bf16 2 + 2, int8 1 + 1 plus a
+    4-byte scale per 64 each way), plus dY and X read once (2 bytes per bf16 element, 1 per E4M3)."""
+    from workloads import MOMENTS
+    per_moment = {"fp32": 8.0, "bf16": 4.0, "int8": 2.0 + 8.0 / 64}[state]
+    per_el = 4.0 + per_moment * sum(MOMENTS[opt])
+    op = 1 if operands == "e4m3" else 2
+    return int(sum(l.d_out * l.d_in * per_el + wl.T * (l.d_out + l.d_in) * op for l in wl.layers))
+
+
 def max_over_ranks(values, world: int, device="cpu"):
     """Element-wise maximum of per-rank timings (the slowest rank defines the job's time).  The
     only collective of the benchmark besides barriers; no data of the path is exchanged."""
@@ -533,6 +544,15 @@ def main():
     flops_launch = r["flops_step"] / n_layers
     achieved = flops_launch / (avg_launch_ms * 1e-3) / 1e12
     value = job_throughput(r["flops_step"], world, r["ms_step"])
+    # the epilogue side of the same launches: HBM bytes per launch over the same launch time
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alg_bytes = algorithmic_bytes(r["wl"], args.opt, args.state, args.operands) / n_layers
+    traffic = _ncu_traffic(args.workload, args.opt, args.state) if not e4m3 else None
+    hbm = {"unit": "GB/s", "peak": hbm_peak, "algorithmic_bytes_per_launch": alg_bytes,
+           "achieved_algorithmic": alg_bytes / (avg_launch_ms * 1e-3) / 1e9,
+           "frac_algorithmic": alg_bytes / (avg_launch_ms * 1e-3) / 1e9 / hbm_peak,
+           "achieved_measured": None if traffic is None else traffic / (avg_launch_ms * 1e-3) / 1e9,
+           "peak_source": f"hbm_gbs of {peaks_src}"}
     line = {
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
@@ -547,7 +567,7 @@ def main():
         "graph": {"ms_per_step": r["graph_ms"], "value": job_throughput(r["flops_step"], world, r["graph_ms"]),
                   "unit": "TFLOP/s", "what": "the fused pass captured once in a CUDA graph and replayed"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": _ncu_traffic(args.workload, args.opt, args.state) if not e4m3 else None,
+                     "frac": achieved / peak, "traffic": traffic, "hbm": hbm,
                      "kernel": "forge_tile_kernel (fused)", "avg_launch_ms": avg_launch_ms,
                      "flops_per_launch": flops_launch, "peak_source": peak_source},
         "clocks": r["clocks"],
