@@ -155,6 +155,29 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _expect(t, dtypes, shape, name: str) -> None:
+    """Argument check before anything reaches the library: dtype among `dtypes`, exact shape."""
+    if t is None:
+        return
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected one of {[str(d) for d in dtypes]}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _state_args(W, m, v, qscales) -> None:
+    import torch
+    states = [t for t in (m, v) if t is not None]
+    if len({t.dtype for t in states}) > 1:
+        raise TypeError("m and v must share one state dtype")
+    for t, name in ((m, "m"), (v, "v")):
+        _expect(t, (torch.float32, torch.int8, torch.bfloat16), W.shape, name)
+    if states and states[0].dtype == torch.int8:
+        if qscales is None:
+            raise ValueError("INT8 states need qscales")
+        _expect(qscales, (torch.float32,), (2 * W.numel() // 64,), "qscales")
+
+
 def _check(status: int, what: str) -> None:
     if status != 0:
         raise ForgeError(status, what)
@@ -179,8 +202,12 @@ def fused_dw_step(dY, X, W, m=None, v=None, qscales=None, opt: str = "adamw", hp
     """One fused step on torch tensors: dY [T, d_out] bf16, X [T, d_in] bf16, W [d_out, d_in] bf16,
     m/v FP32, int8 or bf16 [d_out, d_in] (the dtype picks the state format), qscales FP32
     [2 * d_out * d_in / 64] for int8 states."""
+    import torch
     T, d_out = dY.shape
     d_in = X.shape[1]
+    for t, name, shp in ((dY, "dY", (T, d_out)), (X, "X", (T, d_in)), (W, "W", (d_out, d_in))):
+        _expect(t, (torch.bfloat16,), shp, name)
+    _state_args(W, m, v, qscales)
     shape = _shape(T, d_out, d_in, _state_of(m, v))
     st = lib().forge_fused_dw_step(_ptr(dY), _ptr(X), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), OPT_KINDS[opt],
                                    ctypes.byref(hparams_struct(hp)), ctypes.byref(shape), int(step),
@@ -190,7 +217,11 @@ def fused_dw_step(dY, X, W, m=None, v=None, qscales=None, opt: str = "adamw", hp
 
 def dw_gemm(dY, X, dW, stream=None) -> None:
     """dW [d_out, d_in] FP32 = dY^T X (the unfused baseline's gradient pass)."""
+    import torch
     T, d_out = dY.shape
+    _expect(dY, (torch.bfloat16,), (T, d_out), "dY")
+    _expect(X, (torch.bfloat16,), (T, X.shape[1]), "X")
+    _expect(dW, (torch.float32,), (d_out, X.shape[1]), "dW")
     shape = _shape(T, d_out, X.shape[1], STATE_FP32)
     _check(lib().forge_dw_gemm(_ptr(dY), _ptr(X), _ptr(dW), ctypes.byref(shape), _stream(stream)), "forge_dw_gemm")
 
@@ -199,8 +230,14 @@ def fused_dw_step_e4m3(dY, X, dy_scale: float, x_scale: float, W, m=None, v=None
                        hp: Any = None, step: int = 1, seed: int = 0, stream=None) -> None:
     """The fused step with E4M3 operands: dY [T, d_out] and X [T, d_in] one-byte codes (uint8 or
     float8_e4m3fn tensors) with per-tensor scales; everything else as fused_dw_step."""
+    import torch
     T, d_out = dY.shape
     d_in = X.shape[1]
+    codes = (torch.uint8, torch.float8_e4m3fn)
+    _expect(dY, codes, (T, d_out), "dY")
+    _expect(X, codes, (T, d_in), "X")
+    _expect(W, (torch.bfloat16,), (d_out, d_in), "W")
+    _state_args(W, m, v, qscales)
     shape = _shape(T, d_out, d_in, _state_of(m, v))
     st = lib().forge_fused_dw_step_e4m3(_ptr(dY), _ptr(X), float(dy_scale), float(x_scale), _ptr(W), _ptr(m),
                                         _ptr(v), _ptr(qscales), OPT_KINDS[opt], ctypes.byref(hparams_struct(hp)),
@@ -210,7 +247,12 @@ def fused_dw_step_e4m3(dY, X, dy_scale: float, x_scale: float, W, m=None, v=None
 
 def dw_gemm_e4m3(dY, X, dy_scale: float, x_scale: float, dW, stream=None) -> None:
     """dW [d_out, d_in] FP32 = dy_scale * x_scale * (dY^T X) from E4M3 codes."""
+    import torch
     T, d_out = dY.shape
+    codes = (torch.uint8, torch.float8_e4m3fn)
+    _expect(dY, codes, (T, d_out), "dY")
+    _expect(X, codes, (T, X.shape[1]), "X")
+    _expect(dW, (torch.float32,), (d_out, X.shape[1]), "dW")
     shape = _shape(T, d_out, X.shape[1], STATE_FP32)
     _check(lib().forge_dw_gemm_e4m3(_ptr(dY), _ptr(X), float(dy_scale), float(x_scale), _ptr(dW), ctypes.byref(shape),
                                     _stream(stream)), "forge_dw_gemm_e4m3")
@@ -218,7 +260,11 @@ def dw_gemm_e4m3(dY, X, dy_scale: float, x_scale: float, dW, stream=None) -> Non
 
 def dx_gemm(dY, W, dX, stream=None) -> None:
     """dX [T, d_in] bf16 = dY W, the layer's input gradient (read W before any step replaces it)."""
+    import torch
     T, d_out = dY.shape
+    _expect(dY, (torch.bfloat16,), (T, d_out), "dY")
+    _expect(W, (torch.bfloat16,), (d_out, W.shape[1]), "W")
+    _expect(dX, (torch.bfloat16,), (T, W.shape[1]), "dX")
     shape = _shape(T, d_out, W.shape[1], STATE_FP32)
     _check(lib().forge_dx_gemm(_ptr(dY), _ptr(W), _ptr(dX), ctypes.byref(shape), _stream(stream)), "forge_dx_gemm")
 
@@ -227,8 +273,12 @@ def linear_backward(dY, X, W, m=None, v=None, qscales=None, dX=None, opt: str = 
                     step: int = 1, seed: int = 0, stream=None) -> None:
     """The linear layer's backward with the fused weight step: dX = dY W from the weights before the
     step, then the fused step, on one stream in that order."""
+    import torch
     T, d_out = dY.shape
     d_in = X.shape[1]
+    for t, name, shp in ((dY, "dY", (T, d_out)), (X, "X", (T, d_in)), (W, "W", (d_out, d_in)), (dX, "dX", (T, d_in))):
+        _expect(t, (torch.bfloat16,), shp, name)
+    _state_args(W, m, v, qscales)
     shape = _shape(T, d_out, d_in, _state_of(m, v))
     st = lib().forge_linear_backward(_ptr(dY), _ptr(X), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), _ptr(dX),
                                      OPT_KINDS[opt], ctypes.byref(hparams_struct(hp)), ctypes.byref(shape),
@@ -239,7 +289,11 @@ def linear_backward(dY, X, W, m=None, v=None, qscales=None, dX=None, opt: str = 
 def opt_step(dW, W, m=None, v=None, qscales=None, opt: str = "adamw", hp: Any = None, step: int = 1, seed: int = 0,
              stream=None) -> None:
     """The unfused baseline's optimizer pass over a materialised FP32 gradient (None = zero gradient)."""
+    import torch
     d_out, d_in = W.shape
+    _expect(W, (torch.bfloat16,), (d_out, d_in), "W")
+    _expect(dW, (torch.float32,), (d_out, d_in), "dW")
+    _state_args(W, m, v, qscales)
     shape = _shape(0, d_out, d_in, _state_of(m, v))
     st = lib().forge_opt_step(_ptr(dW), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), OPT_KINDS[opt],
                               ctypes.byref(hparams_struct(hp)), ctypes.byref(shape), int(step),

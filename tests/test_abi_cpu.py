@@ -170,3 +170,31 @@ def test_e4m3_entry_points_reject_bad_arguments(L):
     assert L.forge_dw_gemm_e4m3(A, A, 1.0, 1.0, A + 4, ctypes.byref(_shape()), None) == 3
     if not _cuda_available():
         assert fused(_shape()) == 4                 # arguments pass; no device here
+
+
+def test_binding_rejects_wrong_dtypes_and_shapes_before_the_library():
+    """The Python binding checks dtypes and shapes on the host (CPU tensors suffice: the checks
+    come before any device pointer is taken)."""
+    import torch
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    f32 = lambda *s: torch.zeros(*s, dtype=torch.float32)
+    dy, x, w, m, v = bf(64, 128), bf(64, 256), bf(128, 256), f32(128, 256), f32(128, 256)
+    with pytest.raises(TypeError):
+        fg.fused_dw_step(dy, x, f32(128, 256), m, v)             # W must be bf16
+    with pytest.raises(ValueError):
+        fg.fused_dw_step(dy, x, bf(128, 128), m, v)              # W shape must be d_out x d_in
+    with pytest.raises(ValueError):
+        fg.fused_dw_step(dy, bf(32, 256), w, m, v)               # X must have dY's token count
+    with pytest.raises(TypeError):
+        fg.fused_dw_step(dy, x, w, m, bf(128, 256))              # m and v share one state dtype
+    with pytest.raises(ValueError):
+        fg.fused_dw_step(dy, x, w, torch.zeros(128, 256, dtype=torch.int8),
+                         torch.zeros(128, 256, dtype=torch.int8))  # INT8 states need qscales
+    with pytest.raises(TypeError):
+        fg.fused_dw_step_e4m3(dy, x, 1.0, 1.0, w, m, v)          # E4M3 operands are one byte
+    with pytest.raises(ValueError):
+        fg.dx_gemm(dy, w, bf(64, 128))                           # dX is T x d_in
+    with pytest.raises(TypeError):
+        fg.dw_gemm(dy, x, bf(128, 256))                          # dW is FP32
+    with pytest.raises(TypeError):
+        fg.opt_step(bf(128, 256), w, m, v)                       # a materialised dW is FP32
