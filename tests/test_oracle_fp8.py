@@ -106,3 +106,40 @@ def test_fused_step_fp8_is_the_update_on_the_dequantised_gradient():
     ref = step.apply_update("adamw", fp8.dw_fp8(dy, x, 1e-2, 2e-3), w, m, v, hp, 1, 5, e)
     np.testing.assert_array_equal(out["W"], ref["W"])
     np.testing.assert_array_equal(out["m"], ref["m"])
+
+
+def test_channel_scales_reduce_to_the_tensor_scale():
+    rng = np.random.default_rng(5)
+    dy = rng.integers(0, 0x70, size=(48, 16)).astype(np.uint8)
+    x = rng.integers(0, 0x70, size=(48, 24)).astype(np.uint8)
+    got = fp8.dw_fp8(dy, x, np.full(16, 3e-4, np.float32), np.full(24, 0.7, np.float32))
+    np.testing.assert_array_equal(got, fp8.dw_fp8(dy, x, 3e-4, 0.7))
+
+
+def test_channel_scales_brute_force_and_orientation():
+    """s_dy scales rows of dW (output channels), s_x its columns; exact rational sums, one binary32
+    rounding, then the binary32 product of the two channel scales."""
+    rng = np.random.default_rng(6)
+    dy = rng.integers(0, 0x70, size=(9, 5)).astype(np.uint8)
+    x = rng.integers(0, 0x70, size=(9, 5)).astype(np.uint8)  # square, so a swap would not show in shapes
+    s_dy = (rng.random(5) * 1e-3 + 1e-4).astype(np.float32)
+    s_x = (rng.random(5) + 0.5).astype(np.float32)
+    got = fp8.dw_fp8(dy, x, s_dy, s_x)
+    a, b = _torch_decode(dy), _torch_decode(x)
+    for o in range(5):
+        for i in range(5):
+            exact = sum(Fraction(float(a[t, o])) * Fraction(float(b[t, i])) for t in range(9))
+            s = np.float32(s_dy[o] * s_x[i])
+            assert got[o, i] == np.float32(float(np.float32(float(exact))) * float(s)), (o, i)
+    rows, cols = np.array([4, 0, 2]), np.array([1, 3, 4])
+    np.testing.assert_array_equal(fp8.dw_fp8_at(dy, x, s_dy, s_x, rows, cols), got[rows, cols])
+
+
+def test_channel_quantised_inputs_round_trip():
+    from workloads import fp8_e4m3_channels
+    t = torch.randn(256, 40, generator=torch.Generator().manual_seed(7)) * torch.logspace(-4, 0, 40)[None, :]
+    codes, scale = fp8_e4m3_channels(t)
+    back = fp8.decode_e4m3(codes.numpy()) * scale.numpy()[None, :]
+    assert np.abs(fp8.decode_e4m3(codes.numpy())).max(axis=0).tolist() == [448.0] * 40
+    rel = np.abs(back - t.double().numpy()) / np.maximum(np.abs(t.double().numpy()), 2.0 ** -6 * scale.numpy()[None, :])
+    assert rel.max() <= 2.0 ** -4 + 1e-12

@@ -214,3 +214,14 @@ def activations_fp8(wl: Workload, layer_index: int, step: int, seed: int = 0, de
     dyq, s_dy = fp8_e4m3(dy)
     xq, s_x = fp8_e4m3(x)
     return dyq, s_dy, xq, s_x
+
+
+def fp8_e4m3_channels(t: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-column E4M3 codes of a float32 [rows, cols] tensor: scale[c] = amax(|t[:, c]|) / 448
+    (1 for an all-zero column), codes = PyTorch's float8_e4m3fn cast of t / scale.
+    Returns (uint8 codes, float32 scales [cols])."""
+    t = t.float()
+    amax = t.abs().amax(dim=0) if t.numel() else torch.zeros(t.shape[1])
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
+    codes = (t / scale[None, :]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
