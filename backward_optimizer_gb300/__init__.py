@@ -95,6 +95,12 @@ def lib() -> ctypes.CDLL:
     L.forge_fused_dw_step_e4m3.restype = ctypes.c_int
     L.forge_dw_gemm_e4m3.argtypes = [vp, vp, f32, f32, vp, ctypes.POINTER(ForgeShape), vp]
     L.forge_dw_gemm_e4m3.restype = ctypes.c_int
+    L.forge_fused_dw_step_e4m3_channels.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                                    ctypes.POINTER(ForgeHparams), ctypes.POINTER(ForgeShape), i64,
+                                                    u64, vp]
+    L.forge_fused_dw_step_e4m3_channels.restype = ctypes.c_int
+    L.forge_dw_gemm_e4m3_channels.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(ForgeShape), vp]
+    L.forge_dw_gemm_e4m3_channels.restype = ctypes.c_int
     L.forge_dx_gemm.argtypes = [vp, vp, vp, ctypes.POINTER(ForgeShape), vp]
     L.forge_dx_gemm.restype = ctypes.c_int
     L.forge_linear_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.POINTER(ForgeHparams),
@@ -226,10 +232,23 @@ def dw_gemm(dY, X, dW, stream=None) -> None:
     _check(lib().forge_dw_gemm(_ptr(dY), _ptr(X), _ptr(dW), ctypes.byref(shape), _stream(stream)), "forge_dw_gemm")
 
 
-def fused_dw_step_e4m3(dY, X, dy_scale: float, x_scale: float, W, m=None, v=None, qscales=None, opt: str = "adamw",
+def _channel_scales(dy_scale, x_scale, d_out: int, d_in: int) -> bool:
+    """True for per-channel scales (two FP32 device vectors), False for two per-tensor floats."""
+    import torch
+    vec = isinstance(dy_scale, torch.Tensor), isinstance(x_scale, torch.Tensor)
+    if vec[0] != vec[1]:
+        raise TypeError("dy_scale and x_scale: both floats (per tensor) or both tensors (per channel)")
+    if vec[0]:
+        _expect(dy_scale, (torch.float32,), (d_out,), "dy_scale")
+        _expect(x_scale, (torch.float32,), (d_in,), "x_scale")
+    return vec[0]
+
+
+def fused_dw_step_e4m3(dY, X, dy_scale, x_scale, W, m=None, v=None, qscales=None, opt: str = "adamw",
                        hp: Any = None, step: int = 1, seed: int = 0, stream=None) -> None:
     """The fused step with E4M3 operands: dY [T, d_out] and X [T, d_in] one-byte codes (uint8 or
-    float8_e4m3fn tensors) with per-tensor scales; everything else as fused_dw_step."""
+    float8_e4m3fn tensors) with per-tensor scales (floats) or per-channel scales (FP32 device
+    vectors of d_out and d_in); everything else as fused_dw_step."""
     import torch
     T, d_out = dY.shape
     d_in = X.shape[1]
@@ -239,14 +258,21 @@ def fused_dw_step_e4m3(dY, X, dy_scale: float, x_scale: float, W, m=None, v=None
     _expect(W, (torch.bfloat16,), (d_out, d_in), "W")
     _state_args(W, m, v, qscales)
     shape = _shape(T, d_out, d_in, _state_of(m, v))
+    if _channel_scales(dy_scale, x_scale, d_out, d_in):
+        st = lib().forge_fused_dw_step_e4m3_channels(
+            _ptr(dY), _ptr(X), _ptr(dy_scale), _ptr(x_scale), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), OPT_KINDS[opt],
+            ctypes.byref(hparams_struct(hp)), ctypes.byref(shape), int(step), int(seed) & (2**64 - 1), _stream(stream))
+        _check(st, "forge_fused_dw_step_e4m3_channels")
+        return
     st = lib().forge_fused_dw_step_e4m3(_ptr(dY), _ptr(X), float(dy_scale), float(x_scale), _ptr(W), _ptr(m),
                                         _ptr(v), _ptr(qscales), OPT_KINDS[opt], ctypes.byref(hparams_struct(hp)),
                                         ctypes.byref(shape), int(step), int(seed) & (2**64 - 1), _stream(stream))
     _check(st, "forge_fused_dw_step_e4m3")
 
 
-def dw_gemm_e4m3(dY, X, dy_scale: float, x_scale: float, dW, stream=None) -> None:
-    """dW [d_out, d_in] FP32 = dy_scale * x_scale * (dY^T X) from E4M3 codes."""
+def dw_gemm_e4m3(dY, X, dy_scale, x_scale, dW, stream=None) -> None:
+    """dW [d_out, d_in] FP32 = dy_scale * x_scale * (dY^T X) from E4M3 codes (scales per tensor, or
+    per channel as FP32 device vectors of d_out and d_in)."""
     import torch
     T, d_out = dY.shape
     codes = (torch.uint8, torch.float8_e4m3fn)
@@ -254,6 +280,10 @@ def dw_gemm_e4m3(dY, X, dy_scale: float, x_scale: float, dW, stream=None) -> Non
     _expect(X, codes, (T, X.shape[1]), "X")
     _expect(dW, (torch.float32,), (d_out, X.shape[1]), "dW")
     shape = _shape(T, d_out, X.shape[1], STATE_FP32)
+    if _channel_scales(dy_scale, x_scale, d_out, X.shape[1]):
+        _check(lib().forge_dw_gemm_e4m3_channels(_ptr(dY), _ptr(X), _ptr(dy_scale), _ptr(x_scale), _ptr(dW),
+                                                 ctypes.byref(shape), _stream(stream)), "forge_dw_gemm_e4m3_channels")
+        return
     _check(lib().forge_dw_gemm_e4m3(_ptr(dY), _ptr(X), float(dy_scale), float(x_scale), _ptr(dW), ctypes.byref(shape),
                                     _stream(stream)), "forge_dw_gemm_e4m3")
 

@@ -330,7 +330,7 @@ forge_status run_opt(const float* dW, void* W, void* m, void* v, float* qscales,
 forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m, void* v, float* qscales,
                       forge_opt_kind k, int epi, const forge_hparams* hp, const forge_shape* shape, int64_t step,
                       uint64_t seed, cudaStream_t stream, const DeviceInfo& dev, bool e4m3 = false,
-                      float g_scale = 1.0f) {
+                      float g_scale = 1.0f, const float* row_scales = nullptr, const float* col_scales = nullptr) {
     const bool int8 = shape->state == FORGE_STATE_INT8_B64;
     const uint64_t n = static_cast<uint64_t>(shape->d_out) * static_cast<uint64_t>(shape->d_in);
     forge::TileArgs a;
@@ -344,6 +344,8 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.num_tiles = a.tiles_m * a.tiles_n;
     a.k_blocks = static_cast<int>(ceil_div(a.T, e4m3 ? 128 : forge::kBK));
     a.g_scale = g_scale;
+    a.row_scales = row_scales;
+    a.col_scales = col_scales;
     // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
     a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
     a.dW = dW;
@@ -428,7 +430,8 @@ forge_status check_fused(const void* dY, const void* X, const void* W, const voi
 
 forge_status launch_fused(const void* dY, const void* X, void* W, void* m, void* v, float* qscales,
                           forge_opt_kind k, const forge_hparams* hp, const forge_shape* shape, int64_t step,
-                          uint64_t seed, cudaStream_t stream, bool e4m3 = false, float g_scale = 1.0f) {
+                          uint64_t seed, cudaStream_t stream, bool e4m3 = false, float g_scale = 1.0f,
+                          const float* row_scales = nullptr, const float* col_scales = nullptr) {
     if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
     DeviceInfo* dev = nullptr;
     forge_status st = device_info(&dev);
@@ -436,7 +439,7 @@ forge_status launch_fused(const void* dY, const void* X, void* W, void* m, void*
     if (shape->T == 0)  // no tokens: the gradient is exactly zero
         return run_opt(nullptr, W, m, v, qscales, k, hp, shape, step, seed, stream, *dev);
     return run_tile(dY, X, nullptr, W, m, v, qscales, k, forge::kEpiOptFP32, hp, shape, step, seed, stream, *dev,
-                    e4m3, g_scale);
+                    e4m3, g_scale, row_scales, col_scales);
 }
 
 // E4M3 operands: rows of dY and X are d_out and d_in bytes, a multiple of 16 for TMA; the scales are
@@ -494,6 +497,51 @@ forge_status forge_fused_dw_step_e4m3(const void* dY, const void* X, float dy_sc
     if (st != FORGE_OK) return st;
     const float g_scale = dy_scale * x_scale;  // one binary32 rounding
     return launch_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream, true, g_scale);
+}
+
+// Per-channel E4M3 scales: device vectors of d_out and d_in binary32 values, 16-byte aligned.
+forge_status check_channel_scales(const forge_shape* shape, const float* dy_scales, const float* x_scales) {
+    if (shape->d_out == 0 || shape->d_in == 0 || shape->T == 0) return FORGE_OK;  // not read
+    if (dy_scales == nullptr || x_scales == nullptr) return FORGE_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(dy_scales) & 15u) || (reinterpret_cast<uintptr_t>(x_scales) & 15u))
+        return FORGE_ERR_MISALIGNED;
+    return FORGE_OK;
+}
+
+forge_status forge_fused_dw_step_e4m3_channels(const void* dY, const void* X, const float* dy_scales,
+                                               const float* x_scales, void* W, void* m, void* v, float* qscales,
+                                               forge_opt_kind opt_kind, const forge_hparams* hp,
+                                               const forge_shape* shape, int64_t step, uint64_t seed,
+                                               struct CUstream_st* stream) {
+    forge_status st = check_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step);
+    if (st != FORGE_OK) return st;
+    st = check_e4m3(shape, 1.0f, 1.0f);
+    if (st != FORGE_OK) return st;
+    st = check_channel_scales(shape, dy_scales, x_scales);
+    if (st != FORGE_OK) return st;
+    return launch_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream, true, 1.0f, dy_scales,
+                        x_scales);
+}
+
+forge_status forge_dw_gemm_e4m3_channels(const void* dY, const void* X, const float* dy_scales, const float* x_scales,
+                                         float* dW, const forge_shape* shape, struct CUstream_st* stream) {
+    forge_status st = check_shape(shape);
+    if (st != FORGE_OK) return st;
+    st = check_e4m3(shape, 1.0f, 1.0f);
+    if (st != FORGE_OK) return st;
+    st = check_channel_scales(shape, dy_scales, x_scales);
+    if (st != FORGE_OK) return st;
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
+    if (dW == nullptr || (shape->T > 0 && (dY == nullptr || X == nullptr))) return FORGE_ERR_INVALID_ARGUMENT;
+    if (!aligned32(dW) || (shape->T > 0 && (!aligned32(dY) || !aligned32(X)))) return FORGE_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    if (shape->T == 0)
+        return cuda_status(cudaMemsetAsync(dW, 0, static_cast<size_t>(shape->d_out) * shape->d_in * sizeof(float),
+                                           stream));
+    return run_tile(dY, X, dW, nullptr, nullptr, nullptr, nullptr, FORGE_SGD, forge::kEpiStoreGrad, nullptr, shape,
+                    1, 0, stream, *dev, true, 1.0f, dy_scales, x_scales);
 }
 
 forge_status forge_dw_gemm_e4m3(const void* dY, const void* X, float dy_scale, float x_scale, float* dW,

@@ -87,6 +87,8 @@ struct TileArgs {
     int tiles_m, tiles_n, num_tiles, group_m;
     int k_blocks;                 // reduction slices per tile: T / 64 (dW; T / 128 for E4M3), d_out / 64 (dX)
     float g_scale;                // E4M3 operands: s_dY * s_X, applied to the FP32 gradient tile
+    const float* row_scales;      // or per channel (both set): s_dY [d_out] and s_X [d_in], each
+    const float* col_scales;      //   element's tile value times RN(s_dY[o] * s_X[i])
     float* dW;                    // kEpiStoreGrad: [d_out, d_in] FP32
     uint16_t* dX;                 // kEpiDX: [T, d_in] bf16; token rows >= T are not stored
     uint16_t* W;                  // bf16 [d_out, d_in]
@@ -161,22 +163,40 @@ __device__ __forceinline__ void st_v8_f32(float* p, const uint32_t (&r)[8]) {
 // 32 columns, so every warp-wide access touches 8 rows x one contiguous span instead of 32 rows.
 // The strip is written with its 16-byte chunks XOR-swizzled by (row mod 8), which makes both the
 // row-wise writes and the column-wise reads free of bank conflicts.
+// E4M3 dequantisation of one TMEM strip while each thread still holds its own row `row`, columns
+// col .. col+31: by the per-tensor product, or by each element's channel-scale product.  Column
+// scales are the same for every lane (broadcast loads); d_in is a multiple of 16 with E4M3
+// operands, so each 4-column group is wholly inside or outside the layer.
 template <bool SCALE>
-__device__ __forceinline__ void scale_strip(uint32_t (&g)[32], float scale) {
+__device__ __forceinline__ void scale_strip(uint32_t (&g)[32], const TileArgs& a, int row, int col) {
     if constexpr (SCALE) {
+        if (a.row_scales == nullptr) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = __float_as_uint(__fmul_rn(__uint_as_float(g[i]), scale));
+            for (int i = 0; i < 32; ++i) g[i] = __float_as_uint(__fmul_rn(__uint_as_float(g[i]), a.g_scale));
+        } else {
+            const float rs = row < a.d_out ? a.row_scales[row] : 0.0f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint32_t cs[4] = {0u, 0u, 0u, 0u};
+                if (col + 4 * q < a.d_in) ld_v4(a.col_scales + col + 4 * q, cs);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float s = __fmul_rn(rs, __uint_as_float(cs[j]));
+                    g[4 * q + j] = __float_as_uint(__fmul_rn(__uint_as_float(g[4 * q + j]), s));
+                }
+            }
+        }
     }
 }
 
 template <bool SCALE = false>
 __device__ __forceinline__ void strip_transpose(uint32_t taddr, uint8_t* strip, uint32_t (&out)[4][8],
-                                                float scale = 1.0f) {
+                                                const TileArgs& a, int row, int col) {
     const uint32_t lane = threadIdx.x & 31u;
     uint32_t g[32];
     tmem_ld_32x32b_x32(taddr, g);
     tmem_ld_wait(g);
-    scale_strip<SCALE>(g, scale);
+    scale_strip<SCALE>(g, a, row, col);
     const uint32_t base = smem_addr(strip);
 #pragma unroll
     for (uint32_t j = 0; j < 8; ++j)
@@ -199,12 +219,12 @@ __device__ __forceinline__ void strip_transpose(uint32_t taddr, uint8_t* strip, 
 // The two halves of strip_transpose, for callers that consume one row group at a time: the strip
 // is written once, then lane l reads the 8 columns it owns of row (l div 4) + 8k.
 template <bool SCALE = false>
-__device__ __forceinline__ void strip_store(uint32_t taddr, uint8_t* strip, float scale = 1.0f) {
+__device__ __forceinline__ void strip_store(uint32_t taddr, uint8_t* strip, const TileArgs& a, int row, int col) {
     const uint32_t lane = threadIdx.x & 31u;
     uint32_t g[32];
     tmem_ld_32x32b_x32(taddr, g);
     tmem_ld_wait(g);
-    scale_strip<SCALE>(g, scale);
+    scale_strip<SCALE>(g, a, row, col);
     const uint32_t base = smem_addr(strip);
     __syncwarp();  // earlier reads of the strip are complete
 #pragma unroll
@@ -233,7 +253,7 @@ __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int 
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 32) {
         uint32_t t[4][8];
-        strip_transpose<SCALE>(taddr + c, strip, t, a.g_scale);
+        strip_transpose<SCALE>(taddr + c, strip, t, a, row0 + lane, col0 + c);
         if (col + c < a.d_in) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -275,7 +295,7 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
             }
         }
         // the gradient strip goes to shared memory once; each row group then reads its 8 values
-        strip_store<SCALE>(taddr + c, strip, a.g_scale);
+        strip_store<SCALE>(taddr + c, strip, a, row0 + lane, col0 + c);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const size_t e = lane_base + k * row_step + c;
@@ -461,8 +481,8 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
         if (col0 + c >= a.d_in) break;
         Int8RowIn<OPT> in[2];
         int8_row_load<OPT>(a, lane_base + c, row < a.d_out, in[0]);
-        strip_store<SCALE>(taddr + c, strip, a.g_scale);
-        strip_store<SCALE>(taddr + c + 32, strip + 4096, a.g_scale);
+        strip_store<SCALE>(taddr + c, strip, a, row0 + lane, col0 + c);
+        strip_store<SCALE>(taddr + c + 32, strip + 4096, a, row0 + lane, col0 + c + 32);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             if (k < 3)

@@ -131,7 +131,7 @@ def algorithmic_bytes(wl, opt: str, state: str, operands: str) -> int:
     from workloads import MOMENTS
     per_moment = {"fp32": 8.0, "bf16": 4.0, "int8": 2.0 + 8.0 / 64}[state]
     per_el = 4.0 + per_moment * sum(MOMENTS[opt])
-    op = 1 if operands == "e4m3" else 2
+    op = 2 if operands == "bf16" else 1
     return int(sum(l.d_out * l.d_in * per_el + wl.T * (l.d_out + l.d_in) * op for l in wl.layers))
 
 
@@ -166,8 +166,9 @@ def _make_layer(wl, i, opt, state, device, seed, act_cache, operands="bf16"):
     from workloads import activations, activations_fp8, layer_state
     key = _act_key(wl, i)
     if key not in act_cache:
-        if operands == "e4m3":
-            dyq, s_dy, xq, s_x = activations_fp8(wl, i, 1, seed, device=device)
+        if operands in ("e4m3", "e4m3-channel"):
+            dyq, s_dy, xq, s_x = activations_fp8(wl, i, 1, seed, device=device,
+                                                 per_channel=operands == "e4m3-channel")
             act_cache[key] = (dyq, xq, s_dy, s_x)
         else:
             act_cache[key] = activations(wl, i, 1, seed, device=device) + (1.0, 1.0)
@@ -198,7 +199,7 @@ def run_gpu(args, rank, world):
     hp = default_hparams(args.opt)
     t_step = wl.steps[-1]
     act_cache = {}
-    e4m3 = args.operands == "e4m3"
+    e4m3 = args.operands != "bf16"
     layers = [_make_layer(wl, i, args.opt, args.state, dev, 1000 * rank, act_cache, args.operands)
               for i in range(len(wl.layers))]
     stream = torch.cuda.current_stream()
@@ -473,8 +474,8 @@ def main():
     ap.add_argument("--workload", default="llama8b-mlp")
     ap.add_argument("--opt", default="adamw")
     ap.add_argument("--state", default="fp32", choices=["fp32", "int8", "bf16"])
-    ap.add_argument("--operands", default="bf16", choices=["bf16", "e4m3"],
-                    help="dY/X format: bf16, or E4M3 codes with per-tensor scales")
+    ap.add_argument("--operands", default="bf16", choices=["bf16", "e4m3", "e4m3-channel"],
+                    help="dY/X format: bf16, or E4M3 codes with per-tensor or per-channel scales")
     ap.add_argument("--oracle-rows", type=int, default=0, help="rows per layer of the oracle sample (0: sized by time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -534,7 +535,7 @@ def main():
 
     peaks, peaks_src = _peaks()
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    e4m3 = args.operands == "e4m3"
+    e4m3 = args.operands != "bf16"
     # E4M3 contractions take the FP8 peak: the measured bf16 peak times the nominal ratio 4.5 / 2.25
     peak = 2.0 * bf16_peak if e4m3 else bf16_peak
     peak_source = (f"2 x bf16_tflops of {peaks_src} (nominal fp8/bf16 dense ratio 4.5/2.25)" if e4m3

@@ -190,6 +190,24 @@ FORGE_API forge_status forge_dw_gemm_e4m3(const void *dY, const void *X, float d
                                           const forge_shape *shape, struct CUstream_st *stream);
 
 /*
+ * forge_fused_dw_step_e4m3_channels, forge_dw_gemm_e4m3_channels -- the same with one scale
+ * per channel: dy_scales [d_out] (one per column of dY, the output channels) and x_scales
+ * [d_in] (one per column of X), binary32 device vectors, 16-byte aligned, read-only.  They
+ * factor out of the sum over tokens like the per-tensor scales, so each gradient element is
+ * multiplied by its own binary32 product dy_scales[o] * x_scales[i], formed in the epilogue.
+ * Per-tensor scaling is the case of constant vectors (and gives identical results).
+ */
+FORGE_API forge_status forge_fused_dw_step_e4m3_channels(const void *dY, const void *X, const float *dy_scales,
+                                                         const float *x_scales, void *W, void *m, void *v,
+                                                         float *qscales, forge_opt_kind opt_kind,
+                                                         const forge_hparams *hp, const forge_shape *shape,
+                                                         int64_t step, uint64_t seed, struct CUstream_st *stream);
+
+FORGE_API forge_status forge_dw_gemm_e4m3_channels(const void *dY, const void *X, const float *dy_scales,
+                                                   const float *x_scales, float *dW, const forge_shape *shape,
+                                                   struct CUstream_st *stream);
+
+/*
  * forge_dx_gemm -- the layer's input gradient dX = dY W (the read of W that §5
  * Significance and claims, limitations, requires before the update), on the
  * tensor cores: dX[t, i] = sum_o dY[t, o] W[o, i], accumulated in FP32 on chip

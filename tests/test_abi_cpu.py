@@ -198,3 +198,19 @@ def test_binding_rejects_wrong_dtypes_and_shapes_before_the_library():
         fg.dw_gemm(dy, x, bf(128, 256))                          # dW is FP32
     with pytest.raises(TypeError):
         fg.opt_step(bf(128, 256), w, m, v)                       # a materialised dW is FP32
+
+
+def test_e4m3_channel_scales_reject_bad_vectors(L):
+    hp = fg.hparams_struct()
+
+    def fused(sdy, sx, shape=None):
+        shape = shape or _shape()
+        return L.forge_fused_dw_step_e4m3_channels(A, A, sdy, sx, A, A, A, None, 0, ctypes.byref(hp),
+                                                   ctypes.byref(shape), 1, 0, None)
+    assert fused(None, A) == 1
+    assert fused(A, None) == 1
+    assert fused(A + 4, A) == 3                         # 16-byte aligned vectors
+    assert fused(A, A, _shape(d_in=264)) == 1           # E4M3 rows: multiples of 16 bytes
+    assert L.forge_dw_gemm_e4m3_channels(A, A, A, A + 8, A, ctypes.byref(_shape()), None) == 3
+    if not _cuda_available():
+        assert fused(A, A) == 4

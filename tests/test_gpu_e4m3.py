@@ -183,3 +183,87 @@ def test_llama8b_gate_e4m3_sampled():
     assert_weights(bits(W)[rows, cols], ref["W"], "W", w_old_bits=bits(w)[rows, cols], extra_tol=extra)
     assert_moments(f32(M)[rows, cols], ref["m"], "m", rtol=rt)
     assert_moments(f32(V)[rows, cols], ref["v"], "v", rtol=moment_rtol(wl.T, squared=True))
+
+
+# ---------------------------------------------------------------------------- per-channel scales
+
+def _layer_channels(d_out, d_in, T, opt, seed):
+    """dY and X drawn as for the per-tensor cases, with columns of very different magnitudes, then
+    quantised per column (workloads.fp8_e4m3_channels)."""
+    from workloads import fp8_e4m3_channels
+    g = torch.Generator().manual_seed(seed)
+    dy = torch.randn(T, d_out, generator=g) * torch.logspace(-5, -2, d_out)[None, :]
+    x = torch.randn(T, d_in, generator=g) * torch.logspace(-1, 1, d_in)[None, :]
+    dyq, s_dy = fp8_e4m3_channels(dy)
+    xq, s_x = fp8_e4m3_channels(x)
+    wl = Workload("t", (Layer("w", d_out, d_in),), T, 1.0, 1e-3, m_init="absnormal:1e-4", v_init="uniform:1e-6")
+    w, m, v = layer_state(wl, 0, opt, seed)
+    return dyq, s_dy, xq, s_x, w, m, v
+
+
+@pytest.mark.parametrize("d_out, d_in, T", [(512, 512, 256), (384, 256, 256), (384, 384, 192), (1104, 1296, 100)])
+def test_dw_gemm_e4m3_channel_scales(d_out, d_in, T):
+    """Every tile shape; 1296 columns end 16 past a 32-column strip, so the last 4-column scale
+    groups of a strip lie outside the layer."""
+    dyq, s_dy, xq, s_x, *_ = _layer_channels(d_out, d_in, T, "sgd", seed=d_in + T)
+    dW = torch.empty(d_out, d_in, dtype=torch.float32, device="cuda")
+    fg.dw_gemm_e4m3(dyq.cuda(), xq.cuda(), s_dy.cuda(), s_x.cuda(), dW)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    ref = fp8.dw_fp8(_np8(dyq), _np8(xq), s_dy.numpy(), s_x.numpy())
+    assert_moments(dW.cpu().numpy(), ref, "dW", rtol=moment_rtol(T))
+
+
+def test_constant_channel_scales_equal_the_tensor_scale_bitwise():
+    dyq, s_dy, xq, s_x, w, m, v = _layer(512, 768, 256, "adamw", seed=12)
+    hp = default_hparams("adamw", lr=1e-3)
+    D, X = dyq.cuda(), xq.cuda()
+    W1, M1, V1 = w.cuda(), m.cuda(), v.cuda()
+    W2, M2, V2 = w.cuda(), m.cuda(), v.cuda()
+    fg.fused_dw_step_e4m3(D, X, s_dy, s_x, W1, M1, V1, None, "adamw", hp, 3, seed=7)
+    fg.fused_dw_step_e4m3(D, X, torch.full((512,), s_dy, device="cuda"), torch.full((768,), s_x, device="cuda"),
+                          W2, M2, V2, None, "adamw", hp, 3, seed=7)
+    torch.cuda.synchronize()
+    assert torch.equal(W1.view(torch.int16), W2.view(torch.int16))
+    assert torch.equal(M1, M2) and torch.equal(V1, V2)
+
+
+@pytest.mark.parametrize("opt, state", [("adamw", "fp32"), ("lion", "fp32"), ("rmsprop", "fp32"), ("adamw", "bf16")])
+def test_fused_e4m3_channel_scales(opt, state):
+    T, d_out, d_in = 256, 512, 1024
+    dyq, s_dy, xq, s_x, w, m, v = _layer_channels(d_out, d_in, T, opt, seed=13)
+    if state == "bf16":
+        m, v = (None if t is None else t.to(torch.bfloat16) for t in (m, v))
+    hp = default_hparams(opt, lr=1e-3)
+    dev = lambda t: None if t is None else t.cuda()
+    W, M, V = dev(w), dev(m), dev(v)
+    fg.fused_dw_step_e4m3(dyq.cuda(), xq.cuda(), s_dy.cuda(), s_x.cuda(), W, M, V, None, opt, hp, 2, seed=9)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    mm = None if m is None else (bits(m) if state == "bf16" else f32(m))
+    vv = None if v is None else (bits(v) if state == "bf16" else f32(v))
+    ref = fp8.fused_step_fp8(opt, _np8(dyq), _np8(xq), s_dy.numpy(), s_x.numpy(), bits(w), mm, vv, hp, 2, 9,
+                             state=state)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    for got, old, key in ((M, m, "m"), (V, v, "v")):
+        if got is None:
+            continue
+        if state == "bf16":
+            assert_weights(bits(got), ref[key], key, w_old_bits=bits(old))
+        else:
+            assert_moments(f32(got), ref[key], key)
+
+
+def test_fused_e4m3_channel_scales_equal_unfused_bitwise():
+    dyq, s_dy, xq, s_x, w, m, v = _layer_channels(1104, 1296, 100, "adamw", seed=14)
+    hp = default_hparams("adamw", lr=1e-3)
+    D, X, SD, SX = dyq.cuda(), xq.cuda(), s_dy.cuda(), s_x.cuda()
+    W1, M1, V1 = w.cuda(), m.cuda(), v.cuda()
+    W2, M2, V2 = w.cuda(), m.cuda(), v.cuda()
+    fg.fused_dw_step_e4m3(D, X, SD, SX, W1, M1, V1, None, "adamw", hp, 4, seed=3)
+    dW = torch.empty(w.shape, dtype=torch.float32, device="cuda")
+    fg.dw_gemm_e4m3(D, X, SD, SX, dW)
+    fg.opt_step(dW, W2, M2, V2, None, "adamw", hp, 4, seed=3)
+    torch.cuda.synchronize()
+    assert torch.equal(W1.view(torch.int16), W2.view(torch.int16))
+    assert torch.equal(M1, M2) and torch.equal(V1, V2)

@@ -203,16 +203,21 @@ def fp8_e4m3(t: torch.Tensor) -> Tuple[torch.Tensor, float]:
     return codes, scale
 
 
-def activations_fp8(wl: Workload, layer_index: int, step: int, seed: int = 0, device="cpu"):
+def activations_fp8(wl: Workload, layer_index: int, step: int, seed: int = 0, device="cpu", per_channel=False):
     """(dY codes [T, d_out], s_dY, X codes [T, d_in], s_X): the layer's activations drawn as for
-    ``activations`` (float32, same seeds) and quantised per tensor to E4M3."""
+    ``activations`` (float32, same seeds) and quantised to E4M3 per tensor (float scales) or, with
+    ``per_channel``, per column (float32 scale vectors on `device`)."""
     l = wl.layers[layer_index]
     dy = torch.randn(wl.T, l.d_out, generator=_gen(layer_seed(seed, layer_index, "dy", step), device),
                      device=device) * wl.dy_std
     x = torch.randn(wl.T, l.d_in, generator=_gen(layer_seed(seed, layer_index, "x", step), device),
                     device=device) * wl.x_std
-    dyq, s_dy = fp8_e4m3(dy)
-    xq, s_x = fp8_e4m3(x)
+    if per_channel:
+        dyq, s_dy = fp8_e4m3_channels(dy)
+        xq, s_x = fp8_e4m3_channels(x)
+    else:
+        dyq, s_dy = fp8_e4m3(dy)
+        xq, s_x = fp8_e4m3(x)
     return dyq, s_dy, xq, s_x
 
 
