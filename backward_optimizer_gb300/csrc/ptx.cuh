@@ -333,6 +333,10 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_ma
            | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 256-bit and 128-bit stores.
 __device__ __forceinline__ void st_v8(void* p, const uint32_t (&r)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),

@@ -293,6 +293,18 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                 if constexpr (Tr::kM) ld_v8(static_cast<float*>(a.m) + el, m[k]);
                 if constexpr (Tr::kV) ld_v8(static_cast<float*>(a.v) + el, v[k]);
             }
+            // the next 32 columns' W/m/v into L2 now, so their loads wait on L2 rather than DRAM
+            if (c + 32 < WIDTH && col + c + 32 < a.d_in && row + 8 * k < a.d_out) {
+                const size_t en = lane_base + k * row_step + c + 32;
+                prefetch_l2(a.W + en);
+                if constexpr (BF16S) {
+                    if constexpr (Tr::kM) prefetch_l2(static_cast<uint16_t*>(a.m) + en);
+                    if constexpr (Tr::kV) prefetch_l2(static_cast<uint16_t*>(a.v) + en);
+                } else {
+                    if constexpr (Tr::kM) prefetch_l2(static_cast<float*>(a.m) + en);
+                    if constexpr (Tr::kV) prefetch_l2(static_cast<float*>(a.v) + en);
+                }
+            }
         }
         // the gradient strip goes to shared memory once; each row group then reads its 8 values
         strip_store<SCALE>(taddr + c, strip, a, row0 + lane, col0 + c);
