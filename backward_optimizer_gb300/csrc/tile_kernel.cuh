@@ -266,7 +266,7 @@ __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int 
 // streams (BF16S = true).  The update always runs on binary32 moments; only their storage differs.
 template <int OPT, int WIDTH, bool BF16S, bool SCALE>
 __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int col0, uint32_t taddr,
-                                              uint8_t* strip) {
+                                              uint8_t* strip, int row0n = -1, int col0n = 0) {
     using Tr = OptTraits<OPT>;
     constexpr int kSW = BF16S ? 4 : 8;  // 32-bit words holding a lane's 8 moment values
     const int lane = threadIdx.x & 31;
@@ -293,9 +293,13 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                 if constexpr (Tr::kM) ld_v8(static_cast<float*>(a.m) + el, m[k]);
                 if constexpr (Tr::kV) ld_v8(static_cast<float*>(a.v) + el, v[k]);
             }
-            // the next 32 columns' W/m/v into L2 now, so their loads wait on L2 rather than DRAM
-            if (c + 32 < WIDTH && col + c + 32 < a.d_in && row + 8 * k < a.d_out) {
-                const size_t en = lane_base + k * row_step + c + 32;
+            // the next 32 columns' W/m/v into L2 now, so their loads wait on L2 rather than DRAM; in
+            // the last step, the first 32 columns of this warp's next tile
+            const bool last = c + 32 >= WIDTH;
+            const int rn = last ? row0n + (lane >> 2) + 8 * k : row + 8 * k;
+            const int cn = last ? col0n + 8 * (lane & 3) : col + c + 32;
+            if ((!last || row0n >= 0) && cn < a.d_in && rn < a.d_out) {
+                const size_t en = static_cast<size_t>(rn) * a.d_in + cn;
                 prefetch_l2(a.W + en);
                 if constexpr (BF16S) {
                     if constexpr (Tr::kM) prefetch_l2(static_cast<uint16_t*>(a.m) + en);
@@ -731,8 +735,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* strip = strips + e * C::kStripBytes;
             if constexpr (EPI == kEpiDX) epi_store_dx<kWidth>(a, row0, col0, taddr);
             else if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth, kScale>(a, row0, col0, taddr, strip);
-            else if constexpr (EPI == kEpiOptFP32) epi_opt_dense<OPT, kWidth, false, kScale>(a, row0, col0, taddr, strip);
-            else if constexpr (EPI == kEpiOptBF16) epi_opt_dense<OPT, kWidth, true, kScale>(a, row0, col0, taddr, strip);
+            else if constexpr (EPI == kEpiOptFP32 || EPI == kEpiOptBF16) {
+                int row0n = -1, col0n = 0;
+                if (tile + tile_stride < a.num_tiles) {
+                    int mbn, nbn;
+                    tile_coords(tile + tile_stride, a, mbn, nbn);
+                    row0n = mbn * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
+                    col0n = (nbn * kPairs + static_cast<int>(pair)) * BN + half * kWidth;
+                }
+                epi_opt_dense<OPT, kWidth, EPI == kEpiOptBF16, kScale>(a, row0, col0, taddr, strip, row0n, col0n);
+            }
             else epi_opt_int8<OPT, kWidth, kScale>(a, row0, col0, taddr, strip);
             tc_fence_before();
             __syncwarp();
