@@ -214,3 +214,20 @@ def test_e4m3_channel_scales_reject_bad_vectors(L):
     assert L.forge_dw_gemm_e4m3_channels(A, A, A, A + 8, A, ctypes.byref(_shape()), None) == 3
     if not _cuda_available():
         assert fused(A, A) == 4
+
+
+def test_header_compiles_as_c_and_a_c_program_links(L, tmp_path):
+    """A C11 program (tests/c/abi_host.c) built with gcc -Wall -Werror against include/forge.h and
+    libforge.so makes host-side calls through the C ABI."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    exe = tmp_path / "abi_host"
+    libdir = os.path.dirname(fg.library_path())
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "abi_host.c"), "-L", libdir, "-lforge",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
