@@ -117,6 +117,12 @@ WORKLOADS: Dict[str, Workload] = {
         name="int8-4096", layers=(Layer("w", 4096, 4096),), T=2048, x_std=1.0, dy_std=1e-3,
         steps=(1,), description="one 4096x4096 layer, T=2048, AdamW with INT8 block-64 moments"),
     "qwen14b-sweep": _qwen14b_sweep(40),
+    # the Llama MLP's token count and distributions on one square layer: a case small enough for a
+    # full profiler capture that keeps the Llama layers' balance of mainloop and epilogue
+    "sq4096-t4096": Workload(
+        name="sq4096-t4096", layers=(Layer("w", 4096, 4096),), T=4096, x_std=1.0, dy_std=1e-3,
+        m_init="absnormal:1e-4", v_init="uniform:1e-6", steps=(10,),
+        description="one 4096x4096 layer, T=4096, AdamW with FP32 moments at step 10 (Llama MLP balance)"),
 }
 
 
