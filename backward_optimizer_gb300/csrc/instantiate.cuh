@@ -26,7 +26,7 @@ cudaError_t launch_tile(const TileLaunch& l) {
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = l.stream;
     cfg.attrs = CL > 1 ? &attr : nullptr;
@@ -67,7 +67,7 @@ cudaError_t tile_grid(int num_tiles, int num_sms, int* ctas) {
         attr.val.clusterDim.y = 1;
         attr.val.clusterDim.z = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(C::kThreads, 1, 1);
         cfg.dynamicSmemBytes = C::kSmemBytes;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;

@@ -40,8 +40,6 @@ namespace forge {
 constexpr int kBM = 128;         // tile rows (d_out) = TMEM lanes
 constexpr int kBK = 64;          // tokens per pipeline stage = 128 bytes of one operand column
 constexpr int kUmmaK = 16;       // K of one kind::f16 MMA
-constexpr int kNumEpiWarps = 8;  // two warps per TMEM lane quarter, each owning half the columns
-constexpr int kThreads = 64 + 32 * kNumEpiWarps;
 constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
 
 enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3, kEpiOptBF16 = 4 };
@@ -68,10 +66,15 @@ struct TileCfg {
     static constexpr int kBBytes = kBLoad * kBK * 2;  // one stage of X: kBLoad/64 boxes of [64 tokens][64 cols]
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator (128 lanes x BN)
+    // epilogue warps: two per TMEM lane quarter, each owning half the tile's columns; the INT8-state
+    // epilogue of a CTA pair has four per quarter, one 64-column quantisation block each, because
+    // its dependent arithmetic needs more warps per scheduler to keep issuing
+    static constexpr int kEpiWarps = (EPI == kEpiOptINT8 && CG == 2) ? 16 : 8;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
     // one warp's 32 x 32 FP32 transpose strip; the INT8 epilogue stages two (a 64-column block);
     // the input-gradient epilogue stores rows as they come out of TMEM and needs none
     static constexpr int kStripBytes = EPI == kEpiDX ? 0 : (EPI == kEpiOptINT8 ? 2 : 1) * 32 * 32 * 4;
-    static constexpr int kEpiBytes = kNumEpiWarps * kStripBytes;
+    static constexpr int kEpiBytes = kEpiWarps * kStripBytes;
     static constexpr int kBarrierBytes = 256;
     static constexpr int kMaxSmem = 232448;
     // as many operand stages as fit beside the epilogue buffers, at most 6
@@ -482,7 +485,7 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
     }
 }
 
-template <int OPT, int WIDTH, bool SCALE>
+template <int OPT, int WIDTH, bool SCALE, bool PREFETCH>
 __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int col0, uint32_t taddr,
                                              uint8_t* strip) {
     static_assert(WIDTH % 64 == 0, "whole quantisation blocks");
@@ -495,15 +498,27 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
         // d_in is a multiple of 64, so a 64-column block lies wholly inside or outside the layer:
         // the same for every lane of the warp
         if (col0 + c >= a.d_in) break;
-        Int8RowIn<OPT> in[2];
-        int8_row_load<OPT>(a, lane_base + c, row < a.d_out, in[0]);
         strip_store<SCALE>(taddr + c, strip, a, row0 + lane, col0 + c);
         strip_store<SCALE>(taddr + c + 32, strip + 4096, a, row0 + lane, col0 + c + 32);
+        if constexpr (PREFETCH) {
+            // the next row group's inputs load while this one updates
+            Int8RowIn<OPT> in[2];
+            int8_row_load<OPT>(a, lane_base + c, row < a.d_out, in[0]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if (k < 3)
-                int8_row_load<OPT>(a, lane_base + (k + 1) * row_step + c, row + 8 * (k + 1) < a.d_out, in[(k + 1) & 1]);
-            int8_row_update<OPT>(a, lane_base + k * row_step + c, row + 8 * k < a.d_out, strip, k, in[k & 1]);
+            for (int k = 0; k < 4; ++k) {
+                if (k < 3)
+                    int8_row_load<OPT>(a, lane_base + (k + 1) * row_step + c, row + 8 * (k + 1) < a.d_out,
+                                       in[(k + 1) & 1]);
+                int8_row_update<OPT>(a, lane_base + k * row_step + c, row + 8 * k < a.d_out, strip, k, in[k & 1]);
+            }
+        } else {
+            // enough warps per scheduler to cover the load latency without a second row in flight
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) {
+                Int8RowIn<OPT> in;
+                int8_row_load<OPT>(a, lane_base + k * row_step + c, row + 8 * k < a.d_out, in);
+                int8_row_update<OPT>(a, lane_base + k * row_step + c, row + 8 * k < a.d_out, strip, k, in);
+            }
         }
     }
 }
@@ -523,7 +538,7 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
 //         MMAs have consumed it, so each pair's commit of a stage arrives in all four CTAs.
 
 template <int BN, int CL, int EPI, int OPT, int OPS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI>::kThreads, 1)
     forge_tile_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
                       const TileArgs a) {
     static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
@@ -539,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 128B-swizzle atoms need 1024B alignment
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::kStages * C::kABytes;
-    uint8_t* strips = smem + C::kStages * C::kStageBytes;  // kNumEpiWarps x 4 KiB transpose strips
+    uint8_t* strips = smem + C::kStages * C::kStageBytes;  // one transpose strip (or two) per epilogue warp
     uint64_t* full = reinterpret_cast<uint64_t*>(strips + C::kEpiBytes);
     uint64_t* empty = full + C::kStages;
     uint64_t* acc_full = empty + C::kStages;
@@ -564,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], kNumEpiWarps * CG);
+            mbar_init(&acc_empty[i], C::kEpiWarps * CG);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -716,8 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- epilogue warps (every CTA)
         const int e = warp - 2;
         const int quarter = warp & 3;   // a warp may only touch TMEM lanes 32*(warp%4) .. +31
-        const int half = e >> 2;
-        constexpr int kWidth = BN / 2;
+        const int half = e >> 2;                // column part owned by this warp
+        constexpr int kWidth = BN / (C::kEpiWarps / 4);
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = first_tile; tile < a.num_tiles; tile += tile_stride) {
@@ -745,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 epi_opt_dense<OPT, kWidth, EPI == kEpiOptBF16, kScale>(a, row0, col0, taddr, strip, row0n, col0n);
             }
-            else epi_opt_int8<OPT, kWidth, kScale>(a, row0, col0, taddr, strip);
+            else epi_opt_int8<OPT, kWidth, kScale, C::kEpiWarps == 8>(a, row0, col0, taddr, strip);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
