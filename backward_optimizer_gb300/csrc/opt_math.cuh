@@ -115,6 +115,50 @@ __device__ __forceinline__ uint32_t int8_code(float x, float s) {
     return static_cast<uint32_t>(q) & 0xFFu;
 }
 
+// The same codes without a division or a float-to-int conversion per element, for epilogues that
+// code many values against one block scale.  Words of codes are first XORed with 0x80808080, which
+// turns each signed code c into the byte c + 128.
+//
+// Decoding: that byte as the low mantissa bits of 2^23 is the binary32 value 2^23 + c + 128, and
+// subtracting 2^23 + 128 leaves c exactly.
+__device__ __forceinline__ float int8_at_flipped(uint32_t flipped, int k) {
+    return __fsub_rn(__uint_as_float(__byte_perm(flipped, 0x4B000000u, 0x7650u | static_cast<uint32_t>(k))),
+                     8388736.0f);
+}
+
+// Encoding against one scale s: r = RN(1/s), q = RN(x r).  Then |q - x/s| <= |x/s| (2^-23 + 2^-48)
+// < 2^-16 (|x| <= absmax, so |x/s| <= 127.00001), and RN(x/s) lies within 2^-18 of x/s, so the two
+// differ by less than 2^-15.  Where q is farther than 2^-14 from every half-integer both round to
+// the same integer, which RN(q + 1.5 * 2^23) holds in its low mantissa bits (|q| < 2^22); the
+// clamp cannot act (|q| < 127.5).  Elsewhere -- near or at a tie, s subnormal, 0 or not finite, x
+// NaN -- the code comes from the IEEE division of int8_code.
+struct Int8Coder {
+    float s, r;
+    bool fast;  // s normal and 1/s normal
+};
+
+__device__ __forceinline__ Int8Coder int8_coder(float s) {
+    Int8Coder c;
+    c.s = s;
+    c.fast = s >= 0x1p-126f && s <= 0x1p125f;
+    c.r = c.fast ? __frcp_rn(s) : 0.0f;
+    return c;
+}
+
+// the code in the low byte (higher bytes unspecified)
+__device__ __forceinline__ uint32_t int8_code_low(float x, const Int8Coder& c) {
+    const float q = __fmul_rn(x, c.r);
+    const float t = __fadd_rn(q, 12582912.0f);
+    const float d = __fsub_rn(q, __fsub_rn(t, 12582912.0f));  // q - rne(q), exact
+    if (c.fast && fabsf(d) < 0.49993896484375f) return __float_as_uint(t);  // 0.5 - 2^-14
+    return int8_code(x, c.s);
+}
+
+// four codes (low bytes of a..d) into one word, a in the lowest byte
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
 // ---------------------------------------------------------------- the eight updates
 // g: binary32 gradient; w: binary32 weight (from bfloat16); m, v: binary32 moments, updated
 // in place.  Returns the new binary32 weight.  Intrinsics fix each rounding so that the

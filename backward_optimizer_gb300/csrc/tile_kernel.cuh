@@ -426,6 +426,13 @@ __device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e_row, b
     }
     in.ms = Tr::kM ? a.m_scales[e_row >> 6] : 0.f;
     in.vs = Tr::kV ? a.v_scales[e_row >> 6] : 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            in.mq[h][i] ^= 0x80808080u;  // the biased form int8_at_flipped decodes
+            in.vq[h][i] ^= 0x80808080u;
+        }
 }
 
 template <int OPT>
@@ -441,8 +448,8 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
-            float mm = Tr::kM ? __fmul_rn(int8_at(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
-            float vv = Tr::kV ? __fmul_rn(int8_at(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
+            float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
+            float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
             opt_moments<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
             am = fmaxf(am, fabsf(mm));
             av = fmaxf(av, fabsf(vv));
@@ -454,6 +461,7 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
         av = fmaxf(av, __shfl_xor_sync(0xFFFFFFFFu, av, off));
     }
     const float nms = __fdiv_rn(am, 127.0f), nvs = __fdiv_rn(av, 127.0f);
+    const Int8Coder cm = int8_coder(Tr::kM ? nms : 0.f), cv = int8_coder(Tr::kV ? nvs : 0.f);
     // pass 2: update, round, requantise, store
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -461,17 +469,23 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
         strip_load_row(strip + h * 4096, k, g);
         const size_t e = e_row + 32 * h;
         const Philox4 p = sr_words(e >> 3, a.seed, a.step);
-        uint32_t mo[2] = {0u, 0u}, vo[2] = {0u, 0u};
+        uint32_t mc[8], vc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
-            float mm = Tr::kM ? __fmul_rn(int8_at(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
-            float vv = Tr::kV ? __fmul_rn(int8_at(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
+            float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
+            float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
             const float wn = opt_update<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
             const uint32_t b = sr_bf16(wn, sr_r16(p, j));
             in.w[h][j >> 1] = (j & 1) ? ((in.w[h][j >> 1] & 0xFFFFu) | (b << 16)) : ((in.w[h][j >> 1] & 0xFFFF0000u) | b);
-            if constexpr (Tr::kM) mo[j >> 2] |= int8_code(mm, nms) << (8 * (j & 3));
-            if constexpr (Tr::kV) vo[j >> 2] |= int8_code(vv, nvs) << (8 * (j & 3));
+            if constexpr (Tr::kM) mc[j] = int8_code_low(mm, cm);
+            if constexpr (Tr::kV) vc[j] = int8_code_low(vv, cv);
+        }
+        uint32_t mo[2], vo[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if constexpr (Tr::kM) mo[i] = pack_low_bytes(mc[4 * i], mc[4 * i + 1], mc[4 * i + 2], mc[4 * i + 3]);
+            if constexpr (Tr::kV) vo[i] = pack_low_bytes(vc[4 * i], vc[4 * i + 1], vc[4 * i + 2], vc[4 * i + 3]);
         }
         if (ok) {
             st_v4(a.W + e, in.w[h]);

@@ -1,0 +1,104 @@
+"""INT8 requantisation pinned bit for bit through the kernels (needs a GB300).
+
+The other INT8 parity tests allow codes to differ by one, because the oracle computes the update in
+float64 and the kernels in binary32, so a moment that lands next to a rounding boundary can fall on
+either side.  Here every new moment is exact on both sides: the states start at zero, the decays
+are 1/2, weight decay is 0, and dY and X hold small integers, so dW = dY^T X is an exact integer
+whatever the summation order.  The new moments are then g/2, g or RN(g^2)/2 on both sides, and the
+block scale RN(absmax / 127) and every code rne(RN(x / s)) must agree exactly: this pins the
+kernels' division, rounding and clamping of the codes against the oracle's definition.
+"""
+import numpy as np
+import pytest
+import torch
+
+import backward_optimizer_gb300 as fg
+from oracle import step as ostep
+from tests.helpers import bits
+from workloads import Hparams, OPTIMIZERS, random_codes
+
+pytestmark = pytest.mark.gpu
+
+HALF = Hparams(lr=1e-3, beta1=0.5, beta2=0.5, eps=1e-8, weight_decay=0.0, momentum=0.9, alpha=0.5)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fg.build()
+    fg.lib()
+
+
+def _integer_bf16(shape, seed):
+    """Integers in [-15, 15] as bfloat16 (exact)."""
+    return (random_codes(shape, seed, -15, 15).to(torch.float32)).to(torch.bfloat16)
+
+
+def _case(opt, d_out, d_in, T, seed):
+    dy = _integer_bf16((T, d_out), seed)
+    x = _integer_bf16((T, d_in), seed + 1)
+    w = (torch.randn(d_out, d_in, generator=torch.Generator().manual_seed(seed + 2)) * 0.02).to(torch.bfloat16)
+    zeros = np.zeros((d_out, d_in), np.int8)
+    nblk = d_out * d_in // 64
+    return dy, x, w, zeros, np.zeros((d_out, d_in // 64), np.float32), nblk
+
+
+def _check(opt, M, V, Q, ref, nblk, g):
+    # the construction's premise, on the oracle's side: new moments g/2, g, RN(g^2)/2 or RN(g^2)
+    exact_m = {"sgd_momentum": g}.get(opt, g / 2)
+    g2 = (g.astype(np.float64) ** 2).astype(np.float32)
+    exact_v = g2 if opt == "adagrad" else g2 / 2
+    if ref["m_f32"] is not None:
+        assert np.array_equal(ref["m_f32"], exact_m.astype(np.float32))
+    if ref["v_f32"] is not None:
+        assert np.array_equal(ref["v_f32"], exact_v)
+    q = Q.cpu().numpy()
+    for got, codes, scales, sl in ((M, ref["m"], ref["m_scales"], slice(0, nblk)),
+                                   (V, ref["v"], ref["v_scales"], slice(nblk, 2 * nblk))):
+        if codes is None:
+            continue
+        assert np.array_equal(got.cpu().numpy(), codes), f"{opt}: {np.sum(got.cpu().numpy() != codes)} codes differ"
+        assert np.array_equal(q[sl].view(np.uint32), scales.ravel().astype(np.float32).view(np.uint32)), \
+            f"{opt}: scales differ"
+
+
+def _exact_gradient(dy, x):
+    g = ostep.dw(bits(dy), bits(x))
+    assert np.array_equal(g, np.rint(g)) and np.abs(g).max() < 2 ** 24
+    return g
+
+
+# (d_out, d_in, T): a CTA-pair kernel, 256 x 256 tiles; one CTA on 128-row tiles
+SHAPES = [(512, 768, 256, (256, 256)), (384, 512, 192, (128, 256))]
+
+
+@pytest.mark.parametrize("opt", [o for o in OPTIMIZERS if o != "sgd"])
+@pytest.mark.parametrize("d_out, d_in, T, tile", SHAPES)
+def test_fused_int8_codes_are_exact(opt, d_out, d_in, T, tile):
+    got = fg.launch_shape(d_out, d_in, T)
+    assert (got["tile_rows"], got["tile_cols"]) == tile
+    dy, x, w, zeros, zscales, nblk = _case(opt, d_out, d_in, T, seed=10 * OPTIMIZERS.index(opt))
+    g = _exact_gradient(dy, x)
+    W, M, V = w.cuda(), torch.from_numpy(zeros).cuda(), torch.from_numpy(zeros).cuda()
+    Q = torch.zeros(2 * nblk, dtype=torch.float32, device="cuda")
+    fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, Q, opt, HALF, 1, seed=1)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
+    ref = ostep.apply_update(opt, g, bits(w), zeros, zeros, HALF, 1, 1, e, "int8", zscales, zscales)
+    _check(opt, M, V, Q, ref, nblk, g)
+
+
+@pytest.mark.parametrize("opt", ["adamw", "adagrad", "sgd_momentum"])
+def test_two_phase_int8_codes_are_exact(opt):
+    d_out, d_in, T = 256, 512, 128
+    dy, x, w, zeros, zscales, nblk = _case(opt, d_out, d_in, T, seed=77)
+    g = _exact_gradient(dy, x)
+    W, M, V = w.cuda(), torch.from_numpy(zeros).cuda(), torch.from_numpy(zeros).cuda()
+    Q = torch.zeros(2 * nblk, dtype=torch.float32, device="cuda")
+    fg.opt_step(torch.from_numpy(g).cuda(), W, M, V, Q, opt, HALF, 1, seed=1)
+    torch.cuda.synchronize()
+    e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
+    ref = ostep.apply_update(opt, g, bits(w), zeros, zeros, HALF, 1, 1, e, "int8", zscales, zscales)
+    _check(opt, M, V, Q, ref, nblk, g)
