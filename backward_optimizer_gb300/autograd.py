@@ -2,10 +2,11 @@
 
 `ForgeLinear` computes y = x W^T.  Its backward does for one linear layer what the FORGE method
 does in a training step ("FORGE: Fused On-Register Gradient Elimination for Memory-Efficient LLM
-Training", §2 Method): the input gradient dX = dY W is taken from the weights as they were, then
-the weight gradient dW = dY^T X is accumulated tile by tile and consumed by the optimizer inside the
-same kernel, which updates W and the optimizer state in place (`linear_backward`).  No weight
-gradient exists afterwards: `weight.grad` stays None and there is no separate optimizer step.
+Training", §2 Methodology, Core mechanism): the input gradient dX = dY W is taken from the weights
+as they were, then the weight gradient dW = dY^T X is accumulated tile by tile and consumed by the
+optimizer inside the same kernel, which updates W and the optimizer state in place
+(`linear_backward`).  No weight gradient exists afterwards: `weight.grad` stays None and there is
+no separate optimizer step.
 
 The forward is PyTorch's own `linear`; the backward runs only this library's kernels.  Because the
 weights change during the backward, a weight that the same backward reads again (tied weights, a
