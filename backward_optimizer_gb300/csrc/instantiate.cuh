@@ -12,7 +12,7 @@ namespace forge {
 template <int OPT, int EPI, int BN, int CL, int OPS>
 cudaError_t launch_tile(const TileLaunch& l) {
     constexpr int CG = CL == 1 ? 1 : 2;
-    using C = TileCfg<BN, CG, EPI>;
+    using C = TileCfg<BN, CG, EPI, OPS>;
     auto kernel = forge_tile_kernel<BN, CL, EPI, OPT, OPS>;
     static std::atomic<uint64_t> configured{0};  // one bit per device ordinal
     static std::atomic<int> max_clusters[64];    // co-resident clusters per device

@@ -57,7 +57,7 @@ struct OperandTraits {
     static constexpr int kStepBytes = OPS == kOpsE4M3 ? 4096 : 2048;  // rows one MMA consumes (K)
 };
 
-template <int BN, int CG, int EPI>
+template <int BN, int CG, int EPI, int OPS = kOpsBF16>
 struct TileCfg {
     static_assert(BN == 128 || BN == 256, "tile width");
     static_assert(CG == 1 || CG == 2, "CTA group");
@@ -66,10 +66,14 @@ struct TileCfg {
     static constexpr int kBBytes = kBLoad * kBK * 2;  // one stage of X: kBLoad/64 boxes of [64 tokens][64 cols]
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator (128 lanes x BN)
-    // epilogue warps: two per TMEM lane quarter, each owning half the tile's columns; the INT8-state
-    // epilogue of a CTA pair has four per quarter, one 64-column quantisation block each, because
-    // its dependent arithmetic needs more warps per scheduler to keep issuing
-    static constexpr int kEpiWarps = (EPI == kEpiOptINT8 && CG == 2) ? 16 : 8;
+    // epilogue warps: two per TMEM lane quarter, each owning half the tile's columns.  A CTA pair
+    // runs four per quarter, one 64-column block each, where the epilogue rather than the
+    // operand stream sets the pace: the INT8-state epilogue, whose dependent arithmetic needs
+    // more warps per scheduler to keep issuing, and any optimizer epilogue behind the E4M3
+    // mainloop, which is half as long as the bf16 one
+    static constexpr bool kWideEpi =
+        CG == 2 && (EPI == kEpiOptINT8 || (OPS == kOpsE4M3 && (EPI == kEpiOptFP32 || EPI == kEpiOptBF16)));
+    static constexpr int kEpiWarps = kWideEpi ? 16 : 8;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     // one warp's 32 x 32 FP32 transpose strip; the INT8 epilogue stages two (a 64-column block);
     // the input-gradient epilogue stores rows as they come out of TMEM and needs none
@@ -267,7 +271,7 @@ __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int 
 
 // Dense states: binary32 (BF16S = false) or bfloat16 rounded stochastically with their own Philox
 // streams (BF16S = true).  The update always runs on binary32 moments; only their storage differs.
-template <int OPT, int WIDTH, bool BF16S, bool SCALE>
+template <int OPT, int WIDTH, bool BF16S, bool SCALE, int R>
 __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int col0, uint32_t taddr,
                                               uint8_t* strip, int row0n = -1, int col0n = 0) {
     using Tr = OptTraits<OPT>;
@@ -279,81 +283,90 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
     const size_t row_step = static_cast<size_t>(8) * a.d_in;
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 32) {
-        uint32_t w[4][4], m[4][kSW], v[4][kSW];
-        bool ok[4];
-        // the W/m/v loads do not depend on the gradient: issue them before the TMEM read
+        // R of the four row groups hold their W/m/v in registers at once: all four with two
+        // epilogue warps per scheduler, so that every group's loads overlap the TMEM read; one
+        // with four warps per scheduler, whose 96 registers a thread leave no room for more and
+        // whose other warps cover the load latency instead
+#pragma unroll 1
+        for (int kk = 0; kk < 4; kk += R) {
+            uint32_t w[R][4], m[R][kSW], v[R][kSW];
+            bool ok[R];
+            // the W/m/v loads do not depend on the gradient: issue them before the TMEM read
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            ok[k] = col + c < a.d_in && row + 8 * k < a.d_out;
-            // a run outside the layer loads the layer's first run instead (always valid) and
-            // stores nothing, so the loads stay unconditional
-            const size_t el = ok[k] ? lane_base + k * row_step + c : 0;
-            ld_v4(a.W + el, w[k]);
-            if constexpr (BF16S) {
-                if constexpr (Tr::kM) ld_v4(static_cast<uint16_t*>(a.m) + el, m[k]);
-                if constexpr (Tr::kV) ld_v4(static_cast<uint16_t*>(a.v) + el, v[k]);
-            } else {
-                if constexpr (Tr::kM) ld_v8(static_cast<float*>(a.m) + el, m[k]);
-                if constexpr (Tr::kV) ld_v8(static_cast<float*>(a.v) + el, v[k]);
-            }
-            // the next 32 columns' W/m/v into L2 now, so their loads wait on L2 rather than DRAM; in
-            // the last step, the first 32 columns of this warp's next tile
-            const bool last = c + 32 >= WIDTH;
-            const int rn = last ? row0n + (lane >> 2) + 8 * k : row + 8 * k;
-            const int cn = last ? col0n + 8 * (lane & 3) : col + c + 32;
-            if ((!last || row0n >= 0) && cn < a.d_in && rn < a.d_out) {
-                const size_t en = static_cast<size_t>(rn) * a.d_in + cn;
-                prefetch_l2(a.W + en);
+            for (int r = 0; r < R; ++r) {
+                const int k = kk + r;
+                ok[r] = col + c < a.d_in && row + 8 * k < a.d_out;
+                // a run outside the layer loads the layer's first run instead (always valid) and
+                // stores nothing, so the loads stay unconditional
+                const size_t el = ok[r] ? lane_base + k * row_step + c : 0;
+                ld_v4(a.W + el, w[r]);
                 if constexpr (BF16S) {
-                    if constexpr (Tr::kM) prefetch_l2(static_cast<uint16_t*>(a.m) + en);
-                    if constexpr (Tr::kV) prefetch_l2(static_cast<uint16_t*>(a.v) + en);
+                    if constexpr (Tr::kM) ld_v4(static_cast<uint16_t*>(a.m) + el, m[r]);
+                    if constexpr (Tr::kV) ld_v4(static_cast<uint16_t*>(a.v) + el, v[r]);
                 } else {
-                    if constexpr (Tr::kM) prefetch_l2(static_cast<float*>(a.m) + en);
-                    if constexpr (Tr::kV) prefetch_l2(static_cast<float*>(a.v) + en);
+                    if constexpr (Tr::kM) ld_v8(static_cast<float*>(a.m) + el, m[r]);
+                    if constexpr (Tr::kV) ld_v8(static_cast<float*>(a.v) + el, v[r]);
+                }
+                // the next 32 columns' W/m/v into L2 now, so their loads wait on L2 rather than DRAM;
+                // in the last step, the first 32 columns of this warp's next tile
+                const bool last = c + 32 >= WIDTH;
+                const int rn = last ? row0n + (lane >> 2) + 8 * k : row + 8 * k;
+                const int cn = last ? col0n + 8 * (lane & 3) : col + c + 32;
+                if ((!last || row0n >= 0) && cn < a.d_in && rn < a.d_out) {
+                    const size_t en = static_cast<size_t>(rn) * a.d_in + cn;
+                    prefetch_l2(a.W + en);
+                    if constexpr (BF16S) {
+                        if constexpr (Tr::kM) prefetch_l2(static_cast<uint16_t*>(a.m) + en);
+                        if constexpr (Tr::kV) prefetch_l2(static_cast<uint16_t*>(a.v) + en);
+                    } else {
+                        if constexpr (Tr::kM) prefetch_l2(static_cast<float*>(a.m) + en);
+                        if constexpr (Tr::kV) prefetch_l2(static_cast<float*>(a.v) + en);
+                    }
                 }
             }
-        }
-        // the gradient strip goes to shared memory once; each row group then reads its 8 values
-        strip_store<SCALE>(taddr + c, strip, a, row0 + lane, col0 + c);
+            // the gradient strip goes to shared memory once; each row group then reads its 8 values
+            if (kk == 0) strip_store<SCALE>(taddr + c, strip, a, row0 + lane, col0 + c);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const size_t e = lane_base + k * row_step + c;
-            uint32_t g[8];
-            strip_load_row(strip, k, g);
-            const Philox4 p = sr_words(e >> 3, a.seed, a.step);
-            Philox4 pm{}, pv{};
-            if constexpr (BF16S && Tr::kM) pm = sr_words(e >> 3, a.seed, a.step, kStreamM);
-            if constexpr (BF16S && Tr::kV) pv = sr_words(e >> 3, a.seed, a.step, kStreamV);
+            for (int r = 0; r < R; ++r) {
+                const int k = kk + r;
+                const size_t e = lane_base + k * row_step + c;
+                uint32_t g[8];
+                strip_load_row(strip, k, g);
+                const Philox4 p = sr_words(e >> 3, a.seed, a.step);
+                Philox4 pm{}, pv{};
+                if constexpr (BF16S && Tr::kM) pm = sr_words(e >> 3, a.seed, a.step, kStreamM);
+                if constexpr (BF16S && Tr::kV) pv = sr_words(e >> 3, a.seed, a.step, kStreamV);
 #pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-                const uint32_t wp = w[k][j >> 1];
-                float m0 = 0.f, m1 = 0.f, v0 = 0.f, v1 = 0.f;
-                if constexpr (BF16S) {
-                    if constexpr (Tr::kM) { m0 = bf16_lo(m[k][j >> 1]); m1 = bf16_hi(m[k][j >> 1]); }
-                    if constexpr (Tr::kV) { v0 = bf16_lo(v[k][j >> 1]); v1 = bf16_hi(v[k][j >> 1]); }
-                } else {
-                    if constexpr (Tr::kM) { m0 = __uint_as_float(m[k][j]); m1 = __uint_as_float(m[k][j + 1]); }
-                    if constexpr (Tr::kV) { v0 = __uint_as_float(v[k][j]); v1 = __uint_as_float(v[k][j + 1]); }
+                for (int j = 0; j < 8; j += 2) {
+                    const uint32_t wp = w[r][j >> 1];
+                    float m0 = 0.f, m1 = 0.f, v0 = 0.f, v1 = 0.f;
+                    if constexpr (BF16S) {
+                        if constexpr (Tr::kM) { m0 = bf16_lo(m[r][j >> 1]); m1 = bf16_hi(m[r][j >> 1]); }
+                        if constexpr (Tr::kV) { v0 = bf16_lo(v[r][j >> 1]); v1 = bf16_hi(v[r][j >> 1]); }
+                    } else {
+                        if constexpr (Tr::kM) { m0 = __uint_as_float(m[r][j]); m1 = __uint_as_float(m[r][j + 1]); }
+                        if constexpr (Tr::kV) { v0 = __uint_as_float(v[r][j]); v1 = __uint_as_float(v[r][j + 1]); }
+                    }
+                    const float w0 = opt_update<OPT>(__uint_as_float(g[j]), bf16_lo(wp), m0, v0, a.s);
+                    const float w1 = opt_update<OPT>(__uint_as_float(g[j + 1]), bf16_hi(wp), m1, v1, a.s);
+                    w[r][j >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
+                    if constexpr (BF16S) {
+                        if constexpr (Tr::kM) m[r][j >> 1] = sr_bf16(m0, sr_r16(pm, j)) | (sr_bf16(m1, sr_r16(pm, j + 1)) << 16);
+                        if constexpr (Tr::kV) v[r][j >> 1] = sr_bf16(v0, sr_r16(pv, j)) | (sr_bf16(v1, sr_r16(pv, j + 1)) << 16);
+                    } else {
+                        if constexpr (Tr::kM) { m[r][j] = __float_as_uint(m0); m[r][j + 1] = __float_as_uint(m1); }
+                        if constexpr (Tr::kV) { v[r][j] = __float_as_uint(v0); v[r][j + 1] = __float_as_uint(v1); }
+                    }
                 }
-                const float w0 = opt_update<OPT>(__uint_as_float(g[j]), bf16_lo(wp), m0, v0, a.s);
-                const float w1 = opt_update<OPT>(__uint_as_float(g[j + 1]), bf16_hi(wp), m1, v1, a.s);
-                w[k][j >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
-                if constexpr (BF16S) {
-                    if constexpr (Tr::kM) m[k][j >> 1] = sr_bf16(m0, sr_r16(pm, j)) | (sr_bf16(m1, sr_r16(pm, j + 1)) << 16);
-                    if constexpr (Tr::kV) v[k][j >> 1] = sr_bf16(v0, sr_r16(pv, j)) | (sr_bf16(v1, sr_r16(pv, j + 1)) << 16);
-                } else {
-                    if constexpr (Tr::kM) { m[k][j] = __float_as_uint(m0); m[k][j + 1] = __float_as_uint(m1); }
-                    if constexpr (Tr::kV) { v[k][j] = __float_as_uint(v0); v[k][j + 1] = __float_as_uint(v1); }
-                }
-            }
-            if (ok[k]) {
-                st_v4(a.W + e, w[k]);
-                if constexpr (BF16S) {
-                    if constexpr (Tr::kM) st_v4(static_cast<uint16_t*>(a.m) + e, m[k]);
-                    if constexpr (Tr::kV) st_v4(static_cast<uint16_t*>(a.v) + e, v[k]);
-                } else {
-                    if constexpr (Tr::kM) st_v8(static_cast<float*>(a.m) + e, m[k]);
-                    if constexpr (Tr::kV) st_v8(static_cast<float*>(a.v) + e, v[k]);
+                if (ok[r]) {
+                    st_v4(a.W + e, w[r]);
+                    if constexpr (BF16S) {
+                        if constexpr (Tr::kM) st_v4(static_cast<uint16_t*>(a.m) + e, m[r]);
+                        if constexpr (Tr::kV) st_v4(static_cast<uint16_t*>(a.v) + e, v[r]);
+                    } else {
+                        if constexpr (Tr::kM) st_v8(static_cast<float*>(a.m) + e, m[r]);
+                        if constexpr (Tr::kV) st_v8(static_cast<float*>(a.v) + e, v[r]);
+                    }
                 }
             }
         }
@@ -552,7 +565,7 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
 //         MMAs have consumed it, so each pair's commit of a stage arrives in all four CTAs.
 
 template <int BN, int CL, int EPI, int OPT, int OPS>
-__global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI>::kThreads, 1)
+__global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThreads, 1)
     forge_tile_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
                       const TileArgs a) {
     static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
@@ -561,7 +574,7 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI>::kThreads,
     constexpr bool kScale = OPS == kOpsE4M3;
     constexpr int CG = CL == 1 ? 1 : 2;       // CTAs per MMA (cta_group)
     constexpr int kPairs = CL == 4 ? 2 : 1;   // MMA groups per cluster sharing dY
-    using C = TileCfg<BN, CG, EPI>;
+    using C = TileCfg<BN, CG, EPI, OPS>;
     constexpr bool kAKMajor = EPI == kEpiDX;  // A = dY with d_out (= K) along memory
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -772,7 +785,8 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI>::kThreads,
                     row0n = mbn * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
                     col0n = (nbn * kPairs + static_cast<int>(pair)) * BN + half * kWidth;
                 }
-                epi_opt_dense<OPT, kWidth, EPI == kEpiOptBF16, kScale>(a, row0, col0, taddr, strip, row0n, col0n);
+                epi_opt_dense<OPT, kWidth, EPI == kEpiOptBF16, kScale, (C::kEpiWarps == 8 ? 4 : 1)>(
+                    a, row0, col0, taddr, strip, row0n, col0n);
             }
             else epi_opt_int8<OPT, kWidth, kScale, C::kEpiWarps == 8>(a, row0, col0, taddr, strip);
             tc_fence_before();
