@@ -145,18 +145,19 @@ __device__ __forceinline__ Int8Coder int8_coder(float s) {
     return c;
 }
 
-// the code in the low byte (higher bytes unspecified)
-__device__ __forceinline__ uint32_t int8_code_low(float x, const Int8Coder& c) {
+// The code in the low byte (higher bytes unspecified), without a branch; `exact` is false where
+// the code must come from int8_code instead.
+__device__ __forceinline__ uint32_t int8_code_fast(float x, const Int8Coder& c, bool& exact) {
     const float q = __fmul_rn(x, c.r);
     const float t = __fadd_rn(q, 12582912.0f);
     const float d = __fsub_rn(q, __fsub_rn(t, 12582912.0f));  // q - rne(q), exact
-    if (c.fast && fabsf(d) < 0.49993896484375f) return __float_as_uint(t);  // 0.5 - 2^-14
-    return int8_code(x, c.s);
+    exact = c.fast && fabsf(d) < 0.49993896484375f;           // 0.5 - 2^-14
+    return __float_as_uint(t);
 }
 
-// four codes (low bytes of a..d) into one word, a in the lowest byte
-__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+// word with its byte k (0..3) replaced by the low byte of c
+__device__ __forceinline__ uint32_t put_byte(uint32_t word, uint32_t c, int k) {
+    return __byte_perm(word, c, k == 0 ? 0x3214u : k == 1 ? 0x3240u : k == 2 ? 0x3410u : 0x4210u);
 }
 
 // ---------------------------------------------------------------- the eight updates

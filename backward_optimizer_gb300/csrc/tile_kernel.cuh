@@ -482,7 +482,8 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
         strip_load_row(strip + h * 4096, k, g);
         const size_t e = e_row + 32 * h;
         const Philox4 p = sr_words(e >> 3, a.seed, a.step);
-        uint32_t mc[8], vc[8];
+        uint32_t mo[2] = {0u, 0u}, vo[2] = {0u, 0u}, wo[4];
+        uint32_t redo = 0u;  // bit j: m code j needs the division; bit 8 + j: v code j
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
@@ -490,16 +491,39 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row,
             float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
             const float wn = opt_update<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
             const uint32_t b = sr_bf16(wn, sr_r16(p, j));
-            in.w[h][j >> 1] = (j & 1) ? ((in.w[h][j >> 1] & 0xFFFFu) | (b << 16)) : ((in.w[h][j >> 1] & 0xFFFF0000u) | b);
-            if constexpr (Tr::kM) mc[j] = int8_code_low(mm, cm);
-            if constexpr (Tr::kV) vc[j] = int8_code_low(vv, cv);
+            wo[j >> 1] = (j & 1) ? (wo[j >> 1] | (b << 16)) : b;
+            bool exact = true;
+            if constexpr (Tr::kM) {
+                mo[j >> 2] = put_byte(mo[j >> 2], int8_code_fast(mm, cm, exact), j & 3);
+                redo |= exact ? 0u : (1u << j);
+            }
+            if constexpr (Tr::kV) {
+                vo[j >> 2] = put_byte(vo[j >> 2], int8_code_fast(vv, cv, exact), j & 3);
+                redo |= exact ? 0u : (0x100u << j);
+            }
         }
-        uint32_t mo[2], vo[2];
+        if (redo != 0u) {
+            // rare: a code next to a rounding boundary, or a scale that is not a normal number.
+            // The moments are recomputed from the same inputs (gradient strip, old weights, old
+            // codes) and the IEEE division decides; one branch per 8 elements instead of one per
+            // code.
+            strip_load_row(strip + h * 4096, k, g);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            if constexpr (Tr::kM) mo[i] = pack_low_bytes(mc[4 * i], mc[4 * i + 1], mc[4 * i + 2], mc[4 * i + 3]);
-            if constexpr (Tr::kV) vo[i] = pack_low_bytes(vc[4 * i], vc[4 * i + 1], vc[4 * i + 2], vc[4 * i + 3]);
+            for (int j = 0; j < 8; ++j) {
+                if (redo & (0x101u << j)) {
+                    const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
+                    float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
+                    float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
+                    opt_moments<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
+                    if constexpr (Tr::kM)
+                        if ((redo >> j) & 1u) mo[j >> 2] = put_byte(mo[j >> 2], int8_code(mm, nms), j & 3);
+                    if constexpr (Tr::kV)
+                        if ((redo >> (8 + j)) & 1u) vo[j >> 2] = put_byte(vo[j >> 2], int8_code(vv, nvs), j & 3);
+                }
+            }
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) in.w[h][i] = wo[i];
         if (ok) {
             st_v4(a.W + e, in.w[h]);
             if constexpr (Tr::kM) st_v2(static_cast<int8_t*>(a.m) + e, mo);
