@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import backward_optimizer_gb300 as fg
-from oracle import step as ostep
+from oracle import fp8, step as ostep
 from tests.helpers import bits
 from workloads import Hparams, OPTIMIZERS, random_codes
 
@@ -69,8 +69,9 @@ def _exact_gradient(dy, x):
     return g
 
 
-# (d_out, d_in, T): a CTA-pair kernel, 256 x 256 tiles; one CTA on 128-row tiles
-SHAPES = [(512, 768, 256, (256, 256)), (384, 512, 192, (128, 256))]
+# (d_out, d_in, T): a CTA-pair kernel, 256 x 256 tiles; one CTA on 128-row tiles; two CTA pairs
+# sharing dY slices on 256 x 512 tiles (T = 8192)
+SHAPES = [(512, 768, 256, (256, 256)), (384, 512, 192, (128, 256)), (512, 1024, 8192, (256, 512))]
 
 
 @pytest.mark.parametrize("opt", [o for o in OPTIMIZERS if o != "sgd"])
@@ -101,4 +102,29 @@ def test_two_phase_int8_codes_are_exact(opt):
     torch.cuda.synchronize()
     e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
     ref = ostep.apply_update(opt, g, bits(w), zeros, zeros, HALF, 1, 1, e, "int8", zscales, zscales)
+    _check(opt, M, V, Q, ref, nblk, g)
+
+
+def _e4m3_codes(t):
+    """Small integers (|v| <= 15, exact in E4M3) as E4M3 codes."""
+    return t.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+@pytest.mark.parametrize("opt", ["adamw", "lion", "adagrad"])
+@pytest.mark.parametrize("d_out, d_in, T, tile", [SHAPES[0], SHAPES[2]])
+def test_fused_int8_codes_are_exact_with_e4m3_operands(opt, d_out, d_in, T, tile):
+    """The same construction through the E4M3 mainloop: integer codes with scales 1 keep g exact."""
+    got = fg.launch_shape(d_out, d_in, T)
+    assert (got["tile_rows"], got["tile_cols"]) == tile
+    dy, x, w, zeros, zscales, nblk = _case(opt, d_out, d_in, T, seed=200 + OPTIMIZERS.index(opt))
+    dyq, xq = _e4m3_codes(dy), _e4m3_codes(x)
+    g = fp8.dw_fp8(dyq.numpy(), xq.numpy(), 1.0, 1.0)
+    assert np.array_equal(g, _exact_gradient(dy, x))
+    W, M, V = w.cuda(), torch.from_numpy(zeros).cuda(), torch.from_numpy(zeros).cuda()
+    Q = torch.zeros(2 * nblk, dtype=torch.float32, device="cuda")
+    fg.fused_dw_step_e4m3(dyq.cuda(), xq.cuda(), 1.0, 1.0, W, M, V, Q, opt, HALF, 1, seed=1)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    ref = fp8.fused_step_fp8(opt, dyq.numpy(), xq.numpy(), 1.0, 1.0, bits(w), zeros, zeros, HALF, 1, 1, "int8",
+                             zscales, zscales)
     _check(opt, M, V, Q, ref, nblk, g)
