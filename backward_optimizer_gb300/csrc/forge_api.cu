@@ -233,11 +233,18 @@ struct TileShape {
 };
 // A ragged dimension (not a multiple of the tile) takes the wide shape once it is large enough that
 // the zero-filled tail costs little (over 1024).
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
 TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t T) {
     const bool rows256 = d_out % 256 == 0 || (d_out % 128 != 0 && d_out > 1024);
     const bool cols256 = d_in % 256 == 0 || (d_in % 128 != 0 && d_in > 1024);
     if (d_out % 256 == 0 && d_in % 512 == 0 && T >= 8192) return {256, 2, 4, 2};
-    if (rows256 && cols256) return {256, 2, 2, 1};
+    if (rows256 && cols256) {
+        // fewer than 4 pair tiles would leave all but a few SMs idle: 128 x 128 tiles give such a
+        // layer four times as many CTAs, each with a quarter of the epilogue
+        if (ceil_div(d_out, 256) * ceil_div(d_in, 256) < 4) return {128, 1, 1, 1};
+        return {256, 2, 2, 1};
+    }
     if (cols256) return {256, 1, 1, 1};
     return {128, 1, 1, 1};
 }
@@ -252,8 +259,6 @@ TileShape pick_dx_shape(int64_t T, int64_t d_out, int64_t d_in) {
     if (cols256) return {256, 1, 1, 1};
     return {128, 1, 1, 1};
 }
-
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <int OPS>
 TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t) {

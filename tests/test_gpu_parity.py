@@ -272,7 +272,7 @@ def test_status_word_clean_after_normal_runs():
 
 @pytest.mark.parametrize("d_out, d_in, T, rows, cols, cluster", [
     (512, 512, 8192, 256, 512, 4), (512, 512, 64, 256, 256, 2), (512, 768, 8192, 256, 256, 2),
-    (384, 256, 64, 128, 256, 1), (384, 384, 64, 128, 128, 1)])
+    (384, 256, 64, 128, 256, 1), (384, 384, 64, 128, 128, 1), (512, 256, 256, 128, 128, 1), (1024, 256, 64, 256, 256, 2)])
 def test_launch_shape_query(d_out, d_in, T, rows, cols, cluster):
     import ctypes
     shape = fg.ForgeShape(T=T, d_out=d_out, d_in=d_in, state=0, reserved=0)
