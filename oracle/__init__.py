@@ -22,12 +22,11 @@ Elimination for Memory-Efficient LLM Training" (gist.science technical summary):
 * the layer's input gradient dX = dY W from the weights before the step, and the
   layer backward in that order (§5 Significance and claims, limitations: the
   input gradient must be read before the weights are updated) -- ``backward.py``;
-* FP8 (E4M3) operands with per-tensor scales, dequantised on the gradient tile
-  (§4 Experimental results, "Composability") -- ``fp8.py``.
+* FP8 (E4M3) operands with per-tensor or per-channel scales, dequantised on the
+  gradient tile (§4 Experimental results, "Composability") -- ``fp8.py``.
 
 Every function here is pinned by tests under ``tests/`` against closed forms,
 textbook or library routines (``torch.optim`` in float64), brute force on tiny
-inputs, or a published known-answer value; the one exception is listed as
-"parity unpinned" in its own docstring.
+inputs, or a published known-answer value.
 """
 from . import backward, bf16, fp8, int8_block, optim, philox, step  # noqa: F401
