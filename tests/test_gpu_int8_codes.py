@@ -128,3 +128,40 @@ def test_fused_int8_codes_are_exact_with_e4m3_operands(opt, d_out, d_in, T, tile
     ref = fp8.fused_step_fp8(opt, dyq.numpy(), xq.numpy(), 1.0, 1.0, bits(w), zeros, zeros, HALF, 1, 1, "int8",
                              zscales, zscales)
     _check(opt, M, V, Q, ref, nblk, g)
+
+
+def _random_int8_state(shape, seed):
+    """Random signed m codes and non-negative v codes with positive block scales."""
+    g = torch.Generator().manual_seed(seed)
+    m = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
+    v = torch.randint(0, 128, shape, generator=g, dtype=torch.int8)
+    n = shape[0] * shape[1] // 64
+    q = torch.cat([torch.rand(n, generator=g) * 1e-5, torch.rand(n, generator=g) * 1e-8])
+    return m, v, q
+
+
+@pytest.mark.parametrize("opt", [o for o in OPTIMIZERS if o != "sgd"])
+@pytest.mark.parametrize("d_out, d_in, T, tile", SHAPES)
+def test_fused_int8_equals_two_phase_bitwise(opt, d_out, d_in, T, tile):
+    """Random states and operands: the fused kernel codes from the block's reciprocal (and the
+    IEEE division near rounding boundaries), the two-phase kernel always divides.  Same mainloop,
+    same moments, so weights, codes and scales must agree bit for bit."""
+    got = fg.launch_shape(d_out, d_in, T)
+    assert (got["tile_rows"], got["tile_cols"]) == tile
+    from workloads import normal_bf16
+    dy = normal_bf16((T, d_out), 1e-3, seed=300 + T).cuda()
+    x = normal_bf16((T, d_in), 1.0, seed=301 + T).cuda()
+    w = normal_bf16((d_out, d_in), 2e-2, seed=302).cuda()
+    m, v, q = (t.cuda() for t in _random_int8_state((d_out, d_in), 303 + OPTIMIZERS.index(opt)))
+    hp = Hparams(lr=1e-3)
+    W1, M1, V1, Q1 = w.clone(), m.clone(), v.clone(), q.clone()
+    W2, M2, V2, Q2 = w.clone(), m.clone(), v.clone(), q.clone()
+    fg.fused_dw_step(dy, x, W1, M1, V1, Q1, opt, hp, 3, seed=4)
+    dW = torch.empty(d_out, d_in, dtype=torch.float32, device="cuda")
+    fg.dw_gemm(dy, x, dW)
+    fg.opt_step(dW, W2, M2, V2, Q2, opt, hp, 3, seed=4)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    assert torch.equal(W1.view(torch.int16), W2.view(torch.int16))
+    assert torch.equal(M1, M2) and torch.equal(V1, V2)
+    assert torch.equal(Q1.view(torch.int32), Q2.view(torch.int32))
