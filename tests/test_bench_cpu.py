@@ -32,3 +32,36 @@ def test_llama_mlp_launch_bytes():
     """The figure the profile summary derives: 1.325 GB per Llama-8B MLP launch (AdamW, FP32 states)."""
     wl = WORKLOADS["llama8b-mlp"]
     assert bench.algorithmic_bytes(wl, "adamw", "fp32", "bf16") / 3 == pytest.approx(1.3254e9, rel=1e-4)
+
+
+def _run_bench(*args):
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    return subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], capture_output=True, text=True,
+                          cwd=root, timeout=600)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`--impl reference` times the oracle on a bounded sample and prints one JSON line with the
+    contract's keys; the host-buffer e2e of a CPU program moves no bytes over the host link."""
+    import json
+    r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3", "--oracle-rows", "8")
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["n_gpus"] == 1 and line["steps"] == 1 and line["warmup"] == 3
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["config"]["workload"].startswith(WORKLOADS["llama8b-mlp"].name)
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_fewer_than_three_warmup_steps_are_refused():
+    r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "2")
+    assert r.returncode != 0 and "--warmup must be >= 3" in r.stderr
