@@ -65,3 +65,13 @@ def test_reference_arm_prints_the_contract_line():
 def test_fewer_than_three_warmup_steps_are_refused():
     r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "2")
     assert r.returncode != 0 and "--warmup must be >= 3" in r.stderr
+
+
+def test_traffic_is_reported_only_for_the_sources_it_was_taken_from(monkeypatch):
+    """The committed DRAM traffic per launch stands for the kernel sources whose hash it records;
+    once they change, the bench reports no traffic rather than a stale figure."""
+    got = bench._ncu_traffic("llama8b-mlp", "adamw", "fp32")
+    assert got is not None and got > bench.algorithmic_bytes(WORKLOADS["llama8b-mlp"], "adamw", "fp32", "bf16") / 3
+    monkeypatch.setattr(bench, "_kernel_source_hash", lambda: "0" * 16)
+    assert bench._ncu_traffic("llama8b-mlp", "adamw", "fp32") is None
+    assert bench._ncu_traffic("no-such-workload", "adamw", "fp32") is None
