@@ -70,8 +70,14 @@ def test_fewer_than_three_warmup_steps_are_refused():
 def test_traffic_is_reported_only_for_the_sources_it_was_taken_from(monkeypatch):
     """The committed DRAM traffic per launch stands for the kernel sources whose hash it records;
     once they change, the bench reports no traffic rather than a stale figure."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")) as f:
+        entry = json.load(f)["llama8b-mlp/adamw/fp32"]
+    monkeypatch.setattr(bench, "_kernel_source_hash", lambda: entry["source_hash"])
     got = bench._ncu_traffic("llama8b-mlp", "adamw", "fp32")
-    assert got is not None and got > bench.algorithmic_bytes(WORKLOADS["llama8b-mlp"], "adamw", "fp32", "bf16") / 3
+    assert got == entry["dram_bytes_per_launch"]
+    assert got > bench.algorithmic_bytes(WORKLOADS["llama8b-mlp"], "adamw", "fp32", "bf16") / 3
     monkeypatch.setattr(bench, "_kernel_source_hash", lambda: "0" * 16)
     assert bench._ncu_traffic("llama8b-mlp", "adamw", "fp32") is None
     assert bench._ncu_traffic("no-such-workload", "adamw", "fp32") is None
