@@ -449,9 +449,9 @@ class OracleSample:
         return flops, secs
 
     def rows_for(self, seconds: float) -> int:
-        """Sample size (a multiple of 128 rows, 128 .. 4096) whose step takes about `seconds`."""
-        f, s = self.run(128)
-        return int(min(4096, max(128, 128 * int(seconds / max(s, 1e-6)))))
+        """Sample size (a multiple of 64 rows, 64 .. 4096) whose step takes about `seconds`."""
+        f, s = self.run(64)
+        return int(min(4096, max(64, 64 * int(seconds / max(s, 1e-6)))))
 
 
 def cpu_baseline(args):
