@@ -78,6 +78,25 @@ bool uses_v(forge_opt_kind k) {
     return k == FORGE_ADAMW || k == FORGE_NADAM || k == FORGE_RADAM || k == FORGE_RMSPROP || k == FORGE_ADAGRAD;
 }
 
+// NAdam's product of mu_1 .. mu_t, multiplied in order from i = 1.  Training calls this with the
+// same (beta1, psi) and a step that grows by one, so each thread keeps its last product and
+// extends it (the same sequence of multiplications, so the same bits); a step that goes
+// backwards, or other hyperparameters, start again from 1.
+double nadam_mu_product(double b1, double psi, int64_t step) {
+    thread_local double c_b1 = -1.0, c_psi = -1.0, c_prod = 1.0;
+    thread_local int64_t c_step = 0;
+    if (b1 != c_b1 || psi != c_psi || step < c_step) {
+        c_b1 = b1;
+        c_psi = psi;
+        c_step = 0;
+        c_prod = 1.0;
+    }
+    for (int64_t i = c_step + 1; i <= step; ++i)
+        c_prod *= b1 * (1.0 - 0.5 * std::pow(0.96, static_cast<double>(i) * psi));
+    c_step = step;
+    return c_prod;
+}
+
 // Step-dependent factors in binary64, rounded once to binary32 (optimizer definitions as cited
 // in opt_math.cuh).
 OptScalars derive_scalars(forge_opt_kind k, const forge_hparams& hp, int64_t step) {
@@ -102,8 +121,7 @@ OptScalars derive_scalars(forge_opt_kind k, const forge_hparams& hp, int64_t ste
         case FORGE_NADAM: {
             const double psi = hp.momentum_decay;
             auto mu = [&](double i) { return b1 * (1.0 - 0.5 * std::pow(0.96, i * psi)); };
-            double prod = 1.0;
-            for (int64_t i = 1; i <= step; ++i) prod *= mu(static_cast<double>(i));
+            const double prod = nadam_mu_product(b1, psi, step);
             const double mu_t = mu(t), mu_next = mu(t + 1.0);
             s.c_g = static_cast<float>(lr * (1.0 - mu_t) / (1.0 - prod));
             s.c_m = static_cast<float>(lr * mu_next / (1.0 - prod * mu_next));
@@ -192,6 +210,33 @@ forge_status check_opt_args(const void* W, const void* m, const void* v, const f
 
 forge_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA; }
 
+// L2 residency of the operands.  The tile order keeps up to kL2ResidentBytes of the smaller operand's
+// slices in L2 while the larger operand's slices stream past once per group; the resident
+// operand's loads carry an L2 evict-last hint, the streaming one's evict-normal (FORGE_STREAM_KEEP
+// = 1: evict-last for both).  The weight and moment traffic of the epilogue, which passes through
+// L2 once, shares the rest.
+#ifndef FORGE_L2_RESIDENT_MB
+#define FORGE_L2_RESIDENT_MB 48
+#endif
+#ifndef FORGE_STREAM_KEEP
+#define FORGE_STREAM_KEEP 1
+#endif
+constexpr int64_t kL2ResidentBytes = int64_t{FORGE_L2_RESIDENT_MB} << 20;
+
+void set_order(forge::TileArgs& a, int tiles_m, int tiles_n, int64_t a_block, int64_t b_block) {
+    a.order = forge::schedule_for(tiles_m, tiles_n, a_block, b_block, kL2ResidentBytes);
+    const bool a_resident = a.order.raster_cols == 0;
+    a.l2_keep_a = a_resident || FORGE_STREAM_KEEP;
+    a.l2_keep_b = !a_resident || FORGE_STREAM_KEEP;
+}
+
+// The epilogue's wait for a finished accumulator spans a whole tile mainloop: the base limit plus
+// 4 us per reduction slice (a slice takes well under 1 us on a GB300), saturating.
+uint64_t acc_wait_limit(uint64_t base_ns, int64_t k_blocks) {
+    const uint64_t per = 4000ull, extra = static_cast<uint64_t>(k_blocks) * per;
+    return extra > ~0ull - base_ns ? ~0ull : base_ns + extra;
+}
+
 // Dispatch tables (filled by template instantiation in the inst_*.cu units).
 using TileFn = cudaError_t (*)(const forge::TileLaunch&);
 using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
@@ -221,61 +266,49 @@ TileFn tile_fn_v(forge_opt_kind k, int state) {
 }
 
 // Tile shape per call.  The mainloop is bound by operand traffic from L2 into shared memory, so a
-// wide shape is used: a CTA pair on 256 x 256 (each CTA stages half of X), one CTA on 128 x 256,
-// one CTA on 128 x 128; each is a group of the method's 128 x 128 tiles side by side.  Two pairs
-// sharing dY slices by multicast (256 x 512) cut operand traffic further but fit only 144 of the
-// 152 SMs as 4-CTA clusters; measured, they pay off only for long token runs (T >= 8192).
+// wide shape is preferred: a CTA pair on 256 x 256 (each CTA stages half of X), one CTA on
+// 128 x 256, one CTA on 128 x 128; each is a group of the method's 128 x 128 tiles side by side.
+// A layer whose preferred shape would run on at most half the SMs takes 128 x 128 tiles instead:
+// there the number of SMs sharing the epilogue matters more than the mainloop's efficiency
+// (measured on 1024^2 and 1536^2 layers at T = 4096: 21-25 % faster).
 struct TileShape {
     int bn;     // columns per CTA pair (or per CTA)
-    int cg;     // CTAs per MMA
-    int cl;     // CTAs per cluster
-    int pairs;  // MMA groups per cluster
+    int cg;     // CTAs per MMA = CTAs per cluster
 };
-// A ragged dimension (not a multiple of the tile) takes the wide shape once it is large enough that
-// the zero-filled tail costs little (over 1024).
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t T) {
-    const bool rows256 = d_out % 256 == 0 || (d_out % 128 != 0 && d_out > 1024);
-    const bool cols256 = d_in % 256 == 0 || (d_in % 128 != 0 && d_in > 1024);
-    if (d_out % 256 == 0 && d_in % 512 == 0 && T >= 8192) return {256, 2, 4, 2};
-    if (rows256 && cols256) {
-        // fewer than 4 pair tiles would leave all but a few SMs idle: 128 x 128 tiles give such a
-        // layer four times as many CTAs, each with a quarter of the epilogue
-        if (ceil_div(d_out, 256) * ceil_div(d_in, 256) < 4) return {128, 1, 1, 1};
-        return {256, 2, 2, 1};
-    }
-    if (cols256) return {256, 1, 1, 1};
-    return {128, 1, 1, 1};
+// rows x cols of the output (dW: d_out x d_in; dX: T x d_in).  A ragged dimension (not a multiple
+// of the tile) takes the wide shape once it is large enough that the zero-filled tail costs little
+// (over 1024).
+TileShape pick_tiles(int64_t rows, int64_t cols, int num_sms) {
+    const bool rows256 = rows % 256 == 0 || (rows % 128 != 0 && rows > 1024);
+    const bool cols256 = cols % 256 == 0 || (cols % 128 != 0 && cols > 1024);
+    TileShape t{128, 1};
+    if (rows256 && cols256) t = {256, 2};
+    else if (cols256) t = {256, 1};
+    const int64_t ctas = ceil_div(rows, 128 * t.cg) * ceil_div(cols, t.bn) * t.cg;
+    if (2 * ctas <= num_sms) return {128, 1};
+    return t;
 }
 
-// Input gradient dX = dY W: tile rows are tokens (M = T), columns d_in (N), reduction over d_out
-// (K).  A CTA pair needs 256 token rows per tile to be worth it; two pairs sharing dY slices pay
-// off only for a long reduction, as for the weight gradient.
-TileShape pick_dx_shape(int64_t T, int64_t d_out, int64_t d_in) {
-    const bool cols256 = d_in % 256 == 0 || (d_in % 128 != 0 && d_in > 1024);
-    if (T >= 256 && d_in % 512 == 0 && d_out >= 8192) return {256, 2, 4, 2};
-    if (T >= 256 && cols256) return {256, 2, 2, 1};
-    if (cols256) return {256, 1, 1, 1};
-    return {128, 1, 1, 1};
-}
+TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t /*T*/, int num_sms) { return pick_tiles(d_out, d_in, num_sms); }
+
+// Input gradient dX = dY W: tile rows are tokens (M = T), columns d_in (N), reduction over d_out (K).
+TileShape pick_dx_shape(int64_t T, int64_t /*d_out*/, int64_t d_in, int num_sms) { return pick_tiles(T, d_in, num_sms); }
 
 template <int OPS>
 TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t) {
     using namespace forge;
     if (epi == kEpiDX) {
         if constexpr (OPS != kOpsBF16) return nullptr;
-        if (t.cl == 4) return launch_tile<0, kEpiDX, 256, 4, kOpsBF16>;
-        if (t.cl == 2) return launch_tile<0, kEpiDX, 256, 2, kOpsBF16>;
+        if (t.cg == 2) return launch_tile<0, kEpiDX, 256, 2, kOpsBF16>;
         return t.bn == 256 ? launch_tile<0, kEpiDX, 256, 1, kOpsBF16> : launch_tile<0, kEpiDX, 128, 1, kOpsBF16>;
     }
     if (epi == kEpiStoreGrad) {
-        if (t.cl == 4) return launch_tile<0, kEpiStoreGrad, 256, 4, OPS>;
-        if (t.cl == 2) return launch_tile<0, kEpiStoreGrad, 256, 2, OPS>;
+        if (t.cg == 2) return launch_tile<0, kEpiStoreGrad, 256, 2, OPS>;
         return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1, OPS> : launch_tile<0, kEpiStoreGrad, 128, 1, OPS>;
     }
-    if (t.cl == 4) return tile_fn_v<256, 4, OPS>(k, state);
-    if (t.cl == 2) return tile_fn_v<256, 2, OPS>(k, state);
+    if (t.cg == 2) return tile_fn_v<256, 2, OPS>(k, state);
     return t.bn == 256 ? tile_fn_v<256, 1, OPS>(k, state) : tile_fn_v<128, 1, OPS>(k, state);
 }
 
@@ -343,16 +376,17 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.d_out = static_cast<int>(shape->d_out);
     a.d_in = static_cast<int>(shape->d_in);
     a.T = static_cast<int>(shape->T);
-    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T);
-    a.tiles_m = static_cast<int>(ceil_div(a.d_out, forge::kBM * ts.cg));
-    a.tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn * ts.pairs));
-    a.num_tiles = a.tiles_m * a.tiles_n;
+    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T, dev.num_sms);
+    const int tiles_m = static_cast<int>(ceil_div(a.d_out, forge::kBM * ts.cg));
+    const int tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn));
+    a.num_tiles = tiles_m * tiles_n;
     a.k_blocks = static_cast<int>(ceil_div(a.T, e4m3 ? 128 : forge::kBK));
+    // a tile row reads 128 * cg rows of dY over all tokens, a tile column bn columns of X
+    const int64_t esize = e4m3 ? 1 : 2;
+    set_order(a, tiles_m, tiles_n, int64_t{forge::kBM} * ts.cg * shape->T * esize, int64_t{ts.bn} * shape->T * esize);
     a.g_scale = g_scale;
     a.row_scales = row_scales;
     a.col_scales = col_scales;
-    // Group 8 row tiles: concurrent CTAs then share ~8 dY slices and ~19 X slices in L2.
-    a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
     a.dW = dW;
     a.W = static_cast<uint16_t*>(W);
     a.m = m;
@@ -364,6 +398,7 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.step = static_cast<uint64_t>(step);
     a.status = dev.status;
     a.wait_limit_ns = g_wait_limit_ns.load();
+    a.acc_wait_limit_ns = acc_wait_limit(a.wait_limit_ns, a.k_blocks);
     a.withhold_first_stage = g_withhold_next.exchange(0);
 
     forge::TileLaunch l;
@@ -389,16 +424,18 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
     a.d_out = static_cast<int>(shape->d_out);
     a.d_in = static_cast<int>(shape->d_in);
     a.T = static_cast<int>(shape->T);
-    const TileShape ts = pick_dx_shape(shape->T, shape->d_out, shape->d_in);
+    const TileShape ts = pick_dx_shape(shape->T, shape->d_out, shape->d_in, dev.num_sms);
     const int rows = forge::kBM * ts.cg;
-    a.tiles_m = static_cast<int>(ceil_div(a.T, rows));
-    a.tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn * ts.pairs));
-    a.num_tiles = a.tiles_m * a.tiles_n;
-    a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
+    const int tiles_m = static_cast<int>(ceil_div(a.T, rows));
+    const int tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn));
+    a.num_tiles = tiles_m * tiles_n;
     a.k_blocks = static_cast<int>(ceil_div(a.d_out, forge::kBK));
+    // a tile row reads `rows` token rows of dY over all of d_out, a tile column bn columns of W
+    set_order(a, tiles_m, tiles_n, int64_t{rows} * shape->d_out * 2, int64_t{ts.bn} * shape->d_out * 2);
     a.dX = static_cast<uint16_t*>(dX);
     a.status = dev.status;
     a.wait_limit_ns = g_wait_limit_ns.load();
+    a.acc_wait_limit_ns = acc_wait_limit(a.wait_limit_ns, a.k_blocks);
     a.withhold_first_stage = g_withhold_next.exchange(0);
 
     forge::TileLaunch l;
@@ -646,18 +683,18 @@ forge_status forge_launch_shape(const forge_shape* shape, int32_t* tile_rows, in
     if (st != FORGE_OK) return st;
     if (tile_rows == nullptr || tile_cols == nullptr || cluster == nullptr || ctas == nullptr)
         return FORGE_ERR_INVALID_ARGUMENT;
-    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T);
-    *tile_rows = forge::kBM * ts.cg;
-    *tile_cols = ts.bn * ts.pairs;
-    *cluster = ts.cl;
-    *ctas = 0;
-    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
+    *tile_rows = *tile_cols = *cluster = *ctas = 0;
     DeviceInfo* dev = nullptr;
     st = device_info(&dev);
     if (st != FORGE_OK) return st;
+    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T, dev->num_sms);
+    *tile_rows = forge::kBM * ts.cg;
+    *tile_cols = ts.bn;
+    *cluster = ts.cg;
+    if (shape->d_out == 0 || shape->d_in == 0) return FORGE_OK;
     const int64_t tiles = ceil_div(shape->d_out, *tile_rows) * ceil_div(shape->d_in, *tile_cols);
     int n = 0;
-    if (forge::tile_ctas(ts.bn, ts.cl, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
+    if (forge::tile_ctas(ts.bn, ts.cg, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
     *ctas = n;
     return FORGE_OK;
 }
@@ -668,18 +705,18 @@ forge_status forge_dx_launch_shape(const forge_shape* shape, int32_t* tile_rows,
     if (st != FORGE_OK) return st;
     if (tile_rows == nullptr || tile_cols == nullptr || cluster == nullptr || ctas == nullptr)
         return FORGE_ERR_INVALID_ARGUMENT;
-    const TileShape ts = pick_dx_shape(shape->T, shape->d_out, shape->d_in);
-    *tile_rows = forge::kBM * ts.cg;
-    *tile_cols = ts.bn * ts.pairs;
-    *cluster = ts.cl;
-    *ctas = 0;
-    if (shape->T == 0 || shape->d_in == 0 || shape->d_out == 0) return FORGE_OK;
+    *tile_rows = *tile_cols = *cluster = *ctas = 0;
     DeviceInfo* dev = nullptr;
     st = device_info(&dev);
     if (st != FORGE_OK) return st;
+    const TileShape ts = pick_dx_shape(shape->T, shape->d_out, shape->d_in, dev->num_sms);
+    *tile_rows = forge::kBM * ts.cg;
+    *tile_cols = ts.bn;
+    *cluster = ts.cg;
+    if (shape->T == 0 || shape->d_in == 0 || shape->d_out == 0) return FORGE_OK;
     const int64_t tiles = ceil_div(shape->T, *tile_rows) * ceil_div(shape->d_in, *tile_cols);
     int n = 0;
-    if (forge::tile_ctas(ts.bn, ts.cl, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
+    if (forge::tile_ctas(ts.bn, ts.cg, static_cast<int>(tiles), dev->num_sms, &n) != cudaSuccess) return FORGE_ERR_CUDA;
     *ctas = n;
     return FORGE_OK;
 }

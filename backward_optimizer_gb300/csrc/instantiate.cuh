@@ -90,8 +90,7 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 #define FORGE_INSTANTIATE_TILES_OPS(OPT, EPI, OPS)                                               \
     template cudaError_t forge::launch_tile<OPT, EPI, 128, 1, OPS>(const forge::TileLaunch&);       \
     template cudaError_t forge::launch_tile<OPT, EPI, 256, 1, OPS>(const forge::TileLaunch&);       \
-    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2, OPS>(const forge::TileLaunch&);       \
-    template cudaError_t forge::launch_tile<OPT, EPI, 256, 4, OPS>(const forge::TileLaunch&);
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2, OPS>(const forge::TileLaunch&);
 
 #define FORGE_INSTANTIATE_TILES(OPT, EPI) FORGE_INSTANTIATE_TILES_OPS(OPT, EPI, forge::kOpsBF16)
 

@@ -16,7 +16,7 @@ struct TileLaunch {
     CUtensorMap tmap_dy;
     CUtensorMap tmap_x;
     const TileArgs* args;
-    int num_tiles;  // tiles of the launch's shape (per CTA, CTA pair or cluster of two pairs)
+    int num_tiles;  // tiles of the launch's shape (per CTA or CTA pair)
     int num_sms;
     cudaStream_t stream;
 };
@@ -25,8 +25,7 @@ struct TileLaunch {
 // 3 = input gradient dX = dY W stored as bf16 (tile rows are tokens, columns d_in), 4 = fused optimizer
 // with bfloat16 states.
 // BN: tile columns (128, or 256 = two 128 x 128 tiles side by side).
-// CL: CTAs per cluster (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair; 4: two pairs
-// on a 256 x 2BN tile sharing their dY slices by multicast).
+// CL: CTAs per cluster (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair).
 // OPS: operand format of dY and X, 0 = bf16, 1 = E4M3 (the gradient tile is scaled by s_dY * s_X).
 template <int OPT, int EPI, int BN, int CL, int OPS> cudaError_t launch_tile(const TileLaunch& l);
 

@@ -50,6 +50,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Settles `bytes` of the barrier's current phase without a copy (the transaction count drops as if
+// they had landed).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// try_wait with acquire at cluster scope: what the arriving CTA of the pair wrote before its
+// (release, cluster) arrive is visible once this returns true.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t ld_shared_volatile_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- clusters (CTA pairs)
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -69,6 +95,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_cta_addr, uint32_t
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_cta_addr), "r"(rank));
     return r;
+}
+
+// Store to another CTA's shared memory, given by its shared::cluster address.
+__device__ __forceinline__ void st_shared_cluster_u64(uint32_t cluster_addr, uint64_t v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v) : "memory");
 }
 
 // Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
@@ -103,20 +134,15 @@ __device__ __forceinline__ void tma_load_2d_cg(void* dst, const CUtensorMap* map
     }
 }
 
-// Multicast form (CTA pairs only): the box lands at the same offset in every CTA of `mask`, and
-// each destination's bytes are counted on the barrier of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
-                                                      int32_t c1, uint16_t mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask), "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

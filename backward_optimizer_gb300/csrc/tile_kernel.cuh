@@ -17,8 +17,9 @@
 //               registers (thread = weight row); the optimizer runs in registers (step 2); the
 //               gradient registers are then dropped (step 3); W/m/v are read and written with
 //               256-bit accesses (step 4).  The gradient never reaches device memory.
-// Tiles are visited by a static persistent schedule (tile = blockIdx.x + k * gridDim.x) in
-// grouped order so that concurrently running CTAs share dY and X slices in L2.
+// Tiles are visited by a static persistent schedule (tile = blockIdx.x + k * gridDim.x) in the
+// grouped order of schedule.h, which keeps the smaller operand's slices resident in L2 while the
+// larger one streams past.
 //
 // The same pipeline also computes the layer's input gradient dX = dY W (EPI = kEpiDX), which the
 // fused step's ordering requires before W is overwritten: there the tile rows are tokens, the
@@ -34,6 +35,7 @@
 
 #include "opt_math.cuh"
 #include "ptx.cuh"
+#include "schedule.h"
 
 namespace forge {
 
@@ -91,7 +93,9 @@ struct TileCfg {
 
 struct TileArgs {
     int d_out, d_in, T;
-    int tiles_m, tiles_n, num_tiles, group_m;
+    TileOrder order;              // tile rows x columns and the order they are visited in
+    int num_tiles;
+    int l2_keep_a, l2_keep_b;     // per operand: L2 evict-last (1) or evict-normal (0) on its loads
     int k_blocks;                 // reduction slices per tile: T / 64 (dW; T / 128 for E4M3), d_out / 64 (dX)
     float g_scale;                // E4M3 operands: s_dY * s_X, applied to the FP32 gradient tile
     const float* row_scales;      // or per channel (both set): s_dY [d_out] and s_X [d_in], each
@@ -106,8 +110,9 @@ struct TileArgs {
     OptScalars s;
     uint64_t seed, step;
     int* status;                  // device status word
-    uint64_t wait_limit_ns;
-    int withhold_first_stage;     // test switch: the producer skips the first stage, so a wait runs out
+    uint64_t wait_limit_ns;       // every wait but the epilogue's for a finished accumulator
+    uint64_t acc_wait_limit_ns;   // that one: it spans a whole tile mainloop (wait_limit_ns + k_blocks * 4 us)
+    int withhold_first_stage;     // test switch: the producer arms its first stage but never fills it, so a wait runs out
 };
 
 // ---------------------------------------------------------------- bounded waits
@@ -138,16 +143,6 @@ __device__ __forceinline__ void drain_bounded(uint64_t* bar, uint32_t parity, ui
     while (!mbar_try_wait(bar, parity)) {
         if (global_timer_ns() - t0 > limit_ns) return;
     }
-}
-
-__device__ __forceinline__ void tile_coords(int tile, const TileArgs& a, int& mb, int& nb) {
-    const int per_group = a.group_m * a.tiles_n;
-    const int group = tile / per_group;
-    const int first_m = group * a.group_m;
-    const int gm = min(a.tiles_m - first_m, a.group_m);
-    const int in_group = tile - group * per_group;
-    mb = first_m + in_group % gm;
-    nb = in_group / gm;
 }
 
 // ---------------------------------------------------------------- epilogues
@@ -581,23 +576,44 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
 //         dY^T and its own BN/2 columns of X; the pair's even CTA issues tcgen05.mma.cta_group::2
 //         (M = 256), which reads both CTAs' shared memory and writes each CTA's 128 accumulator
 //         rows into that CTA's TMEM.  Both CTAs' TMA copies complete on the even CTA's stage
-//         barrier; the MMA commits are multicast to both CTAs; both epilogues release a TMEM
-//         buffer on the even CTA's barrier.  Per SM this halves the X bytes pulled from L2.
-// CL = 4: two pairs side by side on a 256 x 2BN cluster tile share their dY^T slices: each pair
-//         loads one of the two 64-row boxes of every slice with a TMA multicast into both pairs,
-//         halving the dY bytes pulled from L2.  A stage slot is free again only when both pairs'
-//         MMAs have consumed it, so each pair's commit of a stage arrives in all four CTAs.
+//         barrier; the MMA commits arrive in both CTAs; both epilogues release a TMEM buffer on
+//         the even CTA's barrier.  Per SM this halves the X bytes pulled from L2.  Every TMA load
+//         reads this GPU's own memory into one CTA's shared memory (no multicast).
+
+// After an abort, before the CTA (or the pair) tears down: waits, bounded, until every TMA copy
+// this CTA (and, in a pair, the odd CTA) has issued into shared memory has landed.  Copies of
+// both CTAs of a pair complete on the even CTA's stage barriers, so its producer does this for
+// both, from the issue counts of the two producers (`n_own`, `n_peer`: stages passed in issue
+// order; stage i uses slot i mod S in phase (i div S) mod 2).  A producer passes stage i only once
+// the MMA consumed stage i - S, so the two counts differ by at most S and each slot is short of
+// at most one side's copies in its last phase; that side's bytes are settled on the barrier
+// (armed for copies that were issued but never armed, or retired for copies that were armed but
+// never issued) and the phase then completes exactly when the copies that were issued have landed.
+template <int S, int CG>
+__device__ __forceinline__ void drain_copies(uint64_t* full, uint64_t n_own, uint64_t n_peer, int64_t withheld,
+                                             uint32_t stage_bytes, uint64_t limit_ns) {
+    for (int s = 0; s < S; ++s) {
+        const int64_t lo = n_own > static_cast<uint64_t>(s) ? s + S * static_cast<int64_t>((n_own - 1 - s) / S) : -1;
+        const int64_t lp =
+            CG == 1 ? lo : (n_peer > static_cast<uint64_t>(s) ? s + S * static_cast<int64_t>((n_peer - 1 - s) / S) : -1);
+        const int64_t last = lo > lp ? lo : lp;
+        if (last < 0) continue;
+        if (CG == 2 && lo < last) mbar_arrive_expect_tx(&full[s], stage_bytes);  // the odd CTA's copies, unarmed
+        if (CG == 2 && lp < last) mbar_complete_tx(&full[s], stage_bytes);       // armed for copies never issued
+        if (last == withheld) mbar_complete_tx(&full[s], stage_bytes);           // the test switch's skipped copies
+        drain_bounded(&full[s], static_cast<uint32_t>((last / S) & 1), limit_ns);
+    }
+}
 
 template <int BN, int CL, int EPI, int OPT, int OPS>
-__global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThreads, 1)
+__global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
     forge_tile_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
                       const TileArgs a) {
-    static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
+    static_assert(CL == 1 || CL == 2, "cluster size");
     static_assert(OPS == kOpsBF16 || EPI != kEpiDX, "the input gradient takes bf16 operands");
     using O = OperandTraits<OPS>;
     constexpr bool kScale = OPS == kOpsE4M3;
-    constexpr int CG = CL == 1 ? 1 : 2;       // CTAs per MMA (cta_group)
-    constexpr int kPairs = CL == 4 ? 2 : 1;   // MMA groups per cluster sharing dY
+    constexpr int CG = CL;                    // CTAs per MMA (cta_group)
     using C = TileCfg<BN, CG, EPI, OPS>;
     constexpr bool kAKMajor = EPI == kEpiDX;  // A = dY with d_out (= K) along memory
     extern __shared__ uint8_t smem_raw[];
@@ -611,28 +627,28 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThr
     uint64_t* acc_full = empty + C::kStages;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* drain = acc_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* peer_done = drain + 1;     // a pair's odd CTA: its producer has stopped issuing
+    uint64_t* peer_count = peer_done + 1;  // ... after this many stages
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer_count + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
-    const uint32_t rank = crank & 1u;      // CTA within its pair; 0 issues the pair's MMAs
-    const uint32_t pair = crank >> 1;      // pair within the cluster
-    const uint32_t leader = crank & ~1u;   // cluster rank of this pair's MMA-issuing CTA
+    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;  // CTA within its pair; 0 issues the pair's MMAs
     const int first_tile = static_cast<int>(blockIdx.x) / CL;
     const int tile_stride = static_cast<int>(gridDim.x) / CL;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kPairs);  // one commit per pair that reads this slot
+            mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], C::kEpiWarps * CG);
         }
         mbar_init(drain, 1);
+        mbar_init(peer_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmap_dy);
@@ -644,91 +660,77 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThr
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (CL > 1) cluster_sync();  // other CTAs' barriers exist before anything signals them
+    if constexpr (CL > 1) cluster_sync();  // the peer's barriers exist before anything signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const AbortCtx ab{abort_flag, a.status, a.wait_limit_ns};
     const int kblocks = a.k_blocks;
+    uint64_t n_issued = 0;   // producer: stages passed (armed and copied, but for the withheld one)
+    int64_t withheld = -1;   // producer: the stage the test switch left without this CTA's copies
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (every CTA)
             int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_phase = 0;
+            uint32_t phase = 0;
             bool ok = true;
-            const uint64_t keep = policy_evict_last();
+            const uint64_t keep_a = a.l2_keep_a ? policy_evict_last() : policy_evict_normal();
+            const uint64_t keep_b = a.l2_keep_b ? policy_evict_last() : policy_evict_normal();
             for (int tile = first_tile; ok && tile < a.num_tiles; tile += tile_stride) {
                 int mb, nb;
-                tile_coords(tile, a, mb, nb);
+                tile_coords(tile, a.order, mb, nb);
                 const int row_a = mb * kBM * CG + static_cast<int>(rank) * kBM;
-                const int col_b = (nb * kPairs + static_cast<int>(pair)) * BN + static_cast<int>(rank) * C::kBLoad;
+                const int col_b = nb * BN + static_cast<int>(rank) * C::kBLoad;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, ab)) { ok = false; break; }
-                    if (a.withhold_first_stage && rank == 0 && tile == first_tile && kb == 0) {
-                        // test switch: never fill this stage, so the MMA thread's wait for it runs out
-                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-                        continue;
-                    }
                     uint32_t bar = smem_addr(&full[stage]);
-                    if constexpr (CG == 2) bar = map_to_rank(bar, leader);
+                    if constexpr (CG == 2) bar = map_to_rank(bar, 0);
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], CG * C::kStageBytes);
-                    uint8_t* a_dst = sA + stage * C::kABytes;
-                    uint8_t* b_dst = sB + stage * C::kBBytes;
-                    const int k0 = kb * O::kTok;
-                    // A box j holds rows row_a + 64j .. +63 of this CTA's 128 A rows; dY's tensor map
-                    // has d_out innermost, so its coordinates are (row, token) for dY^T and
-                    // (d_out slice, token row) for the K-major dY of dX
-                    if constexpr (OPS == kOpsE4M3) {
-                        // E4M3: 128 rows of dY^T fill one 128-byte row; box j is token half j of the
-                        // stage (64 token rows at j * 8 KiB)
-                        if constexpr (kPairs == 2) {
-                            tma_load_2d_multicast(a_dst + pair * 8192, &tmap_dy, bar, row_a, k0 + 64 * static_cast<int>(pair),
-                                                  static_cast<uint16_t>(0x5u << rank), keep);
-                        } else {
+                    if (a.withhold_first_stage && rank == 0 && tile == first_tile && kb == 0) {
+                        // test switch: arm this stage but never copy into it, so the MMA thread's wait
+                        // for it runs out
+                        withheld = static_cast<int64_t>(n_issued);
+                    } else {
+                        uint8_t* a_dst = sA + stage * C::kABytes;
+                        uint8_t* b_dst = sB + stage * C::kBBytes;
+                        const int k0 = kb * O::kTok;
+                        // A box j holds rows row_a + 64j .. +63 of this CTA's 128 A rows; dY's tensor
+                        // map has d_out innermost, so its coordinates are (row, token) for dY^T and
+                        // (d_out slice, token row) for the K-major dY of dX
+                        if constexpr (OPS == kOpsE4M3) {
+                            // E4M3: 128 rows of dY^T fill one 128-byte row; box j is token half j of
+                            // the stage (64 token rows at j * 8 KiB)
 #pragma unroll
                             for (int j = 0; j < 2; ++j)
-                                tma_load_2d_cg<CG>(a_dst + j * 8192, &tmap_dy, bar, row_a, k0 + 64 * j, keep);
-                        }
+                                tma_load_2d_cg<CG>(a_dst + j * 8192, &tmap_dy, bar, row_a, k0 + 64 * j, keep_a);
 #pragma unroll
-                        for (int j = 0; j < C::kBLoad / 128; ++j)
+                            for (int j = 0; j < C::kBLoad / 128; ++j)
 #pragma unroll
-                            for (int h = 0; h < 2; ++h)
-                                tma_load_2d_cg<CG>(b_dst + j * O::kBlockBytes + h * 8192, &tmap_x, bar, col_b + 128 * j,
-                                                   k0 + 64 * h, keep);
-                    } else {
-                        if constexpr (kPairs == 2) {
-                            // box `pair`, for this CTA and its counterpart in the other pair (cluster
-                            // ranks rank and rank + 2)
-                            const int r = row_a + 64 * static_cast<int>(pair);
-                            tma_load_2d_multicast(a_dst + pair * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
-                                                  kAKMajor ? r : k0, static_cast<uint16_t>(0x5u << rank), keep);
+                                for (int h = 0; h < 2; ++h)
+                                    tma_load_2d_cg<CG>(b_dst + j * O::kBlockBytes + h * 8192, &tmap_x, bar,
+                                                       col_b + 128 * j, k0 + 64 * h, keep_b);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
                                 const int r = row_a + 64 * j;
                                 tma_load_2d_cg<CG>(a_dst + j * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
-                                                   kAKMajor ? r : k0, keep);
+                                                   kAKMajor ? r : k0, keep_a);
                             }
-                        }
 #pragma unroll
-                        for (int j = 0; j < C::kBLoad / 64; ++j)
-                            tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep);
+                            for (int j = 0; j < C::kBLoad / 64; ++j)
+                                tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep_b);
+                        }
                     }
-                    issued |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    ++n_issued;
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
-            if (!ok) {
-                if (rank == 0) {
-                    for (int s = 0; s < C::kStages; ++s)
-                        if ((issued >> s) & 1u) drain_bounded(&full[s], (issued_phase >> s) & 1u, a.wait_limit_ns);
-                } else {
-                    // this CTA's copies complete on the peer's barrier, which it cannot wait on:
-                    // give copies in flight a grace period to land before teardown
-                    const uint64_t t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < 200000ull) {
-                    }
+            if constexpr (CG == 2) {
+                if (rank == 1) {
+                    // tell the even CTA how far this producer got: it settles the accounts of the
+                    // stage barriers if the pair aborts
+                    st_shared_cluster_u64(map_to_rank(smem_addr(peer_count), 0), n_issued);
+                    mbar_arrive_remote(map_to_rank(smem_addr(peer_done), 0));
                 }
             }
         }
@@ -764,12 +766,12 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThr
                         else tc_mma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
-                    // the slot is free once read: tell every CTA whose copies fill it
-                    tc_commit_mask<CG>(&empty[stage], kPairs == 2 ? 0xFu : 0x3u);
+                    // the slot is free once read: tell both CTAs of the pair, whose copies fill it
+                    tc_commit_mask<CG>(&empty[stage], 0x3u);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit_mask<CG>(&acc_full[acc], static_cast<uint16_t>(0x3u << leader));
+                tc_commit_mask<CG>(&acc_full[acc], 0x3u);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
@@ -784,18 +786,20 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThr
         const int quarter = warp & 3;   // a warp may only touch TMEM lanes 32*(warp%4) .. +31
         const int half = e >> 2;                // column part owned by this warp
         constexpr int kWidth = BN / (C::kEpiWarps / 4);
+        // the wait for a finished accumulator spans a whole tile mainloop, which grows with T
+        const AbortCtx ab_acc{abort_flag, a.status, a.acc_wait_limit_ns};
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = first_tile; tile < a.num_tiles; tile += tile_stride) {
             int mb, nb;
-            tile_coords(tile, a, mb, nb);
+            tile_coords(tile, a.order, mb, nb);
             int ok = 1;
-            if (lane == 0) ok = wait_bounded(&acc_full[acc], acc_phase, ab) ? 1 : 0;
+            if (lane == 0) ok = wait_bounded(&acc_full[acc], acc_phase, ab_acc) ? 1 : 0;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             tc_fence_after();
             const int row0 = mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
-            const int col0 = (nb * kPairs + static_cast<int>(pair)) * BN + half * kWidth;
+            const int col0 = nb * BN + half * kWidth;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + half * kWidth);
             uint8_t* strip = strips + e * C::kStripBytes;
@@ -805,9 +809,9 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThr
                 int row0n = -1, col0n = 0;
                 if (tile + tile_stride < a.num_tiles) {
                     int mbn, nbn;
-                    tile_coords(tile + tile_stride, a, mbn, nbn);
+                    tile_coords(tile + tile_stride, a.order, mbn, nbn);
                     row0n = mbn * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
-                    col0n = (nbn * kPairs + static_cast<int>(pair)) * BN + half * kWidth;
+                    col0n = nbn * BN + half * kWidth;
                 }
                 epi_opt_dense<OPT, kWidth, EPI == kEpiOptBF16, kScale, (C::kEpiWarps == 8 ? 4 : 1)>(
                     a, row0, col0, taddr, strip, row0n, col0n);
@@ -816,7 +820,7 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThr
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if constexpr (CG == 2) mbar_arrive_remote(map_to_rank(smem_addr(&acc_empty[acc]), leader));
+                if constexpr (CG == 2) mbar_arrive_remote(map_to_rank(smem_addr(&acc_empty[acc]), 0));
                 else mbar_arrive(&acc_empty[acc]);
             }
             acc ^= 1;
@@ -826,8 +830,26 @@ __global__ void __launch_bounds__(TileCfg<BN, (CL == 1 ? 1 : 2), EPI, OPS>::kThr
 
     tc_fence_before();
     __syncthreads();
-    // a cluster tears down together: a pair's MMAs read both CTAs' shared memory and write both
-    // TMEMs, multicast copies and commits land in other CTAs
+    if (warp == 0 && lane == 0 && rank == 0 && *abort_flag) {
+        // an aborted CTA (pair) exits only once no copy into its shared memory is still in flight
+        uint64_t n_peer = n_issued;
+        bool counted = true;
+        if constexpr (CG == 2) {
+            counted = false;
+            const uint64_t t0 = global_timer_ns();
+            while (!counted && global_timer_ns() - t0 <= 4 * a.wait_limit_ns) counted = mbar_try_wait_cluster(peer_done, 0);
+            if (counted) n_peer = ld_shared_volatile_u64(peer_count);
+        }
+        if (counted) {
+            drain_copies<C::kStages, CG>(full, n_issued, n_peer, withheld, C::kStageBytes, a.wait_limit_ns);
+        } else {
+            // the odd CTA never reported (it is itself stuck past every limit): wait for the last
+            // phase this CTA armed on each slot, bounded
+            drain_copies<C::kStages, 1>(full, n_issued, n_issued, withheld, C::kStageBytes, a.wait_limit_ns);
+        }
+    }
+    // a pair tears down together: its MMAs read both CTAs' shared memory and write both TMEMs, and
+    // both CTAs' copies and commits land in the even CTA
     if constexpr (CL > 1) cluster_sync();
     if (warp == 1) {
         __syncwarp();

@@ -413,6 +413,72 @@ def run_gpu(args, rank, world):
                 dx_launch_ms=dx_launch_ms)
 
 
+def run_sweep(name, opt, steps, warmup, rank, world):
+    """A many-layer sweep (one step = every layer once): the fused step against the two-phase
+    schedule (every layer's dW to HBM, then every optimizer pass), with the peak HBM the gradients
+    take in each (torch's allocator high-water mark over the step's own allocations)."""
+    import torch
+    import backward_optimizer_gb300 as fg
+    from workloads import WORKLOADS, default_hparams
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = WORKLOADS[name]
+    hp = default_hparams(opt)
+    t_step = wl.steps[-1]
+    act_cache = {}
+    layers = [_make_layer(wl, i, opt, "fp32", dev, 1000 * rank, act_cache) for i in range(len(wl.layers))]
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def fused_pass():
+        for i, L in enumerate(layers):
+            fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], None, opt, hp, t_step, seed=0x5EED + i,
+                             stream=stream)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        fused_ms = timed(fused_pass)
+    fused_pool = torch.cuda.max_memory_allocated() - base
+    if fg.sync_status() != 0:
+        raise RuntimeError("device status after the sweep's fused steps")
+    torch.cuda.reset_peak_memory_stats()
+    dws = [torch.empty(l.d_out, l.d_in, dtype=torch.float32, device=dev) for l in wl.layers]
+
+    def unfused_pass():
+        for L, dW in zip(layers, dws):
+            fg.dw_gemm(L["dy"], L["x"], dW, stream=stream)
+        for i, (L, dW) in enumerate(zip(layers, dws)):
+            fg.opt_step(dW, L["w"], L["m"], L["v"], None, opt, hp, t_step, seed=0x5EED + i, stream=stream)
+
+    unfused_ms = timed(unfused_pass)
+    unfused_pool = torch.cuda.max_memory_allocated() - base
+    if fg.sync_status() != 0:
+        raise RuntimeError("device status after the sweep's two-phase steps")
+    del dws, layers, act_cache
+    torch.cuda.empty_cache()
+    fused_ms, unfused_ms = max_over_ranks([fused_ms, unfused_ms], world, dev)
+    return dict(wl=wl, fused_ms=fused_ms, unfused_ms=unfused_ms, fused_pool=fused_pool, unfused_pool=unfused_pool,
+                clocks=clocks.summary(), steps=steps, warmup=warmup)
+
+
 # ------------------------------------------------------------------------------------ CPU oracle
 
 class OracleSample:
@@ -454,11 +520,41 @@ class OracleSample:
         return int(min(4096, max(64, 64 * int(seconds / max(s, 1e-6)))))
 
 
+def blas_threads():
+    """Threads numpy's BLAS runs the oracle's float64 products on: from threadpoolctl where it is
+    installed, else from the OpenBLAS library numpy loaded (its get_num_threads symbol)."""
+    import numpy as np
+    np.ones((2, 2)) @ np.ones((2, 2))  # make sure the BLAS is loaded
+    try:
+        from threadpoolctl import threadpool_info
+        for info in threadpool_info():
+            if info.get("user_api") == "blas":
+                return {"threads": int(info["num_threads"]), "library": info.get("internal_api", "blas")}
+    except Exception:
+        pass
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({l.split()[-1] for l in f if "openblas" in l.lower() and ".so" in l})
+        for path in paths:
+            lib = ctypes.CDLL(path)
+            for sym in ("openblas_get_num_threads", "openblas_get_num_threads64_", "scipy_openblas_get_num_threads64_",
+                        "scipy_openblas_get_num_threads"):
+                fn = getattr(lib, sym, None)
+                if fn is not None:
+                    fn.restype = ctypes.c_int
+                    return {"threads": int(fn()), "library": os.path.basename(path)}
+    except OSError:
+        pass
+    return {"threads": None, "library": "unknown"}
+
+
 def cpu_baseline(args):
     sample = OracleSample(args.workload, args.opt)
     rows = sample.rows_for(15.0) if args.oracle_rows <= 0 else args.oracle_rows
     flops, secs = sample.run(rows)
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "blas_threads": blas_threads(),
             "sample": f"first {rows} weight rows of each of the first 3 layers of {args.workload} "
                       f"(float64 NumPy oracle, whole step incl. Philox/SR), {secs:.1f} s"}
 
@@ -478,6 +574,9 @@ def main():
                     help="dY/X format: bf16, or E4M3 codes with per-tensor or per-channel scales")
     ap.add_argument("--oracle-rows", type=int, default=0, help="rows per layer of the oracle sample (0: sized by time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", default="qwen14b-sweep",
+                    help="many-layer sweep timed after the main workload, fused against two-phase ('none': skip)")
+    ap.add_argument("--sweep-steps", type=int, default=5)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -512,6 +611,7 @@ def main():
                 "data": "synthetic", "config": dict(config, ms_per_step="extrapolated to the full step at the "
                                                                         "oracle's measured rate"),
                 "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "blas_threads": blas_threads(),
                                  "sample": f"first {rows} weight rows of each of the first 3 layers per step "
                                            f"(float64 NumPy oracle, whole step incl. Philox/SR)"},
                 "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -526,6 +626,9 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     r = run_gpu(args, rank, world)
+    sweep = None
+    if args.sweep != "none" and args.state == "fp32" and args.operands == "bf16":
+        sweep = run_sweep(args.sweep, args.opt, args.sweep_steps, max(3, min(args.warmup, 5)), rank, world)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -581,6 +684,22 @@ def main():
         line["layer_backward"] = {"ms_per_step": r["bwd_ms"],
                                   "value": job_throughput(2 * r["flops_step"], world, r["bwd_ms"]),
                                   "unit": "TFLOP/s", "what": "dX then the fused step, per layer, one stream"}
+    if sweep is not None:
+        sw = sweep["wl"]
+        sus = float(peaks.get("bf16_tflops_sustained", bf16_peak))
+        fused_v = job_throughput(sw.flops_per_step(), world, sweep["fused_ms"])
+        line["sweep"] = {
+            "workload": f"{sw.name}: {sw.description}", "layers": len(sw.layers), "T": sw.T, "opt": args.opt,
+            "steps": sweep["steps"], "warmup": sweep["warmup"],
+            "fused": {"ms_per_step": sweep["fused_ms"], "value": fused_v, "unit": "TFLOP/s",
+                      "frac": fused_v / world / sus,
+                      "peak": sus, "peak_source": f"bf16_tflops_sustained of {peaks_src} (a step of {len(sw.layers)} launches)"},
+            "unfused": {"ms_per_step": sweep["unfused_ms"],
+                        "value": job_throughput(sw.flops_per_step(), world, sweep["unfused_ms"]), "unit": "TFLOP/s"},
+            "speedup_fused": sweep["unfused_ms"] / sweep["fused_ms"],
+            "grad_pool_bytes": {"fused_hbm": sweep["fused_pool"], "unfused_hbm": sweep["unfused_pool"],
+                                "what": "peak HBM allocated during the step beyond W/m/v/dY/X (torch allocator)"},
+            "clocks": sweep["clocks"]}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(line))

@@ -28,10 +28,16 @@
  *    scale s = absmax / 127; code q = clamp(round_half_even(x / s), -127, 127);
  *    value = q * s.  `qscales` then points to 2 * d_out * d_in / 64 binary32
  *    scales: the m scales first ([d_out, d_in/64] row-major), then the v scales.
- *  - All pointers are DEVICE pointers of the current CUDA device, 32-byte
- *    aligned, owned by the caller.  The library allocates no device memory and
- *    keeps no pointer after a call returns.  W, m, v and qscales are updated in
- *    place.
+ *  - All pointers are DEVICE pointers of the current CUDA device, owned by the
+ *    caller.  The library allocates no device memory and keeps no pointer after a
+ *    call returns.  W, m, v and qscales are updated in place.
+ *  - Alignment: every tensor pointer (dY, X, W, m, v, dW, dX) must be 32-byte
+ *    aligned, qscales 4-byte aligned, per-channel scale vectors 16-byte aligned.
+ *    TMA would accept 16-byte aligned dY and X; the stricter rule is the
+ *    epilogue's: it reads and writes W, m, v, dW and dX with 256-bit accesses
+ *    (8 binary32 moments or 16 bfloat16 values per instruction), which need
+ *    32-byte aligned addresses, and a pointer that fails it is rejected with
+ *    FORGE_ERR_MISALIGNED before anything is launched.
  *  - Sizes: d_out and d_in multiples of 8 (a TMA row stride is a multiple of 16
  *    bytes; with INT8 states d_in is a multiple of 64, so that a block of 64
  *    never spans two rows) and any T >= 0.  The method's 128 x 128 tile (§2
@@ -44,7 +50,10 @@
  *    synchronously; nothing is written in that case.
  *  - Every on-device wait in the kernels is bounded in time.  A wait that runs
  *    out sets a device status word and the kernel returns early; the word is
- *    read and cleared by forge_sync_status().
+ *    read and cleared by forge_sync_status().  There is one status word per
+ *    device, shared by every stream: a timeout in a kernel on stream B is
+ *    reported by the next forge_sync_status() of any stream of that device, and
+ *    that call clears it.
  *  - Ordering (§5 Significance and claims, limitations: the input gradient must
  *    be read before the weights are updated): the layer's input gradient
  *    dX = dY W needs the old W, so it must be enqueued before forge_fused_dw_step
@@ -236,26 +245,36 @@ FORGE_API forge_status forge_linear_backward(const void *dY, const void *X, void
                                              uint64_t seed, struct CUstream_st *stream);
 
 /* Waits for `stream`, then reads and clears the device status word of the current
- * device: FORGE_ERR_TIMEOUT if a bounded wait ran out in a kernel since the last
- * call, FORGE_ERR_CUDA if the stream reported an error, FORGE_OK otherwise. */
+ * device: FORGE_ERR_TIMEOUT if a bounded wait ran out in a kernel (on any stream of
+ * this device) since the last read, FORGE_ERR_CUDA if the stream reported an error,
+ * FORGE_OK otherwise.  A timeout on another stream still running may be reported by a
+ * later call. */
 FORGE_API forge_status forge_sync_status(struct CUstream_st *stream);
 
 /* Time limit of every bounded on-device wait, in nanoseconds (default 2e9).
- * Values below 1e6 are raised to 1e6.  Host-side setting, applies to later launches. */
+ * Values below 1e6 are raised to 1e6.  Host-side setting, applies to later launches.
+ * The epilogue's wait for a finished accumulator spans a whole tile mainloop, whose
+ * length grows with the reduction: it gets the limit plus 4 us per 64-token slice
+ * (128 for E4M3 operands; per 64 rows of d_out for forge_dx_gemm), far above the
+ * slice's time on a GB300, so that a long but healthy run never reports a timeout. */
 FORGE_API void forge_set_wait_limit_ns(uint64_t ns);
 
 /* Test switch for the failure-detection path (the method has no counterpart; it exists so that
  * the bounded waits can be exercised without a real fault).  The next tile-kernel launch (of
  * forge_fused_dw_step, forge_fused_dw_step_e4m3, forge_dw_gemm, forge_dw_gemm_e4m3 or
- * forge_dx_gemm, with work to do) withholds the first pipeline stage of its first tile: the MMA thread's wait for that
- * stage runs out after the wait limit, the kernel records FORGE_ERR_TIMEOUT, stops every other
- * wait, frees its TMEM and returns; forge_sync_status() then reports FORGE_ERR_TIMEOUT and the
+ * forge_dx_gemm, with work to do) arms the first pipeline stage of its first tile but never copies
+ * into it: the MMA thread's wait for that stage runs out after the wait limit, the kernel records
+ * FORGE_ERR_TIMEOUT, stops every other wait, waits (bounded) until every copy it did issue into
+ * shared memory has landed, frees its TMEM and returns; forge_sync_status() then reports FORGE_ERR_TIMEOUT and the
  * CUDA context stays usable.  The outputs of that one call are unspecified.  No fault is raised. */
 FORGE_API void forge_debug_withhold_next_stage(void);
 
 /* The tile shape and persistent grid forge_fused_dw_step (and forge_dw_gemm) use for `shape`:
- * rows x columns of W per tile (a group of the method's 128 x 128 tiles, §2 Methodology), CTAs per
- * thread-block cluster, and CTAs launched on the current device.  Host-side query, no launch. */
+ * rows x columns of W per tile (a group of the method's 128 x 128 tiles, §2 Methodology: 256 x 256
+ * on a CTA pair, 128 x 256 or 128 x 128 on one CTA; a layer whose wider shape would occupy at most
+ * half the SMs takes 128 x 128), CTAs per thread-block cluster (1 or 2), and CTAs launched on the
+ * current device.  Host-side query, no launch; it reads the device's SM count, so it needs a
+ * device (FORGE_ERR_CUDA or FORGE_ERR_NOT_SM103 otherwise). */
 FORGE_API forge_status forge_launch_shape(const forge_shape *shape, int32_t *tile_rows, int32_t *tile_cols,
                                           int32_t *cluster, int32_t *ctas);
 
