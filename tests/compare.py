@@ -15,12 +15,14 @@
   bound is unreachable where dY^T X nearly cancels, because the summation order
   over tokens differs (the summary's exactness statement allows exactly that
   difference); the rms floor bounds the error by the tensor's own scale.
-  rtol = max(1e-5, (T/16) 2^-23): the tensor core adds each 16-token partial
-  product into its FP32 accumulator with an error of up to one binary32 ULP of the
-  running sum (measured: consistently toward zero), so T/16 updates carry up to
-  (T/16) 2^-23 relative error -- the summation the summary allows to differ.  For
-  T <= 1344 this is the 1e-5 of the specification.  v, which squares g, gets twice
-  the bound.
+  rtol(T) = max(1e-5, 0.75 (T/16) 2^-23), from the tensor core's accumulation as
+  measured (tests/tensor_core_sum.py reproduces the GPU's dW bit for bit): every
+  16-token MMA truncates its terms and its sum toward zero, so the deviation from
+  the exact sum grows with T/16; its largest value relative to max(|ref|, rms(ref))
+  is 0.47-0.6 (T/16) 2^-23 on the workloads (up to 1.4e-5 for the Llama layers at
+  T = 4096, against the specification's 1e-5), which tests/test_tensor_core_sum.py
+  and tests/test_gpu_tensor_core_sum.py check against this bound.  For T <= 1789
+  it is the specification's 1e-5.  v, which squares g, gets twice the bound.
 * INT8 codes within +-1; their scales within the moment tolerance.
 * bfloat16 moments (BF16 states) are rounded stochastically like the weight: the weight's
   criterion applies, with the moment before the step in place of W_old and the moment's own
@@ -33,11 +35,14 @@ from oracle import bf16
 
 W_IDENTICAL_FRACTION = 0.999
 MOMENT_RTOL = 1e-5
+# largest deviation of the tensor core's sum from the exact one, relative to max(|ref|, rms(ref)),
+# in units of (T/16) 2^-23 (one binary32 ULP per 16-token MMA), with a margin
+TC_DEVIATION = 0.75
 
 
 def moment_rtol(T: int, squared: bool = False) -> float:
     """Tolerance for a binary32 quantity linear in g (squared: quadratic in g) at T tokens."""
-    r = max(MOMENT_RTOL, (T / 16) * 2.0 ** -23)
+    r = max(MOMENT_RTOL, TC_DEVIATION * (T / 16) * 2.0 ** -23)
     return 2 * r if squared else r
 
 

@@ -62,7 +62,8 @@ def _check(opt, dy, x, w, m, v, W, M, V, hp, t, seed, e=None, ref=None):
     return fracs
 
 
-@pytest.mark.parametrize("opt, d_out, d_in", [(o, 512, 512) for o in STATE_OPTS] + [(o, 384, 256) for o in STATE_OPTS])
+@pytest.mark.parametrize("opt, d_out, d_in", [(o, 2048, 1280) for o in STATE_OPTS] + [(o, 1152, 2560) for o in STATE_OPTS]
+                         + [(o, 384, 256) for o in ("adamw", "lion")])
 def test_fused_bf16_states_match_oracle(opt, d_out, d_in):
     """512 x 512: a CTA pair; 384 x 256: one CTA on 128 x 256.  T = 256, step 3."""
     dy, x, w, m, v = _layer(d_out, d_in, 256, opt, seed=21)
@@ -77,7 +78,7 @@ def test_fused_bf16_states_match_oracle(opt, d_out, d_in):
 @pytest.mark.parametrize("opt", ["adamw", "lion", "adagrad", "sgd_momentum"])
 def test_fused_bf16_equals_unfused_bitwise(opt):
     """Fused step and two-phase step (dW to memory, then the optimizer kernel) agree bit for bit."""
-    dy, x, w, m, v = _layer(512, 768, 320, opt, seed=22)
+    dy, x, w, m, v = _layer(2048, 1280, 320, opt, seed=22)
     hp = default_hparams(opt, lr=1e-3)
     dev = lambda t: None if t is None else t.cuda()
     D, X = dy.cuda(), x.cuda()
@@ -111,10 +112,10 @@ def test_zero_tokens_with_bf16_states():
 
 
 @pytest.mark.parametrize("opt", ["adamw", "rmsprop"])
-def test_two_pairs_sharing_dy_with_bf16_states(opt):
-    """T = 8192 selects clusters of two CTA pairs (256 x 512 tiles)."""
-    T, d_out, d_in = 8192, 512, 1024
-    assert fg.launch_shape(d_out, d_in, T)["cluster"] == 4
+def test_bf16_states_long_token_runs_on_pairs(opt):
+    """T = 8192 on CTA pairs (40 pair tiles of 256 x 256)."""
+    T, d_out, d_in = 8192, 2048, 1280
+    assert fg.launch_shape(d_out, d_in, T)["cluster"] == 2
     dy, x, w, m, v = _layer(d_out, d_in, T, opt, seed=24)
     hp = default_hparams(opt, lr=1e-3)
     W, M, V = w.cuda(), None if m is None else m.cuda(), None if v is None else v.cuda()

@@ -1,8 +1,7 @@
 """The input gradient dX = dY W and the layer backward, CUDA path vs oracle (needs a GB300).
 
 dX runs on the same tile pipeline as the weight gradient with tokens as tile rows, so the cases
-cover each tile shape (one CTA on 128 x 128 or 128 x 256, a CTA pair, two pairs sharing dY), a
-ragged token tail, more tiles than resident CTAs, and the layer backward's ordering: dX must come
+cover each tile shape (one CTA on 128 x 128 or 128 x 256, a CTA pair), a ragged token tail, more tiles than resident CTAs, and the layer backward's ordering: dX must come
 from the weights before the fused step replaces them.
 """
 import numpy as np
@@ -47,10 +46,12 @@ def _run_dx(dy, w, guard_rows=64):
     return out[:T]
 
 
-# (T, d_out, d_in) -> tile: 128 x 128 with a 64-token tail; 128 x 256 with T < 256; CTA pair with a
-# 64-token tail; CTA pair, 170 tiles (more than resident pairs); two pairs sharing dY (d_out >= 8192)
-CASES = [(320, 256, 384, (128, 128, 1)), (192, 384, 512, (128, 256, 1)), (576, 512, 768, (256, 256, 2)),
-         (4160, 512, 2560, (256, 256, 2)), (320, 8192, 1024, (256, 512, 4))]
+# (T, d_out, d_in) -> tile (a shape is taken only when it fills more than half the SMs): 128 x 128
+# with a 64-token tail; 128 x 256 with T not a multiple of 256 (80 tiles); a CTA pair with a 64-token
+# tail (90 pair tiles); a CTA pair, 170 tiles (more than resident pairs); a CTA pair on a long
+# reduction (d_out = 8192, 40 pair tiles); few pair tiles, so 128 x 128 instead
+CASES = [(320, 256, 384, (128, 128, 1)), (640, 384, 4096, (128, 256, 1)), (2112, 512, 2560, (256, 256, 2)),
+         (4160, 512, 2560, (256, 256, 2)), (1024, 8192, 2560, (256, 256, 2)), (576, 512, 768, (128, 128, 1))]
 
 
 @pytest.mark.parametrize("T, d_out, d_in, shape", CASES)
@@ -106,7 +107,7 @@ def _backward_case(opt, T, d_out, d_in, seed):
 
 
 @pytest.mark.parametrize("opt, T, d_out, d_in", [("adamw", 512, 512, 768), ("lion", 256, 384, 384),
-                                                 ("sgd", 192, 256, 512)])
+                                                 ("sgd", 192, 256, 512), ("adamw", 1024, 2048, 2560)])
 def test_linear_backward_reads_weights_before_the_step(opt, T, d_out, d_in):
     """dX equals dY W_old (not dY W_new) and the weight step equals a separate fused step bit for bit."""
     dy, x, w, m, v = _backward_case(opt, T, d_out, d_in, seed=60)
@@ -137,8 +138,8 @@ def test_linear_backward_reads_weights_before_the_step(opt, T, d_out, d_in):
 
 @pytest.mark.parametrize("layer", [0, 2])
 def test_llama8b_dx_sampled(layer):
-    """Llama-3.1-8B MLP gate (dY 4096 x 14336, W 14336 x 4096: two pairs sharing dY) and down (dY
-    4096 x 4096, W 4096 x 14336: CTA pairs), T = 4096: sampled dX elements vs d_out-term dot products."""
+    """Llama-3.1-8B MLP gate (dY 4096 x 14336, W 14336 x 4096) and down (dY 4096 x 4096, W 4096 x
+    14336), both on CTA pairs, T = 4096: sampled dX elements vs d_out-term dot products."""
     wl = WORKLOADS["llama8b-mlp"]
     dy, _ = activations(wl, layer, 1)
     w, _, _ = layer_state(wl, layer, "adamw")

@@ -2,8 +2,7 @@
 
 The tensor core sums E4M3 code products (kind::f8f6f4, 128 tokens per pipeline stage) in FP32;
 the epilogue multiplies the finished gradient tile by s_dY * s_X before the optimizer.  The cases
-cover every tile shape (one CTA on 128 x 128 and 128 x 256, a CTA pair, two pairs sharing dY by
-multicast), a ragged token tail and ragged rows and columns, every optimizer and state format.
+cover every tile shape (one CTA on 128 x 128 and 128 x 256, a CTA pair), a ragged token tail and ragged rows and columns, every optimizer and state format.
 """
 import numpy as np
 import pytest
@@ -38,10 +37,18 @@ def _np8(t):
     return t.numpy().astype(np.uint8)
 
 
-# (d_out, d_in, T, tile): a pair; 128 x 256; 128 x 128 with a token tail; ragged rows and columns on
-# pairs (1104 and 1296 are multiples of 16, not of 128)
-CASES = [(512, 512, 256, (256, 256, 2)), (384, 256, 256, (128, 256, 1)), (384, 384, 192, (128, 128, 1)),
-         (1104, 1296, 100, (256, 256, 2))]
+def _allow(opt, ref, w, m, v, hp, t, seed, T, state="fp32", ms=None, vs=None, what="w_f32"):
+    """Per element, the movement of the oracle's binary32 output `what` under the gradient's
+    allowed summation deviation (compare.gradient_sensitivity) for a whole layer."""
+    e = np.arange(w.numel(), dtype=np.uint64).reshape(w.shape)
+    return gradient_sensitivity(opt, ref["g"], bits(w), m, v, hp, t, seed, e, moment_rtol(T), state, ms, vs,
+                                what=what)
+
+
+# (d_out, d_in, T, tile): a pair (40 pair tiles); 128 x 256 (90 tiles); 128 x 128 with a token tail;
+# ragged rows and columns on pairs (2128 and 1296 are multiples of 16, not of 128; 54 pair tiles)
+CASES = [(2048, 1280, 256, (256, 256, 2)), (1152, 2560, 256, (128, 256, 1)), (384, 384, 192, (128, 128, 1)),
+         (2128, 1296, 100, (256, 256, 2))]
 
 
 @pytest.mark.parametrize("d_out, d_in, T, tile", CASES)
@@ -72,7 +79,7 @@ def test_dw_gemm_e4m3_is_exact_on_integer_patterns():
 
 
 @pytest.mark.parametrize("opt", OPTIMIZERS)
-@pytest.mark.parametrize("d_out, d_in", [(512, 512), (384, 256)])
+@pytest.mark.parametrize("d_out, d_in", [(2048, 1280), (1152, 2560)])
 def test_fused_e4m3_fp32_states(opt, d_out, d_in):
     T = 256
     dyq, s_dy, xq, s_x, w, m, v = _layer(d_out, d_in, T, opt, seed=3)
@@ -84,7 +91,9 @@ def test_fused_e4m3_fp32_states(opt, d_out, d_in):
     assert fg.sync_status() == 0
     ref = fp8.fused_step_fp8(opt, _np8(dyq), _np8(xq), s_dy, s_x, bits(w), None if m is None else f32(m),
                              None if v is None else f32(v), hp, 4, 11)
-    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w),
+                   extra_tol=_allow(opt, ref, w, None if m is None else f32(m), None if v is None else f32(v), hp, 4,
+                                    11, T))
     if m is not None:
         assert_moments(f32(M), ref["m"], "m")
     if v is not None:
@@ -92,7 +101,7 @@ def test_fused_e4m3_fp32_states(opt, d_out, d_in):
 
 
 def test_fused_e4m3_bf16_and_int8_states():
-    T, d_out, d_in = 192, 512, 768
+    T, d_out, d_in = 192, 2048, 1280
     dyq, s_dy, xq, s_x, w, m, v = _layer(d_out, d_in, T, "adamw", seed=4)
     hp = default_hparams("adamw", lr=1e-3)
     # BF16 states
@@ -102,9 +111,10 @@ def test_fused_e4m3_bf16_and_int8_states():
     torch.cuda.synchronize()
     ref = fp8.fused_step_fp8("adamw", _np8(dyq), _np8(xq), s_dy, s_x, bits(w), bits(mb), bits(vb), hp, 2, 5,
                              state="bf16")
-    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
-    assert_weights(bits(M), ref["m"], "m", w_old_bits=bits(mb))
-    assert_weights(bits(V), ref["v"], "v", w_old_bits=bits(vb))
+    allow = lambda what: _allow("adamw", ref, w, bits(mb), bits(vb), hp, 2, 5, T, "bf16", what=what)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=allow("w_f32"))
+    assert_weights(bits(M), ref["m"], "m", w_old_bits=bits(mb), extra_tol=allow("m_f32"))
+    assert_weights(bits(V), ref["v"], "v", w_old_bits=bits(vb), extra_tol=allow("v_f32"))
     # INT8 states
     rng = np.random.default_rng(4)
     m32 = (f32(moment_init("absnormal:1e-4", w.shape, 6)) * np.sign(rng.standard_normal(w.shape))).astype(np.float32)
@@ -116,7 +126,8 @@ def test_fused_e4m3_bf16_and_int8_states():
     fg.fused_dw_step_e4m3(dyq.cuda(), xq.cuda(), s_dy, s_x, W, M, V, Q, "adamw", hp, 3, seed=8)
     torch.cuda.synchronize()
     ref = fp8.fused_step_fp8("adamw", _np8(dyq), _np8(xq), s_dy, s_x, bits(w), mq, vq, hp, 3, 8, "int8", ms, vs)
-    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w),
+                   extra_tol=_allow("adamw", ref, w, mq, vq, hp, 3, 8, T, "int8", ms, vs))
     assert_codes(M.cpu().numpy(), ref["m"], "m codes")
     assert_codes(V.cpu().numpy(), ref["v"], "v codes")
     n64 = w.numel() // 64
@@ -125,7 +136,7 @@ def test_fused_e4m3_bf16_and_int8_states():
     assert_moments(q[n64:], ref["v_scales"].ravel(), "v scales")
 
 
-@pytest.mark.parametrize("d_out, d_in, T", [(512, 768, 320), (1104, 1296, 100)])
+@pytest.mark.parametrize("d_out, d_in, T", [(2048, 1280, 320), (2128, 1296, 100), (512, 768, 320)])
 def test_fused_e4m3_equals_unfused_bitwise(d_out, d_in, T):
     dyq, s_dy, xq, s_x, w, m, v = _layer(d_out, d_in, T, "adamw", seed=9)
     hp = default_hparams("adamw", lr=1e-3)
@@ -142,10 +153,10 @@ def test_fused_e4m3_equals_unfused_bitwise(d_out, d_in, T):
 
 
 @pytest.mark.parametrize("opt", ["adamw", "lion"])
-def test_two_pairs_sharing_dy_with_e4m3(opt):
-    """T = 8192: clusters of two CTA pairs, each loading one token half of every dY stage by multicast."""
-    T, d_out, d_in = 8192, 512, 1024
-    assert fg.launch_shape(d_out, d_in, T)["cluster"] == 4
+def test_e4m3_long_token_runs_on_pairs(opt):
+    """T = 8192 on CTA pairs: 64 stages of 128 tokens per tile."""
+    T, d_out, d_in = 8192, 2048, 1280
+    assert fg.launch_shape(d_out, d_in, T)["cluster"] == 2
     dyq, s_dy, xq, s_x, w, m, v = _layer(d_out, d_in, T, opt, seed=10)
     hp = default_hparams(opt, lr=1e-3)
     W, M, V = w.cuda(), m.cuda(), None if v is None else v.cuda()
@@ -201,7 +212,8 @@ def _layer_channels(d_out, d_in, T, opt, seed):
     return dyq, s_dy, xq, s_x, w, m, v
 
 
-@pytest.mark.parametrize("d_out, d_in, T", [(512, 512, 256), (384, 256, 256), (384, 384, 192), (1104, 1296, 100)])
+@pytest.mark.parametrize("d_out, d_in, T", [(2048, 1280, 256), (1152, 2560, 256), (384, 384, 192),
+                                            (2128, 1296, 100)])
 def test_dw_gemm_e4m3_channel_scales(d_out, d_in, T):
     """Every tile shape; 1296 columns end 16 past a 32-column strip, so the last 4-column scale
     groups of a strip lie outside the layer."""
@@ -215,13 +227,13 @@ def test_dw_gemm_e4m3_channel_scales(d_out, d_in, T):
 
 
 def test_constant_channel_scales_equal_the_tensor_scale_bitwise():
-    dyq, s_dy, xq, s_x, w, m, v = _layer(512, 768, 256, "adamw", seed=12)
+    dyq, s_dy, xq, s_x, w, m, v = _layer(2048, 1280, 256, "adamw", seed=12)
     hp = default_hparams("adamw", lr=1e-3)
     D, X = dyq.cuda(), xq.cuda()
     W1, M1, V1 = w.cuda(), m.cuda(), v.cuda()
     W2, M2, V2 = w.cuda(), m.cuda(), v.cuda()
     fg.fused_dw_step_e4m3(D, X, s_dy, s_x, W1, M1, V1, None, "adamw", hp, 3, seed=7)
-    fg.fused_dw_step_e4m3(D, X, torch.full((512,), s_dy, device="cuda"), torch.full((768,), s_x, device="cuda"),
+    fg.fused_dw_step_e4m3(D, X, torch.full((2048,), s_dy, device="cuda"), torch.full((1280,), s_x, device="cuda"),
                           W2, M2, V2, None, "adamw", hp, 3, seed=7)
     torch.cuda.synchronize()
     assert torch.equal(W1.view(torch.int16), W2.view(torch.int16))
@@ -230,7 +242,7 @@ def test_constant_channel_scales_equal_the_tensor_scale_bitwise():
 
 @pytest.mark.parametrize("opt, state", [("adamw", "fp32"), ("lion", "fp32"), ("rmsprop", "fp32"), ("adamw", "bf16")])
 def test_fused_e4m3_channel_scales(opt, state):
-    T, d_out, d_in = 256, 512, 1024
+    T, d_out, d_in = 256, 2048, 1280
     dyq, s_dy, xq, s_x, w, m, v = _layer_channels(d_out, d_in, T, opt, seed=13)
     if state == "bf16":
         m, v = (None if t is None else t.to(torch.bfloat16) for t in (m, v))
@@ -244,18 +256,19 @@ def test_fused_e4m3_channel_scales(opt, state):
     vv = None if v is None else (bits(v) if state == "bf16" else f32(v))
     ref = fp8.fused_step_fp8(opt, _np8(dyq), _np8(xq), s_dy.numpy(), s_x.numpy(), bits(w), mm, vv, hp, 2, 9,
                              state=state)
-    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=_allow(opt, ref, w, mm, vv, hp, 2, 9, T, state))
     for got, old, key in ((M, m, "m"), (V, v, "v")):
         if got is None:
             continue
         if state == "bf16":
-            assert_weights(bits(got), ref[key], key, w_old_bits=bits(old))
+            assert_weights(bits(got), ref[key], key, w_old_bits=bits(old),
+                           extra_tol=_allow(opt, ref, w, mm, vv, hp, 2, 9, T, state, what=key + "_f32"))
         else:
             assert_moments(f32(got), ref[key], key)
 
 
 def test_fused_e4m3_channel_scales_equal_unfused_bitwise():
-    dyq, s_dy, xq, s_x, w, m, v = _layer_channels(1104, 1296, 100, "adamw", seed=14)
+    dyq, s_dy, xq, s_x, w, m, v = _layer_channels(2128, 1296, 100, "adamw", seed=14)
     hp = default_hparams("adamw", lr=1e-3)
     D, X, SD, SX = dyq.cuda(), xq.cuda(), s_dy.cuda(), s_x.cuda()
     W1, M1, V1 = w.cuda(), m.cuda(), v.cuda()

@@ -163,3 +163,68 @@ def test_sub_ulp_updates_accumulate_without_bias():
     assert abs(diff.mean()) < 3 * sigma, (diff.mean(), sigma)
     moved = (gpu - w0) * np.sign(master - w0)
     assert moved.mean() > 0.5 * np.abs(master - w0).mean()
+
+
+# ---------------------------------------------------------------------------- Qwen3-14B layer shapes
+
+def _device_sampled_check(wl, layer, opt, t, seed, n=2048, pos_seed=0):
+    """One fused step on a full-size layer whose inputs are drawn on the device; the oracle gets
+    the sampled positions' inputs copied back (the dY and X columns they read, W/m/v there)."""
+    l = wl.layers[layer]
+    hp = default_hparams(opt)
+    dev = torch.device("cuda")
+    dy, x = activations(wl, layer, 1, device=dev)
+    W, M, V = layer_state(wl, layer, opt, device=dev)
+    rows, cols = (np.asarray(a) for a in sample_positions(l.d_out, l.d_in, n, pos_seed))
+    ri_t, ci_t = torch.from_numpy(rows).to(dev), torch.from_numpy(cols).to(dev)
+    w0 = bits(W[ri_t, ci_t])
+    m0 = None if M is None else f32(M[ri_t, ci_t])
+    v0 = None if V is None else f32(V[ri_t, ci_t])
+    ur, ri = np.unique(rows, return_inverse=True)
+    uc, ci = np.unique(cols, return_inverse=True)
+    dy_cols = bits(dy[:, torch.from_numpy(ur).to(dev)])
+    x_cols = bits(x[:, torch.from_numpy(uc).to(dev)])
+    fg.fused_dw_step(dy, x, W, M, V, None, opt, hp, t, seed=seed)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    g = ostep.dw_at(dy_cols, x_cols, ri, ci)
+    e = (rows * l.d_in + cols).astype(np.uint64)
+    ref = ostep.apply_update(opt, g, w0, m0, v0, hp, t, seed, e)
+    rt = moment_rtol(wl.T)
+    extra = gradient_sensitivity(opt, g, w0, m0, v0, hp, t, seed, e, rt)
+    assert_weights(bits(W[ri_t, ci_t]), ref["W"], "W", w_old_bits=w0, extra_tol=extra)
+    if M is not None:
+        assert_moments(f32(M[ri_t, ci_t]), ref["m"], "m", rtol=rt)
+    if V is not None:
+        assert_moments(f32(V[ri_t, ci_t]), ref["v"], "v", rtol=moment_rtol(wl.T, squared=True))
+    return fg.launch_shape(l.d_out, l.d_in, wl.T)
+
+
+@pytest.mark.parametrize("layer, name", [(0, "q"), (1, "k"), (4, "gate"), (6, "down")])
+def test_qwen14b_layer_sampled(layer, name):
+    """Qwen3-14B-shaped layers at T = 8192 (q 5120 x 5120, k 1024 x 5120, gate 17408 x 5120, down
+    5120 x 17408), AdamW with FP32 moments at step 10, sampled elements against the oracle.  Every
+    shape runs on CTA pairs, most with more tiles than resident pairs."""
+    wl = WORKLOADS["qwen14b-sweep"]
+    assert wl.layers[layer].name.endswith(name)
+    shape = _device_sampled_check(wl, layer, "adamw", 10, 0x5EED + layer, n=2048, pos_seed=layer)
+    assert (shape["tile_rows"], shape["tile_cols"], shape["cluster"]) == (256, 256, 2)
+
+
+def test_qwen14b_gate_fused_equals_two_phase_bitwise():
+    """Every element of the largest Qwen3-14B layer (gate, 17408 x 5120, T = 8192): the fused step
+    and the two-phase step agree bit for bit."""
+    wl = WORKLOADS["qwen14b-sweep"]
+    hp = default_hparams("adamw")
+    dev = torch.device("cuda")
+    dy, x = activations(wl, 4, 1, device=dev)
+    W1, M1, V1 = layer_state(wl, 4, "adamw", device=dev)
+    W2, M2, V2 = W1.clone(), M1.clone(), V1.clone()
+    fg.fused_dw_step(dy, x, W1, M1, V1, None, "adamw", hp, 10, seed=5)
+    dW = torch.empty(W1.shape, dtype=torch.float32, device=dev)
+    fg.dw_gemm(dy, x, dW)
+    fg.opt_step(dW, W2, M2, V2, None, "adamw", hp, 10, seed=5)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    assert torch.equal(W1.view(torch.int16), W2.view(torch.int16))
+    assert torch.equal(M1, M2) and torch.equal(V1, V2)

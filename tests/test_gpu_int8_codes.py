@@ -69,9 +69,9 @@ def _exact_gradient(dy, x):
     return g
 
 
-# (d_out, d_in, T): a CTA-pair kernel, 256 x 256 tiles; one CTA on 128-row tiles; two CTA pairs
-# sharing dY slices on 256 x 512 tiles (T = 8192)
-SHAPES = [(512, 768, 256, (256, 256)), (384, 512, 192, (128, 256)), (512, 1024, 8192, (256, 512))]
+# (d_out, d_in, T): a CTA pair on 256 x 256 tiles (40 pair tiles); one CTA on 128 x 256 tiles (90);
+# a CTA pair over a long token run (T = 8192)
+SHAPES = [(2048, 1280, 256, (256, 256)), (1152, 2560, 192, (128, 256)), (2048, 1280, 8192, (256, 256))]
 
 
 @pytest.mark.parametrize("opt", [o for o in OPTIMIZERS if o != "sgd"])

@@ -11,7 +11,8 @@ import torch
 
 import backward_optimizer_gb300 as fg
 from oracle import backward as obw, int8_block, step as ostep
-from tests.compare import assert_bf16_sum, assert_codes, assert_moments, assert_weights, moment_rtol
+from tests.compare import (assert_bf16_sum, assert_codes, assert_moments, assert_weights, gradient_sensitivity,
+                           moment_rtol)
 from tests.helpers import bits, f32
 from workloads import Layer, Workload, activations, default_hparams, layer_state, moment_init
 
@@ -53,9 +54,9 @@ def _layer(d_out, d_in, T, opt, seed):
 
 
 # (d_out, d_in, T, tile): 128 x 128 with ragged rows, columns (d_in not a multiple of 16) and
-# tokens; a CTA pair whose last row tile leaves one CTA wholly outside the layer; 128 x 256 with
-# ragged columns; an 8 x 8 layer with one token
-CASES = [(200, 136, 100, (128, 128, 1)), (1096, 1288, 70, (256, 256, 2)), (384, 1032, 64, (128, 256, 1)),
+# tokens; a CTA pair whose last row tile leaves one CTA wholly outside the layer (54 pair tiles);
+# 128 x 256 with ragged columns (115 tiles); an 8 x 8 layer with one token
+CASES = [(200, 136, 100, (128, 128, 1)), (2056, 1288, 70, (256, 256, 2)), (2944, 1032, 64, (128, 256, 1)),
          (8, 8, 1, (128, 128, 1))]
 
 
@@ -78,7 +79,10 @@ def test_fused_fp32_states_on_ragged_layers(opt, d_out, d_in, T, tile):
     assert fg.sync_status() == 0
     ref = ostep.fused_step(opt, bits(dy), bits(x), bits(w), None if m is None else f32(m),
                            None if v is None else f32(v), hp, 3, 17)
-    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
+    extra = gradient_sensitivity(opt, ref["g"], bits(w), None if m is None else f32(m),
+                                 None if v is None else f32(v), hp, 3, 17, e, moment_rtol(T))
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=extra)
     assert _tail_intact(fw, w.numel())
     for flat, got, old, key in ((fm, M, m, "m"), (fv, V, v, "v")):
         if old is not None:
@@ -86,7 +90,7 @@ def test_fused_fp32_states_on_ragged_layers(opt, d_out, d_in, T, tile):
             assert _tail_intact(flat, old.numel())
 
 
-@pytest.mark.parametrize("d_out, d_in, T", [(200, 136, 100), (1096, 1288, 70)])
+@pytest.mark.parametrize("d_out, d_in, T", [(200, 136, 100), (2056, 1288, 70)])
 def test_fused_bf16_states_on_ragged_layers(d_out, d_in, T):
     dy, x, w, m, v = _layer(d_out, d_in, T, "adamw", seed=5)
     m, v = m.to(torch.bfloat16), v.to(torch.bfloat16)
@@ -97,16 +101,19 @@ def test_fused_bf16_states_on_ragged_layers(d_out, d_in, T):
     fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, None, "adamw", hp, 2, seed=6)
     torch.cuda.synchronize()
     ref = ostep.fused_step("adamw", bits(dy), bits(x), bits(w), bits(m), bits(v), hp, 2, 6, state="bf16")
-    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
-    assert_weights(bits(M), ref["m"], "m", w_old_bits=bits(m))
-    assert_weights(bits(V), ref["v"], "v", w_old_bits=bits(v))
+    e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
+    args = ("adamw", ref["g"], bits(w), bits(m), bits(v), hp, 2, 6, e, moment_rtol(T), "bf16")
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=gradient_sensitivity(*args))
+    assert_weights(bits(M), ref["m"], "m", w_old_bits=bits(m), extra_tol=gradient_sensitivity(*args, what="m_f32"))
+    assert_weights(bits(V), ref["v"], "v", w_old_bits=bits(v), extra_tol=gradient_sensitivity(*args, what="v_f32"))
     for flat, t in ((fw, w), (fm, m), (fv, v)):
         assert _tail_intact(flat, t.numel())
 
 
-@pytest.mark.parametrize("d_out, d_in, T", [(200, 320, 100), (1096, 1088, 70)])
+@pytest.mark.parametrize("d_out, d_in, T", [(200, 320, 100), (2056, 1088, 70)])
 def test_fused_int8_states_on_ragged_layers(d_out, d_in, T):
-    """d_in a multiple of 64 (1088 = 17 blocks, a ragged 256-column tile), ragged rows and tokens."""
+    """d_in a multiple of 64 (1088 = 17 blocks, a ragged 256-column tile of a CTA pair), ragged rows
+    and tokens."""
     dy, x, w, _, _ = _layer(d_out, d_in, T, "adamw", seed=7)
     rng = np.random.default_rng(7)
     m32 = (f32(moment_init("absnormal:1e-4", w.shape, 8)) * np.sign(rng.standard_normal(w.shape))).astype(np.float32)
@@ -121,7 +128,9 @@ def test_fused_int8_states_on_ragged_layers(d_out, d_in, T):
     fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, Q, "adamw", hp, 5, seed=12)
     torch.cuda.synchronize()
     ref = ostep.fused_step("adamw", bits(dy), bits(x), bits(w), mq, vq, hp, 5, 12, "int8", ms, vs)
-    assert_weights(bits(W), ref["W"], w_old_bits=bits(w))
+    e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
+    extra = gradient_sensitivity("adamw", ref["g"], bits(w), mq, vq, hp, 5, 12, e, moment_rtol(T), "int8", ms, vs)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=extra)
     n64 = w.numel() // 64
     q = Q.cpu().numpy()
     assert_codes(M.cpu().numpy(), ref["m"], "m codes")
@@ -132,7 +141,7 @@ def test_fused_int8_states_on_ragged_layers(d_out, d_in, T):
         assert _tail_intact(flat, n)
 
 
-@pytest.mark.parametrize("d_out, d_in, T", [(200, 136, 100), (1096, 1288, 70)])
+@pytest.mark.parametrize("d_out, d_in, T", [(200, 136, 100), (2056, 1288, 70)])
 def test_fused_equals_unfused_on_ragged_layers(d_out, d_in, T):
     """The two-phase kernel's last warp is partly past the end (d_out d_in / 8 not a multiple of 32)."""
     dy, x, w, m, v = _layer(d_out, d_in, T, "adamw", seed=9)
