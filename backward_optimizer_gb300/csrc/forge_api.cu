@@ -210,24 +210,15 @@ forge_status check_opt_args(const void* W, const void* m, const void* v, const f
 
 forge_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FORGE_OK : FORGE_ERR_CUDA; }
 
-// L2 residency of the operands.  The tile order keeps up to kL2ResidentBytes of the smaller operand's
-// slices in L2 while the larger operand's slices stream past once per group; the resident
-// operand's loads carry an L2 evict-last hint, the streaming one's evict-normal (FORGE_STREAM_KEEP
-// = 1: evict-last for both).  The weight and moment traffic of the epilogue, which passes through
-// L2 once, shares the rest.
-#ifndef FORGE_L2_RESIDENT_MB
-#define FORGE_L2_RESIDENT_MB 48
-#endif
-#ifndef FORGE_STREAM_KEEP
-#define FORGE_STREAM_KEEP 1
-#endif
-constexpr int64_t kL2ResidentBytes = int64_t{FORGE_L2_RESIDENT_MB} << 20;
+// Tile order: groups of kGroupRows tile rows, each group swept one tile column at a time, so the
+// CTAs running at once share about kGroupRows dY slices and 76 / kGroupRows X slices in L2.  Both
+// operands load with an L2 evict-last hint, ahead of the epilogue's weight and moment stream, which
+// passes through L2 once.  Orders that keep the smaller operand wholly resident in L2 and stream the
+// other (fewer DRAM bytes) measured 3-4 % slower on every Llama-3.1-8B and Qwen3-14B layer shape.
+constexpr int kGroupRows = 8;
 
-void set_order(forge::TileArgs& a, int tiles_m, int tiles_n, int64_t a_block, int64_t b_block) {
-    a.order = forge::schedule_for(tiles_m, tiles_n, a_block, b_block, kL2ResidentBytes);
-    const bool a_resident = a.order.raster_cols == 0;
-    a.l2_keep_a = a_resident || FORGE_STREAM_KEEP;
-    a.l2_keep_b = !a_resident || FORGE_STREAM_KEEP;
+forge::TileOrder tile_order(int tiles_m, int tiles_n) {
+    return forge::TileOrder{tiles_m, tiles_n, tiles_m < kGroupRows ? tiles_m : kGroupRows, 0};
 }
 
 // The epilogue's wait for a finished accumulator spans a whole tile mainloop: the base limit plus
@@ -381,9 +372,7 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     const int tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn));
     a.num_tiles = tiles_m * tiles_n;
     a.k_blocks = static_cast<int>(ceil_div(a.T, e4m3 ? 128 : forge::kBK));
-    // a tile row reads 128 * cg rows of dY over all tokens, a tile column bn columns of X
-    const int64_t esize = e4m3 ? 1 : 2;
-    set_order(a, tiles_m, tiles_n, int64_t{forge::kBM} * ts.cg * shape->T * esize, int64_t{ts.bn} * shape->T * esize);
+    a.order = tile_order(tiles_m, tiles_n);
     a.g_scale = g_scale;
     a.row_scales = row_scales;
     a.col_scales = col_scales;
@@ -430,8 +419,7 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
     const int tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn));
     a.num_tiles = tiles_m * tiles_n;
     a.k_blocks = static_cast<int>(ceil_div(a.d_out, forge::kBK));
-    // a tile row reads `rows` token rows of dY over all of d_out, a tile column bn columns of W
-    set_order(a, tiles_m, tiles_n, int64_t{rows} * shape->d_out * 2, int64_t{ts.bn} * shape->d_out * 2);
+    a.order = tile_order(tiles_m, tiles_n);
     a.dX = static_cast<uint16_t*>(dX);
     a.status = dev.status;
     a.wait_limit_ns = g_wait_limit_ns.load();

@@ -18,8 +18,7 @@
 //               gradient registers are then dropped (step 3); W/m/v are read and written with
 //               256-bit accesses (step 4).  The gradient never reaches device memory.
 // Tiles are visited by a static persistent schedule (tile = blockIdx.x + k * gridDim.x) in the
-// grouped order of schedule.h, which keeps the smaller operand's slices resident in L2 while the
-// larger one streams past.
+// grouped order of schedule.h, so that concurrently running CTAs share dY and X slices in L2.
 //
 // The same pipeline also computes the layer's input gradient dX = dY W (EPI = kEpiDX), which the
 // fused step's ordering requires before W is overwritten: there the tile rows are tokens, the
@@ -95,7 +94,6 @@ struct TileArgs {
     int d_out, d_in, T;
     TileOrder order;              // tile rows x columns and the order they are visited in
     int num_tiles;
-    int l2_keep_a, l2_keep_b;     // per operand: L2 evict-last (1) or evict-normal (0) on its loads
     int k_blocks;                 // reduction slices per tile: T / 64 (dW; T / 128 for E4M3), d_out / 64 (dX)
     float g_scale;                // E4M3 operands: s_dY * s_X, applied to the FP32 gradient tile
     const float* row_scales;      // or per channel (both set): s_dY [d_out] and s_X [d_in], each
@@ -406,128 +404,104 @@ __device__ __forceinline__ void epi_store_dx(const TileArgs& a, int row0, int co
     }
 }
 
-// INT8 moments, on the transposed ownership of strip_transpose.  For each group of 64 columns (one
-// quantisation block per row) the warp stages both 32-column gradient strips; lane l then owns 8
-// consecutive columns in each half of rows (l div 4) + 8k, and the 4 lanes 4q .. 4q+3 together
-// hold each of those rows' 64-element block, so a block's absmax takes two shuffles.  Rows are
-// handled one at a time (the next row's W, codes and scales are loaded while the current one is
-// computed): pass 1 computes the row block's new moments and absmax, pass 2 recomputes the same
-// moments bit for bit, updates the weight with the unquantised moments and writes the codes under
-// the new scales.
+// INT8 moments.  For each group of 64 columns (one quantisation block per row) the warp stages
+// both 32-column gradient strips; lane l then owns the 8 columns 8 (l mod 8) .. +7 of the block in
+// rows (l div 8) + 4k, k = 0..7, so the 8 lanes 8r .. 8r+7 together hold a row's block and its
+// absmax takes three shuffles.  Per row, one pass computes everything but the codes -- the new
+// moments in binary32, the weight update from them and its stochastic rounding, the block
+// absmax -- and keeps the new moments in registers; the codes then follow from the new scale.
 template <int OPT>
 struct Int8RowIn {
-    uint32_t w[2][4];   // 2 halves x 8 bf16
-    uint32_t mq[2][2];  // 2 halves x 8 codes
-    uint32_t vq[2][2];
+    uint32_t w[4];  // 8 bf16
+    uint32_t mq[2];  // 8 codes, biased (c + 128 per byte, as int8_at_flipped decodes)
+    uint32_t vq[2];
     float ms, vs;
 };
 
 template <int OPT>
-__device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e_row, bool ok, Int8RowIn<OPT>& in) {
+__device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e, bool ok, Int8RowIn<OPT>& in) {
     using Tr = OptTraits<OPT>;
-    if (!ok) e_row = 0;  // a row past the layer's last reads the first (always valid) and stores nothing
+    if (!ok) e = 0;  // a row past the layer's last reads the first (always valid) and stores nothing
+    ld_v4(a.W + e, in.w);
+    if constexpr (Tr::kM) ld_v2(static_cast<int8_t*>(a.m) + e, in.mq);
+    if constexpr (Tr::kV) ld_v2(static_cast<int8_t*>(a.v) + e, in.vq);
+    in.ms = Tr::kM ? a.m_scales[e >> 6] : 0.f;
+    in.vs = Tr::kV ? a.v_scales[e >> 6] : 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        ld_v4(a.W + e_row + 32 * h, in.w[h]);
-        if constexpr (Tr::kM) ld_v2(static_cast<int8_t*>(a.m) + e_row + 32 * h, in.mq[h]);
-        if constexpr (Tr::kV) ld_v2(static_cast<int8_t*>(a.v) + e_row + 32 * h, in.vq[h]);
+    for (int i = 0; i < 2; ++i) {
+        in.mq[i] ^= 0x80808080u;
+        in.vq[i] ^= 0x80808080u;
     }
-    in.ms = Tr::kM ? a.m_scales[e_row >> 6] : 0.f;
-    in.vs = Tr::kV ? a.v_scales[e_row >> 6] : 0.f;
+}
+
+// The 8 gradient values of strip row r, columns 8 c8 .. 8 c8 + 7 (c8 < 4) of a 32-column strip.
+__device__ __forceinline__ void strip_load_run(const uint8_t* strip, uint32_t r, uint32_t c8, uint32_t (&out)[8]) {
+    const uint32_t base = smem_addr(strip) + r * 128u;
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            in.mq[h][i] ^= 0x80808080u;  // the biased form int8_at_flipped decodes
-            in.vq[h][i] ^= 0x80808080u;
-        }
+    for (uint32_t h = 0; h < 2; ++h) ld_shared_v4(base + (((2u * c8 + h) ^ (r & 7u)) << 4), &out[4 * h]);
 }
 
 template <int OPT>
-__device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e_row, bool ok, const uint8_t* strip,
-                                                int k, Int8RowIn<OPT>& in) {
+__device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e, bool ok, const uint32_t (&g)[8],
+                                                const Int8RowIn<OPT>& in) {
     using Tr = OptTraits<OPT>;
-    // pass 1: absmax of the row block's new moments
+    const Philox4 p = sr_words(e >> 3, a.seed, a.step);
+    float mn[8], vn[8];
+    uint32_t wo[4];
     float am = 0.f, av = 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t g[8];
-        strip_load_row(strip + h * 4096, k, g);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
-            float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
-            float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
-            opt_moments<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
-            am = fmaxf(am, fabsf(mm));
-            av = fmaxf(av, fabsf(vv));
-        }
+    for (int j = 0; j < 8; ++j) {
+        const float wf = (j & 1) ? bf16_hi(in.w[j >> 1]) : bf16_lo(in.w[j >> 1]);
+        float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[j >> 2], j & 3), in.ms) : 0.f;
+        float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[j >> 2], j & 3), in.vs) : 0.f;
+        const float wn = opt_update<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
+        const uint32_t b = sr_bf16(wn, sr_r16(p, j));
+        wo[j >> 1] = (j & 1) ? (wo[j >> 1] | (b << 16)) : b;
+        mn[j] = mm;
+        vn[j] = vv;
+        am = fmaxf(am, fabsf(mm));
+        av = fmaxf(av, fabsf(vv));
     }
 #pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
-        av = fmaxf(av, __shfl_xor_sync(0xFFFFFFFFu, av, off));
+    for (int off = 1; off < 8; off <<= 1) {
+        if constexpr (Tr::kM) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
+        if constexpr (Tr::kV) av = fmaxf(av, __shfl_xor_sync(0xFFFFFFFFu, av, off));
     }
     const float nms = __fdiv_rn(am, 127.0f), nvs = __fdiv_rn(av, 127.0f);
     const Int8Coder cm = int8_coder(Tr::kM ? nms : 0.f), cv = int8_coder(Tr::kV ? nvs : 0.f);
-    // pass 2: update, round, requantise, store
+    uint32_t mo[2] = {0u, 0u}, vo[2] = {0u, 0u};
+    uint32_t redo = 0u;  // bit j: m code j needs the division; bit 8 + j: v code j
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t g[8];
-        strip_load_row(strip + h * 4096, k, g);
-        const size_t e = e_row + 32 * h;
-        const Philox4 p = sr_words(e >> 3, a.seed, a.step);
-        uint32_t mo[2] = {0u, 0u}, vo[2] = {0u, 0u}, wo[4];
-        uint32_t redo = 0u;  // bit j: m code j needs the division; bit 8 + j: v code j
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
-            float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
-            float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
-            const float wn = opt_update<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
-            const uint32_t b = sr_bf16(wn, sr_r16(p, j));
-            wo[j >> 1] = (j & 1) ? (wo[j >> 1] | (b << 16)) : b;
-            bool exact = true;
-            if constexpr (Tr::kM) {
-                mo[j >> 2] = put_byte(mo[j >> 2], int8_code_fast(mm, cm, exact), j & 3);
-                redo |= exact ? 0u : (1u << j);
-            }
-            if constexpr (Tr::kV) {
-                vo[j >> 2] = put_byte(vo[j >> 2], int8_code_fast(vv, cv, exact), j & 3);
-                redo |= exact ? 0u : (0x100u << j);
-            }
+    for (int j = 0; j < 8; ++j) {
+        bool exact = true;
+        if constexpr (Tr::kM) {
+            mo[j >> 2] = put_byte(mo[j >> 2], int8_code_fast(mn[j], cm, exact), j & 3);
+            redo |= exact ? 0u : (1u << j);
         }
-        if (redo != 0u) {
-            // rare: a code next to a rounding boundary, or a scale that is not a normal number.
-            // The moments are recomputed from the same inputs (gradient strip, old weights, old
-            // codes) and the IEEE division decides; one branch per 8 elements instead of one per
-            // code.
-            strip_load_row(strip + h * 4096, k, g);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (redo & (0x101u << j)) {
-                    const float wf = (j & 1) ? bf16_hi(in.w[h][j >> 1]) : bf16_lo(in.w[h][j >> 1]);
-                    float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[h][j >> 2], j & 3), in.ms) : 0.f;
-                    float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[h][j >> 2], j & 3), in.vs) : 0.f;
-                    opt_moments<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
-                    if constexpr (Tr::kM)
-                        if ((redo >> j) & 1u) mo[j >> 2] = put_byte(mo[j >> 2], int8_code(mm, nms), j & 3);
-                    if constexpr (Tr::kV)
-                        if ((redo >> (8 + j)) & 1u) vo[j >> 2] = put_byte(vo[j >> 2], int8_code(vv, nvs), j & 3);
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) in.w[h][i] = wo[i];
-        if (ok) {
-            st_v4(a.W + e, in.w[h]);
-            if constexpr (Tr::kM) st_v2(static_cast<int8_t*>(a.m) + e, mo);
-            if constexpr (Tr::kV) st_v2(static_cast<int8_t*>(a.v) + e, vo);
+        if constexpr (Tr::kV) {
+            vo[j >> 2] = put_byte(vo[j >> 2], int8_code_fast(vn[j], cv, exact), j & 3);
+            redo |= exact ? 0u : (0x100u << j);
         }
     }
-    if (ok && (threadIdx.x & 3u) == 0) {
-        if constexpr (Tr::kM) a.m_scales[e_row >> 6] = nms;
-        if constexpr (Tr::kV) a.v_scales[e_row >> 6] = nvs;
+    if (redo != 0u) {
+        // rare: a code next to a rounding boundary, or a scale that is not a normal number: the IEEE
+        // division decides (one branch per 8 elements, not one per code)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if constexpr (Tr::kM)
+                if ((redo >> j) & 1u) mo[j >> 2] = put_byte(mo[j >> 2], int8_code(mn[j], nms), j & 3);
+            if constexpr (Tr::kV)
+                if ((redo >> (8 + j)) & 1u) vo[j >> 2] = put_byte(vo[j >> 2], int8_code(vn[j], nvs), j & 3);
+        }
+    }
+    if (ok) {
+        st_v4(a.W + e, wo);
+        if constexpr (Tr::kM) st_v2(static_cast<int8_t*>(a.m) + e, mo);
+        if constexpr (Tr::kV) st_v2(static_cast<int8_t*>(a.v) + e, vo);
+        if ((threadIdx.x & 7u) == 0) {
+            if constexpr (Tr::kM) a.m_scales[e >> 6] = nms;
+            if constexpr (Tr::kV) a.v_scales[e >> 6] = nvs;
+        }
     }
 }
 
@@ -535,37 +509,42 @@ template <int OPT, int WIDTH, bool SCALE, bool PREFETCH>
 __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int col0, uint32_t taddr,
                                              uint8_t* strip) {
     static_assert(WIDTH % 64 == 0, "whole quantisation blocks");
-    const int lane = threadIdx.x & 31;
-    const int row = row0 + (lane >> 2);
-    const size_t lane_base = static_cast<size_t>(row) * a.d_in + col0 + 8 * (lane & 3);
-    const size_t row_step = static_cast<size_t>(8) * a.d_in;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t q = lane & 7u, rsub = lane >> 3;  // column run (8 columns) and first row of this lane
+    const uint8_t* half = strip + (q >> 2) * 4096;    // the 32-column strip holding the run
+    const int row = row0 + static_cast<int>(rsub);
 #pragma unroll 1
     for (int c = 0; c < WIDTH; c += 64) {
         // d_in is a multiple of 64, so a 64-column block lies wholly inside or outside the layer:
         // the same for every lane of the warp
         if (col0 + c >= a.d_in) break;
-        strip_store<SCALE>(taddr + c, strip, a, row0 + lane, col0 + c);
-        strip_store<SCALE>(taddr + c + 32, strip + 4096, a, row0 + lane, col0 + c + 32);
+        strip_store<SCALE>(taddr + c, strip, a, row0 + static_cast<int>(lane), col0 + c);
+        strip_store<SCALE>(taddr + c + 32, strip + 4096, a, row0 + static_cast<int>(lane), col0 + c + 32);
+        const size_t e0 = static_cast<size_t>(row) * a.d_in + col0 + c + 8 * q;
+        const size_t row_step = static_cast<size_t>(4) * a.d_in;
         if constexpr (PREFETCH) {
-            // the next row group's inputs load while this one updates
+            // the next row's inputs load while this one updates
             Int8RowIn<OPT> in[2];
-            int8_row_load<OPT>(a, lane_base + c, row < a.d_out, in[0]);
+            int8_row_load<OPT>(a, e0, row < a.d_out, in[0]);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (k < 3)
-                    int8_row_load<OPT>(a, lane_base + (k + 1) * row_step + c, row + 8 * (k + 1) < a.d_out,
-                                       in[(k + 1) & 1]);
-                int8_row_update<OPT>(a, lane_base + k * row_step + c, row + 8 * k < a.d_out, strip, k, in[k & 1]);
+            for (int k = 0; k < 8; ++k) {
+                if (k < 7) int8_row_load<OPT>(a, e0 + (k + 1) * row_step, row + 4 * (k + 1) < a.d_out, in[(k + 1) & 1]);
+                uint32_t g[8];
+                strip_load_run(half, rsub + 4u * k, q & 3u, g);
+                int8_row_update<OPT>(a, e0 + k * row_step, row + 4 * k < a.d_out, g, in[k & 1]);
             }
         } else {
             // enough warps per scheduler to cover the load latency without a second row in flight
 #pragma unroll 1
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 8; ++k) {
                 Int8RowIn<OPT> in;
-                int8_row_load<OPT>(a, lane_base + k * row_step + c, row + 8 * k < a.d_out, in);
-                int8_row_update<OPT>(a, lane_base + k * row_step + c, row + 8 * k < a.d_out, strip, k, in);
+                int8_row_load<OPT>(a, e0 + k * row_step, row + 4 * k < a.d_out, in);
+                uint32_t g[8];
+                strip_load_run(half, rsub + 4u * k, q & 3u, g);
+                int8_row_update<OPT>(a, e0 + k * row_step, row + 4 * k < a.d_out, g, in);
             }
         }
+        __syncwarp();  // every lane has read the strips before the next block overwrites them
     }
 }
 
@@ -674,8 +653,7 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            const uint64_t keep_a = a.l2_keep_a ? policy_evict_last() : policy_evict_normal();
-            const uint64_t keep_b = a.l2_keep_b ? policy_evict_last() : policy_evict_normal();
+            const uint64_t keep = policy_evict_last();
             for (int tile = first_tile; ok && tile < a.num_tiles; tile += tile_stride) {
                 int mb, nb;
                 tile_coords(tile, a.order, mb, nb);
@@ -702,23 +680,23 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
                             // the stage (64 token rows at j * 8 KiB)
 #pragma unroll
                             for (int j = 0; j < 2; ++j)
-                                tma_load_2d_cg<CG>(a_dst + j * 8192, &tmap_dy, bar, row_a, k0 + 64 * j, keep_a);
+                                tma_load_2d_cg<CG>(a_dst + j * 8192, &tmap_dy, bar, row_a, k0 + 64 * j, keep);
 #pragma unroll
                             for (int j = 0; j < C::kBLoad / 128; ++j)
 #pragma unroll
                                 for (int h = 0; h < 2; ++h)
                                     tma_load_2d_cg<CG>(b_dst + j * O::kBlockBytes + h * 8192, &tmap_x, bar,
-                                                       col_b + 128 * j, k0 + 64 * h, keep_b);
+                                                       col_b + 128 * j, k0 + 64 * h, keep);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
                                 const int r = row_a + 64 * j;
                                 tma_load_2d_cg<CG>(a_dst + j * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
-                                                   kAKMajor ? r : k0, keep_a);
+                                                   kAKMajor ? r : k0, keep);
                             }
 #pragma unroll
                             for (int j = 0; j < C::kBLoad / 64; ++j)
-                                tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep_b);
+                                tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep);
                         }
                     }
                     ++n_issued;

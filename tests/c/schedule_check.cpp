@@ -1,6 +1,6 @@
 // Host build of the tile kernel's schedule (backward_optimizer_gb300/csrc/schedule.h), checked on
-// the CPU: every tile order is a bijection onto the tile grid, and schedule_for picks the grouping
-// named on the command line for a few layer shapes (printed for the Python test to compare).
+// the CPU: every tile order is a bijection onto the tile grid; the first tiles of a 20 x 4 grid
+// grouped by 8 rows, and of the same grid grouped by 3 columns, are printed for the Python test.
 #include <cstdio>
 #include <vector>
 
@@ -21,16 +21,15 @@ int main() {
                     }
                 }
     std::printf("bijection_failures %d\n", bad);
-    // (tiles_m, tiles_n, a_block, b_block): pair tiles of the Llama-3.1-8B MLP at T = 4096 and of
-    // Qwen3-14B at T = 8192 (bf16 operands: 256 rows x T tokens x 2 bytes per block)
-    const long long MiB = 1 << 20;
-    struct Case { const char* name; int tm, tn; long long a, b; } cases[] = {
-        {"llama_gate", 56, 16, 2 * MiB, 2 * MiB}, {"llama_down", 16, 56, 2 * MiB, 2 * MiB},
-        {"qwen_q", 20, 20, 4 * MiB, 4 * MiB}, {"qwen_k", 4, 20, 4 * MiB, 4 * MiB},
-        {"qwen_gate", 68, 20, 4 * MiB, 4 * MiB}, {"qwen_down", 20, 68, 4 * MiB, 4 * MiB}};
-    for (const Case& c : cases) {
-        forge::TileOrder o = forge::schedule_for(c.tm, c.tn, c.a, c.b, 48 * MiB);
-        std::printf("%s raster_cols %d group %d\n", c.name, o.raster_cols, o.group);
+    for (int rc = 0; rc < 2; ++rc) {
+        forge::TileOrder o{20, 4, rc ? 3 : 8, rc};
+        std::printf("%s", rc ? "cols3" : "rows8");
+        for (int t : {0, 1, 7, 8, 31, 32, 33, 79}) {
+            int mb, nb;
+            forge::tile_coords(t, o, mb, nb);
+            std::printf(" %d:%d", mb, nb);
+        }
+        std::printf("\n");
     }
     return bad != 0;
 }

@@ -58,8 +58,17 @@ def test_reference_arm_prints_the_contract_line():
     assert line["config"]["workload"].startswith(WORKLOADS["llama8b-mlp"].name)
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["blas_threads"]["threads"] >= 1  # the float64 BLAS the oracle's products run on
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_blas_thread_count_without_threadpoolctl(monkeypatch):
+    """The GPU machine has no threadpoolctl: the count then comes from numpy's OpenBLAS itself."""
+    import sys
+    monkeypatch.setitem(sys.modules, "threadpoolctl", None)
+    got = bench.blas_threads()
+    assert got["threads"] is not None and got["threads"] >= 1 and got["library"] != "unknown"
 
 
 def test_fewer_than_three_warmup_steps_are_refused():

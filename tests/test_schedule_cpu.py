@@ -26,12 +26,12 @@ def test_every_tile_order_is_a_bijection(report):
     assert report["bijection_failures"] == ["0"]
 
 
-@pytest.mark.parametrize("case, raster_cols, group", [
-    # X (the smaller operand) resident: all 16 tile columns per group, tile rows stream past
-    ("llama_gate", 1, 16),
-    # dY resident: all 16 tile rows per group
-    ("llama_down", 0, 16),
-    # equal operands: rows grouped, as many 4 MiB dY blocks as fit in 48 MiB
-    ("qwen_q", 0, 12), ("qwen_k", 0, 4), ("qwen_gate", 1, 12), ("qwen_down", 0, 12)])
-def test_the_smaller_operand_is_kept_resident(report, case, raster_cols, group):
-    assert report[case] == ["raster_cols", str(raster_cols), "group", str(group)]
+def test_groups_of_rows_sweep_one_column_at_a_time(report):
+    # 20 x 4 tiles in groups of 8 rows: tiles 0..7 are rows 0..7 of column 0, tile 8 starts column 1;
+    # the first group ends at tile 31 (row 7, column 3); the last group has the 4 rows 16..19
+    assert report["rows8"] == ["0:0", "1:0", "7:0", "0:1", "7:3", "8:0", "9:0", "19:3"]
+
+
+def test_groups_of_columns_sweep_one_row_at_a_time(report):
+    # the same grid in groups of 3 columns: tiles 0..2 are columns 0..2 of row 0
+    assert report["cols3"] == ["0:0", "0:1", "2:1", "2:2", "10:1", "10:2", "11:0", "19:3"]
