@@ -142,6 +142,28 @@ def hparams_struct(hp: Any = None, **overrides) -> ForgeHparams:
     return ForgeHparams(**{k: float(v) for k, v in vals.items()})
 
 
+_HP_CACHE: dict = {}
+
+
+def _hp_arg(hp: Any):
+    """ctypes reference to the ForgeHparams of `hp`.  Immutable hyperparameter objects whose hash
+    follows their values (a frozen dataclass such as workloads.Hparams, a tuple, None) are converted
+    once and the struct is reused by later calls; anything else (a dict, an object whose fields a
+    schedule may change between steps) is converted on every call.  The library copies what it
+    needs during the call and keeps no pointer."""
+    import dataclasses
+    frozen = hp is None or isinstance(hp, tuple) or (
+        dataclasses.is_dataclass(hp) and not isinstance(hp, type) and hp.__dataclass_params__.frozen)
+    if not frozen:
+        return ctypes.byref(hparams_struct(hp))
+    hs = _HP_CACHE.get(hp)
+    if hs is None:
+        if len(_HP_CACHE) >= 256:
+            _HP_CACHE.clear()
+        hs = _HP_CACHE[hp] = hparams_struct(hp)
+    return ctypes.byref(hs)
+
+
 # ------------------------------------------------------------------ torch-facing wrappers
 
 def _ptr(t) -> Optional[int]:
@@ -216,7 +238,7 @@ def fused_dw_step(dY, X, W, m=None, v=None, qscales=None, opt: str = "adamw", hp
     _state_args(W, m, v, qscales)
     shape = _shape(T, d_out, d_in, _state_of(m, v))
     st = lib().forge_fused_dw_step(_ptr(dY), _ptr(X), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), OPT_KINDS[opt],
-                                   ctypes.byref(hparams_struct(hp)), ctypes.byref(shape), int(step),
+                                   _hp_arg(hp), ctypes.byref(shape), int(step),
                                    int(seed) & (2**64 - 1), _stream(stream))
     _check(st, "forge_fused_dw_step")
 
@@ -261,11 +283,11 @@ def fused_dw_step_e4m3(dY, X, dy_scale, x_scale, W, m=None, v=None, qscales=None
     if _channel_scales(dy_scale, x_scale, d_out, d_in):
         st = lib().forge_fused_dw_step_e4m3_channels(
             _ptr(dY), _ptr(X), _ptr(dy_scale), _ptr(x_scale), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), OPT_KINDS[opt],
-            ctypes.byref(hparams_struct(hp)), ctypes.byref(shape), int(step), int(seed) & (2**64 - 1), _stream(stream))
+            _hp_arg(hp), ctypes.byref(shape), int(step), int(seed) & (2**64 - 1), _stream(stream))
         _check(st, "forge_fused_dw_step_e4m3_channels")
         return
     st = lib().forge_fused_dw_step_e4m3(_ptr(dY), _ptr(X), float(dy_scale), float(x_scale), _ptr(W), _ptr(m),
-                                        _ptr(v), _ptr(qscales), OPT_KINDS[opt], ctypes.byref(hparams_struct(hp)),
+                                        _ptr(v), _ptr(qscales), OPT_KINDS[opt], _hp_arg(hp),
                                         ctypes.byref(shape), int(step), int(seed) & (2**64 - 1), _stream(stream))
     _check(st, "forge_fused_dw_step_e4m3")
 
@@ -311,7 +333,7 @@ def linear_backward(dY, X, W, m=None, v=None, qscales=None, dX=None, opt: str = 
     _state_args(W, m, v, qscales)
     shape = _shape(T, d_out, d_in, _state_of(m, v))
     st = lib().forge_linear_backward(_ptr(dY), _ptr(X), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), _ptr(dX),
-                                     OPT_KINDS[opt], ctypes.byref(hparams_struct(hp)), ctypes.byref(shape),
+                                     OPT_KINDS[opt], _hp_arg(hp), ctypes.byref(shape),
                                      int(step), int(seed) & (2**64 - 1), _stream(stream))
     _check(st, "forge_linear_backward")
 
@@ -326,7 +348,7 @@ def opt_step(dW, W, m=None, v=None, qscales=None, opt: str = "adamw", hp: Any = 
     _state_args(W, m, v, qscales)
     shape = _shape(0, d_out, d_in, _state_of(m, v))
     st = lib().forge_opt_step(_ptr(dW), _ptr(W), _ptr(m), _ptr(v), _ptr(qscales), OPT_KINDS[opt],
-                              ctypes.byref(hparams_struct(hp)), ctypes.byref(shape), int(step),
+                              _hp_arg(hp), ctypes.byref(shape), int(step),
                               int(seed) & (2**64 - 1), _stream(stream))
     _check(st, "forge_opt_step")
 

@@ -160,7 +160,7 @@ OptScalars derive_scalars(forge_opt_kind k, const forge_hparams& hp, int64_t ste
     return s;
 }
 
-forge_status make_operand_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, bool e4m3 = false) {
+forge_status encode_operand_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, bool e4m3) {
     // A [rows, cols] row-major operand, bf16 or E4M3, read in boxes of 64 rows whose rows are
     // exactly one 128-byte swizzle span (64 bf16 or 128 E4M3 columns).
     const int64_t esize = e4m3 ? 1 : 2;
@@ -173,6 +173,46 @@ forge_status make_operand_map(CUtensorMap* map, const void* base, int64_t cols, 
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FORGE_OK : FORGE_ERR_CUDA;
+}
+
+// Encoded tensor maps of recent calls, per host thread.  A training loop passes the same buffers
+// with the same shapes every step, and encoding a map costs host time comparable to a small layer's
+// whole kernel.  A map is plain host data determined by (base, cols, rows, element type), handed to
+// the kernel by value, so a cached one is exactly the one a new encoding would give, whatever
+// happened to the buffer in between.
+struct MapKey {
+    const void* base;
+    int64_t cols, rows;
+    bool e4m3;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && cols == o.cols && rows == o.rows && e4m3 == o.e4m3;
+    }
+};
+struct MapSlot {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+};
+constexpr int kMapSlots = 64;
+thread_local MapSlot t_maps[kMapSlots];
+
+forge_status make_operand_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, bool e4m3 = false) {
+    const MapKey key{base, cols, rows, e4m3};
+    uint64_t h = reinterpret_cast<uintptr_t>(base) * 0x9E3779B97F4A7C15ull;
+    h ^= static_cast<uint64_t>(cols) * 0xC2B2AE3D27D4EB4Full ^ static_cast<uint64_t>(rows) * 0x165667B19E3779F9ull;
+    h ^= e4m3 ? 0x27D4EB2F165667C5ull : 0;
+    MapSlot& slot = t_maps[(h >> 32) % kMapSlots];
+    if (slot.used && slot.key == key) {
+        *map = slot.map;
+        return FORGE_OK;
+    }
+    forge_status st = encode_operand_map(map, base, cols, rows, e4m3);
+    if (st == FORGE_OK) {
+        slot.key = key;
+        slot.map = *map;
+        slot.used = true;
+    }
+    return st;
 }
 
 // Sizes: any T >= 0 (the last 64-token slice is zero-filled past T); d_out and d_in multiples of 8,
@@ -235,7 +275,10 @@ using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
 template <int OPT, int BN, int CL, int OPS>
 TileFn tile_fn_state(int state) {
     using namespace forge;
-    if (state == FORGE_STATE_INT8_B64) return launch_tile<OPT, kEpiOptINT8, BN, CL, OPS>;
+    if (state == FORGE_STATE_INT8_B64) {
+        if constexpr (BN == 64) return nullptr;  // INT8 blocks need 64 columns per epilogue warp
+        else return launch_tile<OPT, kEpiOptINT8, BN, CL, OPS>;
+    }
     if (state == FORGE_STATE_BF16) return launch_tile<OPT, kEpiOptBF16, BN, CL, OPS>;
     return launch_tile<OPT, kEpiOptFP32, BN, CL, OPS>;
 }
@@ -261,7 +304,9 @@ TileFn tile_fn_v(forge_opt_kind k, int state) {
 // 128 x 256, one CTA on 128 x 128; each is a group of the method's 128 x 128 tiles side by side.
 // A layer whose preferred shape would run on at most half the SMs takes 128 x 128 tiles instead:
 // there the number of SMs sharing the epilogue matters more than the mainloop's efficiency
-// (measured on 1024^2 and 1536^2 layers at T = 4096: 21-25 % faster).
+// (measured on 1024^2 and 1536^2 layers at T = 4096: 21-25 % faster).  If even those would run on
+// at most half the SMs, calls that allow it (bf16 operands, an epilogue that works on 32-column
+// runs: not INT8 states) take 128 x 64 tiles, twice as many CTAs again.
 struct TileShape {
     int bn;     // columns per CTA pair (or per CTA)
     int cg;     // CTAs per MMA = CTAs per cluster
@@ -271,21 +316,28 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // rows x cols of the output (dW: d_out x d_in; dX: T x d_in).  A ragged dimension (not a multiple
 // of the tile) takes the wide shape once it is large enough that the zero-filled tail costs little
 // (over 1024).
-TileShape pick_tiles(int64_t rows, int64_t cols, int num_sms) {
+TileShape pick_tiles(int64_t rows, int64_t cols, int num_sms, bool narrow_ok) {
     const bool rows256 = rows % 256 == 0 || (rows % 128 != 0 && rows > 1024);
     const bool cols256 = cols % 256 == 0 || (cols % 128 != 0 && cols > 1024);
+    auto ctas = [&](TileShape t) { return ceil_div(rows, 128 * t.cg) * ceil_div(cols, t.bn) * t.cg; };
     TileShape t{128, 1};
     if (rows256 && cols256) t = {256, 2};
     else if (cols256) t = {256, 1};
-    const int64_t ctas = ceil_div(rows, 128 * t.cg) * ceil_div(cols, t.bn) * t.cg;
-    if (2 * ctas <= num_sms) return {128, 1};
+    if (2 * ctas(t) > num_sms) return t;
+    t = {128, 1};
+    if (narrow_ok && 2 * ctas(t) <= num_sms) return {64, 1};
     return t;
 }
 
-TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t /*T*/, int num_sms) { return pick_tiles(d_out, d_in, num_sms); }
+// narrow_ok: bf16 operands and binary32 or bfloat16 states (or the dW GEMM alone)
+TileShape pick_shape(int64_t d_out, int64_t d_in, int64_t /*T*/, int num_sms, bool narrow_ok) {
+    return pick_tiles(d_out, d_in, num_sms, narrow_ok);
+}
 
 // Input gradient dX = dY W: tile rows are tokens (M = T), columns d_in (N), reduction over d_out (K).
-TileShape pick_dx_shape(int64_t T, int64_t /*d_out*/, int64_t d_in, int num_sms) { return pick_tiles(T, d_in, num_sms); }
+TileShape pick_dx_shape(int64_t T, int64_t /*d_out*/, int64_t d_in, int num_sms) {
+    return pick_tiles(T, d_in, num_sms, true);
+}
 
 template <int OPS>
 TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t) {
@@ -293,13 +345,22 @@ TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t) {
     if (epi == kEpiDX) {
         if constexpr (OPS != kOpsBF16) return nullptr;
         if (t.cg == 2) return launch_tile<0, kEpiDX, 256, 2, kOpsBF16>;
+        if (t.bn == 64) return launch_tile<0, kEpiDX, 64, 1, kOpsBF16>;
         return t.bn == 256 ? launch_tile<0, kEpiDX, 256, 1, kOpsBF16> : launch_tile<0, kEpiDX, 128, 1, kOpsBF16>;
     }
     if (epi == kEpiStoreGrad) {
         if (t.cg == 2) return launch_tile<0, kEpiStoreGrad, 256, 2, OPS>;
+        if (t.bn == 64) {
+            if constexpr (OPS != kOpsBF16) return nullptr;
+            else return launch_tile<0, kEpiStoreGrad, 64, 1, kOpsBF16>;
+        }
         return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1, OPS> : launch_tile<0, kEpiStoreGrad, 128, 1, OPS>;
     }
     if (t.cg == 2) return tile_fn_v<256, 2, OPS>(k, state);
+    if (t.bn == 64) {
+        if constexpr (OPS != kOpsBF16) return nullptr;
+        else return state == FORGE_STATE_INT8_B64 ? nullptr : tile_fn_v<64, 1, OPS>(k, state);
+    }
     return t.bn == 256 ? tile_fn_v<256, 1, OPS>(k, state) : tile_fn_v<128, 1, OPS>(k, state);
 }
 
@@ -367,7 +428,9 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.d_out = static_cast<int>(shape->d_out);
     a.d_in = static_cast<int>(shape->d_in);
     a.T = static_cast<int>(shape->T);
-    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T, dev.num_sms);
+    // 128 x 64 tiles need bf16 operands and an epilogue on 32-column runs (not INT8 states)
+    const bool narrow_ok = !e4m3 && (epi == forge::kEpiStoreGrad || shape->state != FORGE_STATE_INT8_B64);
+    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T, dev.num_sms, narrow_ok);
     const int tiles_m = static_cast<int>(ceil_div(a.d_out, forge::kBM * ts.cg));
     const int tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn));
     a.num_tiles = tiles_m * tiles_n;
@@ -675,7 +738,8 @@ forge_status forge_launch_shape(const forge_shape* shape, int32_t* tile_rows, in
     DeviceInfo* dev = nullptr;
     st = device_info(&dev);
     if (st != FORGE_OK) return st;
-    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T, dev->num_sms);
+    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T, dev->num_sms,
+                                    shape->state != FORGE_STATE_INT8_B64);
     *tile_rows = forge::kBM * ts.cg;
     *tile_cols = ts.bn;
     *cluster = ts.cg;

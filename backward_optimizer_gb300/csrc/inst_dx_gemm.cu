@@ -2,3 +2,4 @@
 #include "instantiate.cuh"
 
 FORGE_INSTANTIATE_TILES(0, forge::kEpiDX)
+FORGE_INSTANTIATE_NARROW(0, forge::kEpiDX)

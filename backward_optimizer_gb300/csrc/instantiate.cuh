@@ -92,6 +92,10 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
     template cudaError_t forge::launch_tile<OPT, EPI, 256, 1, OPS>(const forge::TileLaunch&);       \
     template cudaError_t forge::launch_tile<OPT, EPI, 256, 2, OPS>(const forge::TileLaunch&);
 
+// 128 x 64 tiles for small layers: bf16 operands, every epilogue but the INT8 one.
+#define FORGE_INSTANTIATE_NARROW(OPT, EPI) \
+    template cudaError_t forge::launch_tile<OPT, EPI, 64, 1, forge::kOpsBF16>(const forge::TileLaunch&);
+
 #define FORGE_INSTANTIATE_TILES(OPT, EPI) FORGE_INSTANTIATE_TILES_OPS(OPT, EPI, forge::kOpsBF16)
 
 // E4M3 operands, every state format.
@@ -102,6 +106,7 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 
 #define FORGE_INSTANTIATE_OPT(OPT)                    \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptFP32) \
+    FORGE_INSTANTIATE_NARROW(OPT, forge::kEpiOptFP32) \
     template cudaError_t forge::launch_opt<OPT, 0>(const forge::OptArgs&, int, cudaStream_t);
 
 #define FORGE_INSTANTIATE_OPT_INT8(OPT)               \
@@ -110,4 +115,5 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 
 #define FORGE_INSTANTIATE_OPT_BF16(OPT)               \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptBF16) \
+    FORGE_INSTANTIATE_NARROW(OPT, forge::kEpiOptBF16) \
     template cudaError_t forge::launch_opt<OPT, 2>(const forge::OptArgs&, int, cudaStream_t);

@@ -164,25 +164,58 @@ __device__ __forceinline__ uint32_t put_byte(uint32_t word, uint32_t c, int k) {
 // g: binary32 gradient; w: binary32 weight (from bfloat16); m, v: binary32 moments, updated
 // in place.  Returns the new binary32 weight.  Intrinsics fix each rounding so that the
 // kernel's result does not depend on the compiler's contraction choices.
+//
+// APPROX selects how the weight step divides and takes square roots: the IEEE-rounded
+// operations, or the hardware approximations (sqrt.approx.f32, div.approx.f32: a few units in
+// the last place, no slow-path branches).  The moments never depend on it.  Epilogues bound by
+// the memory system (binary32 and bfloat16 states) take the approximations, which measured
+// 1-7 % faster there; the INT8-state epilogue, bound by its own instruction issue, measured
+// faster with the IEEE forms.  The fused and the two-phase kernel of one state format always
+// take the same forms, so they agree bit for bit.
 
-template <int OPT>
+__device__ __forceinline__ float sqrt_approx(float x) {
+    float r;
+    asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float div_approx(float a, float b) {
+    float r;
+    asm("div.approx.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+template <bool APPROX>
+__device__ __forceinline__ float step_sqrt(float x) {
+    if constexpr (APPROX) return sqrt_approx(x);
+    else return __fsqrt_rn(x);
+}
+
+// a / b for the weight step; b >= eps > 0 and below 2^126 there (b = sqrt(v) c + eps, v finite)
+template <bool APPROX>
+__device__ __forceinline__ float step_div(float a, float b) {
+    if constexpr (APPROX) return div_approx(a, b);
+    else return __fdiv_rn(a, b);
+}
+
+template <int OPT, bool APPROX = false>
 __device__ __forceinline__ float opt_update(float g, float w, float& m, float& v, const OptScalars& s) {
     if constexpr (OPT == kAdamW) {
         m = __fmaf_rn(s.b1, m, __fmul_rn(s.omb1, g));
         v = __fmaf_rn(s.b2, v, __fmul_rn(s.omb2, __fmul_rn(g, g)));
-        const float denom = __fmaf_rn(__fsqrt_rn(v), s.inv_sqrt_bc2, s.eps);
-        return __fmaf_rn(-s.step_size, __fdiv_rn(m, denom), __fmul_rn(w, s.decay));
+        const float denom = __fmaf_rn(step_sqrt<APPROX>(v), s.inv_sqrt_bc2, s.eps);
+        return __fmaf_rn(-s.step_size, step_div<APPROX>(m, denom), __fmul_rn(w, s.decay));
     } else if constexpr (OPT == kNAdam) {
         const float gc = __fmaf_rn(s.wd, w, g);
         m = __fmaf_rn(s.b1, m, __fmul_rn(s.omb1, gc));
         v = __fmaf_rn(s.b2, v, __fmul_rn(s.omb2, __fmul_rn(gc, gc)));
-        const float denom = __fmaf_rn(__fsqrt_rn(v), s.inv_sqrt_bc2, s.eps);
-        return __fsub_rn(w, __fdiv_rn(__fmaf_rn(s.c_g, gc, __fmul_rn(s.c_m, m)), denom));
+        const float denom = __fmaf_rn(step_sqrt<APPROX>(v), s.inv_sqrt_bc2, s.eps);
+        return __fsub_rn(w, step_div<APPROX>(__fmaf_rn(s.c_g, gc, __fmul_rn(s.c_m, m)), denom));
     } else if constexpr (OPT == kRAdam) {
         const float gc = __fmaf_rn(s.wd, w, g);
         m = __fmaf_rn(s.b1, m, __fmul_rn(s.omb1, gc));
         v = __fmaf_rn(s.b2, v, __fmul_rn(s.omb2, __fmul_rn(gc, gc)));
-        if (s.rectified) return __fmaf_rn(-s.step_size, __fdiv_rn(m, __fadd_rn(__fsqrt_rn(v), s.eps)), w);
+        if (s.rectified) return __fmaf_rn(-s.step_size, step_div<APPROX>(m, __fadd_rn(step_sqrt<APPROX>(v), s.eps)), w);
         return __fmaf_rn(-s.step_size, m, w);
     } else if constexpr (OPT == kLion) {
         const float c = __fmaf_rn(s.b1, m, __fmul_rn(s.omb1, g));
@@ -192,11 +225,11 @@ __device__ __forceinline__ float opt_update(float g, float w, float& m, float& v
     } else if constexpr (OPT == kRMSprop) {
         const float gc = __fmaf_rn(s.wd, w, g);
         v = __fmaf_rn(s.b2, v, __fmul_rn(s.omb2, __fmul_rn(gc, gc)));
-        return __fmaf_rn(-s.lr, __fdiv_rn(gc, __fadd_rn(__fsqrt_rn(v), s.eps)), w);
+        return __fmaf_rn(-s.lr, step_div<APPROX>(gc, __fadd_rn(step_sqrt<APPROX>(v), s.eps)), w);
     } else if constexpr (OPT == kAdaGrad) {
         const float gc = __fmaf_rn(s.wd, w, g);
         v = __fmaf_rn(gc, gc, v);
-        return __fmaf_rn(-s.lr, __fdiv_rn(gc, __fadd_rn(__fsqrt_rn(v), s.eps)), w);
+        return __fmaf_rn(-s.lr, step_div<APPROX>(gc, __fadd_rn(step_sqrt<APPROX>(v), s.eps)), w);
     } else if constexpr (OPT == kSGD) {
         return __fmaf_rn(-s.lr, __fmaf_rn(s.wd, w, g), w);
     } else {  // kSGDMomentum

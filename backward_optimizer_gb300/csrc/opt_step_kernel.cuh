@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(256) forge_opt_kernel(const OptArgs a) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float wf = (j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]);
-            wn[j] = opt_update<OPT>(__uint_as_float(g[j]), wf, mf[j], vf[j], a.s);
+            wn[j] = opt_update<OPT, !INT8>(__uint_as_float(g[j]), wf, mf[j], vf[j], a.s);  // the fused kernel's forms
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k)

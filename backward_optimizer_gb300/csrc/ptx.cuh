@@ -107,6 +107,13 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive without ordering any memory access (relaxed, cluster scope), for signals that only order
+// tcgen05 operations, which the tcgen05 fences around the barrier already do.  A release arrive
+// would also wait for the thread's earlier global stores to be performed.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

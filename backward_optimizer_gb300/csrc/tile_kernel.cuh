@@ -60,7 +60,10 @@ struct OperandTraits {
 
 template <int BN, int CG, int EPI, int OPS = kOpsBF16>
 struct TileCfg {
-    static_assert(BN == 128 || BN == 256, "tile width");
+    // 64-column tiles (one X box per stage, N = 64 MMAs) serve small layers with bf16 operands and
+    // epilogues that work on 32-column runs; E4M3 rows hold 128 elements, INT8 blocks 64 per warp
+    static_assert(BN == 128 || BN == 256 || (BN == 64 && CG == 1 && OPS == kOpsBF16 && EPI != kEpiOptINT8),
+                  "tile width");
     static_assert(CG == 1 || CG == 2, "CTA group");
     static constexpr int kBLoad = BN / CG;         // X columns staged by this CTA
     static constexpr int kABytes = kBM * kBK * 2;  // one stage of A: 2 boxes of 64 x 64 (dY^T, or dY for dX)
@@ -340,8 +343,8 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                         if constexpr (Tr::kM) { m0 = __uint_as_float(m[r][j]); m1 = __uint_as_float(m[r][j + 1]); }
                         if constexpr (Tr::kV) { v0 = __uint_as_float(v[r][j]); v1 = __uint_as_float(v[r][j + 1]); }
                     }
-                    const float w0 = opt_update<OPT>(__uint_as_float(g[j]), bf16_lo(wp), m0, v0, a.s);
-                    const float w1 = opt_update<OPT>(__uint_as_float(g[j + 1]), bf16_hi(wp), m1, v1, a.s);
+                    const float w0 = opt_update<OPT, true>(__uint_as_float(g[j]), bf16_lo(wp), m0, v0, a.s);
+                    const float w1 = opt_update<OPT, true>(__uint_as_float(g[j + 1]), bf16_hi(wp), m1, v1, a.s);
                     w[r][j >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
                     if constexpr (BF16S) {
                         if constexpr (Tr::kM) m[r][j >> 1] = sr_bf16(m0, sr_r16(pm, j)) | (sr_bf16(m1, sr_r16(pm, j + 1)) << 16);
@@ -361,6 +364,31 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                         if constexpr (Tr::kV) st_v8(static_cast<float*>(a.v) + e, v[r]);
                     }
                 }
+            }
+        }
+    }
+}
+
+// Before the first tile's accumulator is ready: bring the W/m/v of the warp's first 32-column run
+// into L2, so that the epilogue's first loads wait on L2 while the mainloop runs.  Later runs are
+// prefetched by epi_opt_dense itself, one run ahead.
+template <int OPT, bool BF16S>
+__device__ __forceinline__ void prefetch_first_run(const TileArgs& a, int row0, int col0) {
+    using Tr = OptTraits<OPT>;
+    const int lane = threadIdx.x & 31;
+    const int col = col0 + 8 * (lane & 3);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int row = row0 + (lane >> 2) + 8 * k;
+        if (row < a.d_out && col < a.d_in) {
+            const size_t e = static_cast<size_t>(row) * a.d_in + col;
+            prefetch_l2(a.W + e);
+            if constexpr (BF16S) {
+                if constexpr (Tr::kM) prefetch_l2(static_cast<uint16_t*>(a.m) + e);
+                if constexpr (Tr::kV) prefetch_l2(static_cast<uint16_t*>(a.v) + e);
+            } else {
+                if constexpr (Tr::kM) prefetch_l2(static_cast<float*>(a.m) + e);
+                if constexpr (Tr::kV) prefetch_l2(static_cast<float*>(a.v) + e);
             }
         }
     }
@@ -454,7 +482,7 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e, boo
         const float wf = (j & 1) ? bf16_hi(in.w[j >> 1]) : bf16_lo(in.w[j >> 1]);
         float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[j >> 2], j & 3), in.ms) : 0.f;
         float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[j >> 2], j & 3), in.vs) : 0.f;
-        const float wn = opt_update<OPT>(__uint_as_float(g[j]), wf, mm, vv, a.s);
+        const float wn = opt_update<OPT, false>(__uint_as_float(g[j]), wf, mm, vv, a.s);
         const uint32_t b = sr_bf16(wn, sr_r16(p, j));
         wo[j >> 1] = (j & 1) ? (wo[j >> 1] | (b << 16)) : b;
         mn[j] = mm;
@@ -766,6 +794,14 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
         constexpr int kWidth = BN / (C::kEpiWarps / 4);
         // the wait for a finished accumulator spans a whole tile mainloop, which grows with T
         const AbortCtx ab_acc{abort_flag, a.status, a.acc_wait_limit_ns};
+        if constexpr (EPI == kEpiOptFP32 || EPI == kEpiOptBF16) {
+            if (first_tile < a.num_tiles) {
+                int mb, nb;
+                tile_coords(first_tile, a.order, mb, nb);
+                prefetch_first_run<OPT, EPI == kEpiOptBF16>(
+                    a, mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32, nb * BN + half * kWidth);
+            }
+        }
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = first_tile; tile < a.num_tiles; tile += tile_stride) {
@@ -795,12 +831,12 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
                     a, row0, col0, taddr, strip, row0n, col0n);
             }
             else epi_opt_int8<OPT, kWidth, kScale, C::kEpiWarps == 8>(a, row0, col0, taddr, strip);
+            // the buffer's TMEM columns may be overwritten once every lane's reads of them have
+            // completed (tcgen05.wait::ld) and been ordered before the arrive (tcgen05 fence); the
+            // arrive publishes no memory, so it is relaxed
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                if constexpr (CG == 2) mbar_arrive_remote(map_to_rank(smem_addr(&acc_empty[acc]), 0));
-                else mbar_arrive(&acc_empty[acc]);
-            }
+            if (lane == 0) mbar_arrive_relaxed(map_to_rank(smem_addr(&acc_empty[acc]), 0));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }

@@ -135,6 +135,24 @@ def algorithmic_bytes(wl, opt: str, state: str, operands: str) -> int:
     return int(sum(l.d_out * l.d_in * per_el + wl.T * (l.d_out + l.d_in) * op for l in wl.layers))
 
 
+def roofline_entry(flops, alg_bytes, launch_ms, tensor_peak, hbm_peak, traffic, hbm, tensor_src, hbm_src):
+    """The fused kernel's roofline: the bound is the unit whose time at its peak is longer for the
+    launch's algorithmic work -- the tensor core for its flops (TFLOP/s) or HBM for its bytes (GB/s)
+    -- and `achieved` is that work over the measured launch time.  The other side is kept as
+    `other` (frac of its own peak) so both can be read."""
+    secs = launch_ms * 1e-3
+    t_tensor = flops / (tensor_peak * 1e12)
+    t_hbm = alg_bytes / (hbm_peak * 1e9)
+    tensor = {"achieved": flops / secs / 1e12, "peak": tensor_peak, "unit": "TFLOP/s",
+              "frac": flops / secs / 1e12 / tensor_peak, "peak_source": tensor_src}
+    mem = {"achieved": alg_bytes / secs / 1e9, "peak": hbm_peak, "unit": "GB/s",
+           "frac": alg_bytes / secs / 1e9 / hbm_peak, "peak_source": hbm_src}
+    bound, main, other = ("tensor", tensor, mem) if t_tensor >= t_hbm else ("hbm", mem, tensor)
+    return {"bound": bound, **main, "traffic": traffic, "hbm": hbm, "kernel": "forge_tile_kernel (fused)",
+            "avg_launch_ms": launch_ms, "flops_per_launch": flops, "bytes_per_launch": alg_bytes,
+            "other": dict(other, bound="tensor" if bound == "hbm" else "hbm")}
+
+
 def max_over_ranks(values, world: int, device="cpu"):
     """Element-wise maximum of per-rank timings (the slowest rank defines the job's time).  The
     only collective of the benchmark besides barriers; no data of the path is exchanged."""
@@ -234,8 +252,6 @@ def run_gpu(args, rank, world):
     status = fg.sync_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
-    per_launch = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in layers] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = fg.launch_count()
     barrier()
@@ -243,16 +259,33 @@ def run_gpu(args, rank, world):
     with ClockSampler(torch.cuda.current_device()) as clocks:
         start.record(stream)
         for k in range(args.steps):
-            fused_pass(per_launch[k])
+            fused_pass()
         stop.record(stream)
         torch.cuda.synchronize()
     barrier()
     launches = fg.launch_count() - launches0
     elapsed_ms = start.elapsed_time(stop)
-    launch_ms = [a.elapsed_time(b) for step_ev in per_launch for (a, b) in step_ev]
     status = fg.sync_status()
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
+    # the same K steps again with an event pair around every launch, for the kernel's average
+    # launch duration (the roofline).  Kept out of the step timing: recording two events per launch
+    # costs host time that a small layer's launch does not hide.
+    per_launch = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in layers] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for k in range(args.steps):
+        fused_pass(per_launch[k])
+    l1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launch_ms = [a.elapsed_time(b) for step_ev in per_launch for (a, b) in step_ev]
+    launch_pass_ms = l0.elapsed_time(l1) / args.steps
+    if fg.sync_status() != 0:
+        raise RuntimeError("device status in the per-launch timing")
 
     # ---- the same fused pass captured once in a CUDA graph and replayed: no host launch path per
     # layer (it matters only for small layers, whose kernels are shorter than a launch)
@@ -284,14 +317,15 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     mem0 = torch.cuda.memory_allocated()
 
-    def unfused_pass():
+    def unfused_pass(on=None):
+        on = stream if on is None else on
         for L, dW in zip(layers, dws):
             if e4m3:
-                fg.dw_gemm_e4m3(L["dy"], L["x"], L["s_dy"], L["s_x"], dW, stream=stream)
+                fg.dw_gemm_e4m3(L["dy"], L["x"], L["s_dy"], L["s_x"], dW, stream=on)
             else:
-                fg.dw_gemm(L["dy"], L["x"], dW, stream=stream)
+                fg.dw_gemm(L["dy"], L["x"], dW, stream=on)
         for i, (L, dW) in enumerate(zip(layers, dws)):
-            fg.opt_step(dW, L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step, seed=0x5EED + i, stream=stream)
+            fg.opt_step(dW, L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step, seed=0x5EED + i, stream=on)
 
     for _ in range(args.warmup):
         unfused_pass()
@@ -304,6 +338,24 @@ def run_gpu(args, rank, world):
     u1.record(stream)
     torch.cuda.synchronize()
     unfused_ms = u0.elapsed_time(u1) / args.steps
+    # the two-phase pass from a CUDA graph too, beside the fused pass's graph: for small layers,
+    # whose kernels are shorter than a launch, the two differ most there
+    ugraph = torch.cuda.CUDAGraph()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side), torch.cuda.graph(ugraph):
+        unfused_pass(on=torch.cuda.current_stream())
+    stream.wait_stream(side)
+    for _ in range(args.warmup):
+        ugraph.replay()
+    barrier()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(args.steps):
+        ugraph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    unfused_graph_ms = g0.elapsed_time(g1) / args.steps
+    del ugraph
     grad_pool_unfused = sum(d.numel() * 4 for d in dws)
     del dws
     torch.cuda.synchronize()
@@ -404,12 +456,13 @@ def run_gpu(args, rank, world):
         raise RuntimeError(f"device status {status} in the dX / backward timing")
     del dxs
 
-    elapsed_ms, unfused_ms, e2e_ms, dx_ms, bwd_ms, graph_ms = max_over_ranks(
-        [elapsed_ms, unfused_ms, e2e_ms, timed["dx"], timed["backward"], graph_ms], world, dev)
+    elapsed_ms, unfused_ms, e2e_ms, dx_ms, bwd_ms, graph_ms, unfused_graph_ms = max_over_ranks(
+        [elapsed_ms, unfused_ms, e2e_ms, timed["dx"], timed["backward"], graph_ms, unfused_graph_ms], world, dev)
     ms_step = elapsed_ms / args.steps
     return dict(ms_step=ms_step, flops_step=flops_step, launch_ms=launch_ms, launches=launches,
                 unfused_ms=unfused_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks.summary(),
                 grad_pool_unfused=grad_pool_unfused, mem_fused=mem0, wl=wl, dx_ms=dx_ms, bwd_ms=bwd_ms, graph_ms=graph_ms,
+                launch_pass_ms=launch_pass_ms, unfused_graph_ms=unfused_graph_ms,
                 dx_launch_ms=dx_launch_ms)
 
 
@@ -662,7 +715,9 @@ def main():
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16", "data": "synthetic", "config": config,
         "unfused": {"ms_per_step": r["unfused_ms"], "value": job_throughput(r["flops_step"], world, r["unfused_ms"]),
-                    "speedup_fused": r["unfused_ms"] / r["ms_step"]},
+                    "speedup_fused": r["unfused_ms"] / r["ms_step"],
+                    "graph_ms_per_step": r["unfused_graph_ms"],
+                    "graph_speedup_fused": r["unfused_graph_ms"] / r["graph_ms"]},
         "grad_pool_bytes": {"fused_hbm": 0, "unfused_hbm": r["grad_pool_unfused"],
                             "fused_on_chip": "two FP32 accumulators per SM in TMEM (at most 2 x 128x256 = 256 KiB), independent of model size"},
         "e2e": {"value": job_throughput(r["flops_step"], world, r["e2e_ms"]), "unit": "TFLOP/s",
@@ -670,10 +725,10 @@ def main():
         "gpu_launches": r["launches"],
         "graph": {"ms_per_step": r["graph_ms"], "value": job_throughput(r["flops_step"], world, r["graph_ms"]),
                   "unit": "TFLOP/s", "what": "the fused pass captured once in a CUDA graph and replayed"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic, "hbm": hbm,
-                     "kernel": "forge_tile_kernel (fused)", "avg_launch_ms": avg_launch_ms,
-                     "flops_per_launch": flops_launch, "peak_source": peak_source},
+        "roofline": dict(roofline_entry(flops_launch, alg_bytes, avg_launch_ms, peak, hbm_peak, traffic, hbm,
+                                        peak_source, f"hbm_gbs of {peaks_src}"),
+                         launch_timing=f"CUDA events around each launch on its stream, over {args.steps} steps timed "
+                                       f"again after the step timing ({r['launch_pass_ms']:.4f} ms per step there)"),
         "clocks": r["clocks"],
         # the layer's input gradient dX = dY W (same flops as dW) and the ordered layer backward
     }

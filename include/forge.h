@@ -269,12 +269,14 @@ FORGE_API void forge_set_wait_limit_ns(uint64_t ns);
  * CUDA context stays usable.  The outputs of that one call are unspecified.  No fault is raised. */
 FORGE_API void forge_debug_withhold_next_stage(void);
 
-/* The tile shape and persistent grid forge_fused_dw_step (and forge_dw_gemm) use for `shape`:
- * rows x columns of W per tile (a group of the method's 128 x 128 tiles, §2 Methodology: 256 x 256
- * on a CTA pair, 128 x 256 or 128 x 128 on one CTA; a layer whose wider shape would occupy at most
- * half the SMs takes 128 x 128), CTAs per thread-block cluster (1 or 2), and CTAs launched on the
- * current device.  Host-side query, no launch; it reads the device's SM count, so it needs a
- * device (FORGE_ERR_CUDA or FORGE_ERR_NOT_SM103 otherwise). */
+/* The tile shape and persistent grid forge_fused_dw_step (and forge_dw_gemm) use for `shape` with
+ * bf16 operands: rows x columns of W per tile (256 x 256 on a CTA pair, a group of the method's
+ * 128 x 128 tiles, §2 Methodology; 128 x 256 or 128 x 128 on one CTA; a layer whose wider shape
+ * would occupy at most half the SMs takes 128 x 128, and if those would too, 128 x 64 -- half of
+ * one of the method's tiles -- except with INT8 states), CTAs per thread-block cluster (1 or 2),
+ * and CTAs launched on the current device.  E4M3 operands never take 128 x 64 tiles: where the
+ * query answers 128 x 64 they run on 128 x 128.  Host-side query, no launch; it reads the
+ * device's SM count, so it needs a device (FORGE_ERR_CUDA or FORGE_ERR_NOT_SM103 otherwise). */
 FORGE_API forge_status forge_launch_shape(const forge_shape *shape, int32_t *tile_rows, int32_t *tile_cols,
                                           int32_t *cluster, int32_t *ctas);
 

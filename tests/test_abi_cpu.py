@@ -231,3 +231,21 @@ def test_header_compiles_as_c_and_a_c_program_links(L, tmp_path):
                     f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
+def test_hyperparameter_struct_follows_a_mutable_object():
+    """A schedule that changes the fields of its hyperparameter object between steps is seen on the
+    next call; immutable objects (workloads.Hparams) are converted once and reused."""
+    import backward_optimizer_gb300 as fg
+    from workloads import Hparams
+
+    class Schedule:
+        lr = 1e-3
+        weight_decay = 0.0
+    hp = Schedule()
+    assert fg._hp_arg(hp)._obj.lr == pytest.approx(1e-3)
+    hp.lr = 5e-2
+    assert fg._hp_arg(hp)._obj.lr == pytest.approx(5e-2)
+    frozen = Hparams(lr=2e-3)
+    assert fg._hp_arg(frozen)._obj is fg._hp_arg(Hparams(lr=2e-3))._obj
+    assert fg._hp_arg({"lr": 3e-3})._obj.lr == pytest.approx(3e-3)

@@ -90,3 +90,21 @@ def test_traffic_is_reported_only_for_the_sources_it_was_taken_from(monkeypatch)
     monkeypatch.setattr(bench, "_kernel_source_hash", lambda: "0" * 16)
     assert bench._ncu_traffic("llama8b-mlp", "adamw", "fp32") is None
     assert bench._ncu_traffic("no-such-workload", "adamw", "fp32") is None
+
+
+def test_roofline_bound_is_the_slower_unit():
+    """The Llama MLP with bf16 operands and FP32 states needs more time at the tensor peak
+    (481 GFLOP / 1938 TFLOP/s = 248 us) than at the copy peak (1.325 GB / 6789 GB/s = 195 us):
+    tensor-bound.  With E4M3 operands the FP8 peak halves the flop time (124 us) and the same
+    W/m/v bytes make it HBM-bound."""
+    wl = WORKLOADS["llama8b-mlp"]
+    flops = wl.flops_per_step() / 3
+    b16 = bench.algorithmic_bytes(wl, "adamw", "fp32", "bf16") / 3
+    r = bench.roofline_entry(flops, b16, 0.35, 1938.1, 6789.0, None, {}, "t", "h")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["frac"] == pytest.approx(flops / 0.35e-3 / 1e12 / 1938.1)
+    assert r["other"]["bound"] == "hbm" and r["other"]["unit"] == "GB/s"
+    b8 = bench.algorithmic_bytes(wl, "adamw", "fp32", "e4m3") / 3
+    r8 = bench.roofline_entry(flops, b8, 0.28, 2 * 1938.1, 6789.0, None, {}, "t", "h")
+    assert r8["bound"] == "hbm" and r8["unit"] == "GB/s"
+    assert r8["achieved"] == pytest.approx(b8 / 0.28e-3 / 1e9) and r8["other"]["bound"] == "tensor"

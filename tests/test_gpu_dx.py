@@ -46,12 +46,14 @@ def _run_dx(dy, w, guard_rows=64):
     return out[:T]
 
 
-# (T, d_out, d_in) -> tile (a shape is taken only when it fills more than half the SMs): 128 x 128
+# (T, d_out, d_in) -> tile (a shape is taken only when it fills more than half the SMs): 128 x 64
 # with a 64-token tail; 128 x 256 with T not a multiple of 256 (80 tiles); a CTA pair with a 64-token
 # tail (90 pair tiles); a CTA pair, 170 tiles (more than resident pairs); a CTA pair on a long
-# reduction (d_out = 8192, 40 pair tiles); few pair tiles, so 128 x 128 instead
-CASES = [(320, 256, 384, (128, 128, 1)), (640, 384, 4096, (128, 256, 1)), (2112, 512, 2560, (256, 256, 2)),
-         (4160, 512, 2560, (256, 256, 2)), (1024, 8192, 2560, (256, 256, 2)), (576, 512, 768, (128, 128, 1))]
+# reduction (d_out = 8192, 40 pair tiles); few pair tiles and 128 x 128 tiles, so 128 x 64; 128 x
+# 128 (90 tiles)
+CASES = [(320, 256, 384, (128, 64, 1)), (640, 384, 4096, (128, 256, 1)), (2112, 512, 2560, (256, 256, 2)),
+         (4160, 512, 2560, (256, 256, 2)), (1024, 8192, 2560, (256, 256, 2)), (576, 512, 768, (128, 64, 1)),
+         (1152, 512, 1280, (128, 128, 1))]
 
 
 @pytest.mark.parametrize("T, d_out, d_in, shape", CASES)

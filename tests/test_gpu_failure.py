@@ -37,8 +37,9 @@ def _layer(d_out, d_in, T):
 
 
 # (2048, 1280): a CTA pair, over a long and a short token run; (1152, 2560): one CTA, 128 x 256;
-# (384, 384): one CTA, 128 x 128
-@pytest.mark.parametrize("d_out, d_in, T", [(2048, 1280, 8192), (2048, 1280, 512), (1152, 2560, 512), (384, 384, 512)])
+# (1536, 1536): one CTA, 128 x 128; (384, 384): one CTA, 128 x 64
+@pytest.mark.parametrize("d_out, d_in, T", [(2048, 1280, 8192), (2048, 1280, 512), (1152, 2560, 512), (1536, 1536, 512),
+                                            (384, 384, 512)])
 def test_withheld_stage_times_out_and_context_survives(d_out, d_in, T):
     dy, x, w, m, v = _layer(d_out, d_in, T)
     hp = default_hparams("adamw", lr=1e-3)

@@ -7,7 +7,7 @@ import backward_optimizer_gb300 as fg
 from oracle import int8_block, step as ostep
 from tests.compare import assert_codes, assert_moments, assert_weights, gradient_sensitivity, moment_rtol
 from tests.helpers import bits, f32
-from tests.shapes import FEW_PAIRS, PAIR, PAIR_MANY, SMALL, TILE, WIDE
+from tests.shapes import FEW_PAIRS, MID, PAIR, PAIR_MANY, SMALL, TILE, WIDE
 from workloads import (OPTIMIZERS, WORKLOADS, Hparams, Layer, Workload, activations, default_hparams,
                        layer_state, moment_init, normal_bf16)
 
@@ -137,13 +137,14 @@ def test_tiny_workload_three_steps():
         rw, rm, rv = bits(W), f32(M), f32(V)  # continue from the GPU's state: per-step parity
 
 
-# every tile kernel: a CTA pair on 256 x 256, one CTA on 128 x 256, one CTA on 128 x 128 (a small
-# layer, and a layer whose few pair tiles would leave most SMs idle)
-SHAPES = [PAIR, WIDE, SMALL, FEW_PAIRS]
+# every tile kernel: a CTA pair on 256 x 256, one CTA on 128 x 256, one CTA on 128 x 128 (a layer
+# whose few pair tiles would leave most SMs idle), one CTA on 128 x 64 (small layers)
+SHAPES = [PAIR, WIDE, MID, SMALL, FEW_PAIRS]
 
 
 @pytest.mark.parametrize("opt, d_out, d_in", [(o,) + PAIR for o in OPTIMIZERS] + [(o,) + WIDE for o in OPTIMIZERS]
-                         + [(o,) + s for o in ("adamw", "nadam", "sgd") for s in (SMALL, FEW_PAIRS)])
+                         + [(o,) + SMALL for o in OPTIMIZERS]
+                         + [(o,) + s for o in ("adamw", "nadam", "sgd") for s in (MID, FEW_PAIRS)])
 def test_fused_matches_oracle_every_optimizer(opt, d_out, d_in):
     got = fg.launch_shape(d_out, d_in, 192)
     assert (got["tile_rows"], got["tile_cols"], got["cluster"]) == TILE[(d_out, d_in)]
@@ -284,10 +285,13 @@ def test_status_word_clean_after_normal_runs():
 @pytest.mark.parametrize("d_out, d_in, T, rows, cols, cluster", [
     (2048, 1280, 8192, 256, 256, 2), (2048, 1280, 64, 256, 256, 2), (1536, 1792, 64, 256, 256, 2),
     (1536, 1536, 64, 128, 128, 1), (1152, 2560, 64, 128, 256, 1), (1152, 2048, 64, 128, 128, 1),
-    (384, 384, 64, 128, 128, 1), (512, 256, 256, 128, 128, 1), (1024, 1024, 4096, 128, 128, 1)])
+    (384, 384, 64, 128, 64, 1), (512, 256, 256, 128, 64, 1), (1024, 1024, 4096, 128, 64, 1),
+    (1280, 1280, 64, 128, 128, 1)])
 def test_launch_shape_query(d_out, d_in, T, rows, cols, cluster):
     """Pairs once they fill more than half the SMs (1536 x 1792: 42 pair tiles; 1536 x 1536: 36, so
-    144 tiles of 128 x 128); 128 x 256 likewise (1152 x 2560: 90 CTAs; 1152 x 2048: 72)."""
+    144 tiles of 128 x 128); 128 x 256 likewise (1152 x 2560: 90 CTAs; 1152 x 2048: 72); 128 x 64
+    once 128 x 128 would fill at most half (1024^2: 64 CTAs of 128 x 128, so 128 of 128 x 64;
+    1280^2: 100 of 128 x 128)."""
     import ctypes
     shape = fg.ForgeShape(T=T, d_out=d_out, d_in=d_in, state=0, reserved=0)
     r, c, cl, n = (ctypes.c_int32() for _ in range(4))

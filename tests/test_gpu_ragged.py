@@ -53,11 +53,12 @@ def _layer(d_out, d_in, T, opt, seed):
     return dy, x, w, m, v
 
 
-# (d_out, d_in, T, tile): 128 x 128 with ragged rows, columns (d_in not a multiple of 16) and
+# (d_out, d_in, T, tile): 128 x 64 with ragged rows, columns (d_in not a multiple of 16) and
 # tokens; a CTA pair whose last row tile leaves one CTA wholly outside the layer (54 pair tiles);
-# 128 x 256 with ragged columns (115 tiles); an 8 x 8 layer with one token
-CASES = [(200, 136, 100, (128, 128, 1)), (2056, 1288, 70, (256, 256, 2)), (2944, 1032, 64, (128, 256, 1)),
-         (8, 8, 1, (128, 128, 1))]
+# 128 x 256 with ragged columns (115 tiles); 128 x 128 with ragged rows and columns (110 tiles);
+# an 8 x 8 layer with one token
+CASES = [(200, 136, 100, (128, 64, 1)), (2056, 1288, 70, (256, 256, 2)), (2944, 1032, 64, (128, 256, 1)),
+         (1288, 1272, 90, (128, 128, 1)), (8, 8, 1, (128, 64, 1))]
 
 
 @pytest.mark.parametrize("d_out, d_in, T, tile", CASES)
