@@ -272,29 +272,30 @@ uint64_t acc_wait_limit(uint64_t base_ns, int64_t k_blocks) {
 using TileFn = cudaError_t (*)(const forge::TileLaunch&);
 using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
 
-template <int OPT, int BN, int CL, int OPS>
+template <int OPT, int BN, int CL, int OPS, int G = 1>
 TileFn tile_fn_state(int state) {
     using namespace forge;
     if (state == FORGE_STATE_INT8_B64) {
         if constexpr (BN == 64) return nullptr;  // INT8 blocks need 64 columns per epilogue warp
-        else return launch_tile<OPT, kEpiOptINT8, BN, CL, OPS>;
+        else return launch_tile<OPT, kEpiOptINT8, BN, CL, OPS, G>;
     }
-    if (state == FORGE_STATE_BF16) return launch_tile<OPT, kEpiOptBF16, BN, CL, OPS>;
-    return launch_tile<OPT, kEpiOptFP32, BN, CL, OPS>;
+    if (state == FORGE_STATE_BF16) return launch_tile<OPT, kEpiOptBF16, BN, CL, OPS, G>;
+    return launch_tile<OPT, kEpiOptFP32, BN, CL, OPS, G>;
 }
 
-template <int BN, int CL, int OPS>
+template <int BN, int CL, int OPS, int G = 1>
 TileFn tile_fn_v(forge_opt_kind k, int state) {
     using namespace forge;
     switch (k) {
-        case FORGE_ADAMW: return tile_fn_state<kAdamW, BN, CL, OPS>(state);
-        case FORGE_NADAM: return tile_fn_state<kNAdam, BN, CL, OPS>(state);
-        case FORGE_RADAM: return tile_fn_state<kRAdam, BN, CL, OPS>(state);
-        case FORGE_LION: return tile_fn_state<kLion, BN, CL, OPS>(state);
-        case FORGE_RMSPROP: return tile_fn_state<kRMSprop, BN, CL, OPS>(state);
-        case FORGE_ADAGRAD: return tile_fn_state<kAdaGrad, BN, CL, OPS>(state);
-        case FORGE_SGD: return state == FORGE_STATE_FP32 ? launch_tile<kSGD, kEpiOptFP32, BN, CL, OPS> : nullptr;
-        case FORGE_SGD_MOMENTUM: return tile_fn_state<kSGDMomentum, BN, CL, OPS>(state);
+        case FORGE_ADAMW: return tile_fn_state<kAdamW, BN, CL, OPS, G>(state);
+        case FORGE_NADAM: return tile_fn_state<kNAdam, BN, CL, OPS, G>(state);
+        case FORGE_RADAM: return tile_fn_state<kRAdam, BN, CL, OPS, G>(state);
+        case FORGE_LION: return tile_fn_state<kLion, BN, CL, OPS, G>(state);
+        case FORGE_RMSPROP: return tile_fn_state<kRMSprop, BN, CL, OPS, G>(state);
+        case FORGE_ADAGRAD: return tile_fn_state<kAdaGrad, BN, CL, OPS, G>(state);
+        case FORGE_SGD:
+            return state == FORGE_STATE_FP32 ? launch_tile<kSGD, kEpiOptFP32, BN, CL, OPS, G> : nullptr;
+        case FORGE_SGD_MOMENTUM: return tile_fn_state<kSGDMomentum, BN, CL, OPS, G>(state);
     }
     return nullptr;
 }
@@ -344,17 +345,17 @@ TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t) {
     using namespace forge;
     if (epi == kEpiDX) {
         if constexpr (OPS != kOpsBF16) return nullptr;
-        if (t.cg == 2) return launch_tile<0, kEpiDX, 256, 2, kOpsBF16>;
-        if (t.bn == 64) return launch_tile<0, kEpiDX, 64, 1, kOpsBF16>;
-        return t.bn == 256 ? launch_tile<0, kEpiDX, 256, 1, kOpsBF16> : launch_tile<0, kEpiDX, 128, 1, kOpsBF16>;
+        if (t.cg == 2) return launch_tile<0, kEpiDX, 256, 2, kOpsBF16, 1>;
+        if (t.bn == 64) return launch_tile<0, kEpiDX, 64, 1, kOpsBF16, 1>;
+        return t.bn == 256 ? launch_tile<0, kEpiDX, 256, 1, kOpsBF16, 1> : launch_tile<0, kEpiDX, 128, 1, kOpsBF16, 1>;
     }
     if (epi == kEpiStoreGrad) {
-        if (t.cg == 2) return launch_tile<0, kEpiStoreGrad, 256, 2, OPS>;
+        if (t.cg == 2) return launch_tile<0, kEpiStoreGrad, 256, 2, OPS, 1>;
         if (t.bn == 64) {
             if constexpr (OPS != kOpsBF16) return nullptr;
-            else return launch_tile<0, kEpiStoreGrad, 64, 1, kOpsBF16>;
+            else return launch_tile<0, kEpiStoreGrad, 64, 1, kOpsBF16, 1>;
         }
-        return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1, OPS> : launch_tile<0, kEpiStoreGrad, 128, 1, OPS>;
+        return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1, OPS, 1> : launch_tile<0, kEpiStoreGrad, 128, 1, OPS, 1>;
     }
     if (t.cg == 2) return tile_fn_v<256, 2, OPS>(k, state);
     if (t.bn == 64) {
@@ -416,21 +417,19 @@ forge_status run_opt(const float* dW, void* W, void* m, void* v, float* qscales,
     return cuda_status(fn(a, grid, stream));
 }
 
-// e4m3: dY and X are E4M3 codes and the gradient tile is scaled by g_scale = s_dY * s_X.
-forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m, void* v, float* qscales,
-                      forge_opt_kind k, int epi, const forge_hparams* hp, const forge_shape* shape, int64_t step,
-                      uint64_t seed, cudaStream_t stream, const DeviceInfo& dev, bool e4m3 = false,
-                      float g_scale = 1.0f, const float* row_scales = nullptr, const float* col_scales = nullptr) {
+// One layer's kernel arguments and tensor maps for tile shape ts.  e4m3: dY and X are E4M3 codes and
+// the gradient tile is scaled by g_scale = s_dY * s_X (or per channel by row_scales x col_scales).
+forge_status prepare_layer(forge::TileArgs& a, CUtensorMap* maps, const void* dY, const void* X, float* dW, void* W,
+                           void* m, void* v, float* qscales, forge_opt_kind k, const forge_hparams* hp,
+                           const forge_shape* shape, int64_t step, uint64_t seed, const DeviceInfo& dev, TileShape ts,
+                           bool e4m3, float g_scale, const float* row_scales, const float* col_scales,
+                           int withhold) {
     const bool int8 = shape->state == FORGE_STATE_INT8_B64;
     const uint64_t n = static_cast<uint64_t>(shape->d_out) * static_cast<uint64_t>(shape->d_in);
-    forge::TileArgs a;
     std::memset(&a, 0, sizeof(a));
     a.d_out = static_cast<int>(shape->d_out);
     a.d_in = static_cast<int>(shape->d_in);
     a.T = static_cast<int>(shape->T);
-    // 128 x 64 tiles need bf16 operands and an epilogue on 32-column runs (not INT8 states)
-    const bool narrow_ok = !e4m3 && (epi == forge::kEpiStoreGrad || shape->state != FORGE_STATE_INT8_B64);
-    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T, dev.num_sms, narrow_ok);
     const int tiles_m = static_cast<int>(ceil_div(a.d_out, forge::kBM * ts.cg));
     const int tiles_n = static_cast<int>(ceil_div(a.d_in, ts.bn));
     a.num_tiles = tiles_m * tiles_n;
@@ -451,17 +450,27 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     a.status = dev.status;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.acc_wait_limit_ns = acc_wait_limit(a.wait_limit_ns, a.k_blocks);
-    a.withhold_first_stage = g_withhold_next.exchange(0);
+    a.withhold_first_stage = withhold;
+    forge_status st = make_operand_map(&maps[0], dY, shape->d_out, shape->T, e4m3);
+    if (st != FORGE_OK) return st;
+    return make_operand_map(&maps[1], X, shape->d_in, shape->T, e4m3);
+}
 
-    forge::TileLaunch l;
-    forge_status st = make_operand_map(&l.tmap_dy, dY, shape->d_out, shape->T, e4m3);
+forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m, void* v, float* qscales,
+                      forge_opt_kind k, int epi, const forge_hparams* hp, const forge_shape* shape, int64_t step,
+                      uint64_t seed, cudaStream_t stream, const DeviceInfo& dev, bool e4m3 = false,
+                      float g_scale = 1.0f, const float* row_scales = nullptr, const float* col_scales = nullptr) {
+    // 128 x 64 tiles need bf16 operands and an epilogue on 32-column runs (not INT8 states)
+    const bool narrow_ok = !e4m3 && (epi == forge::kEpiStoreGrad || shape->state != FORGE_STATE_INT8_B64);
+    const TileShape ts = pick_shape(shape->d_out, shape->d_in, shape->T, dev.num_sms, narrow_ok);
+    forge::TileGroup<1> g;
+    g.n = 1;
+    forge_status st = prepare_layer(g.layer[0], g.maps, dY, X, dW, W, m, v, qscales, k, hp, shape, step, seed, dev,
+                                    ts, e4m3, g_scale, row_scales, col_scales, g_withhold_next.exchange(0));
     if (st != FORGE_OK) return st;
-    st = make_operand_map(&l.tmap_x, X, shape->d_in, shape->T, e4m3);
-    if (st != FORGE_OK) return st;
-    l.args = &a;
-    l.num_tiles = a.num_tiles;
-    l.num_sms = dev.num_sms;
-    l.stream = stream;
+    g.tile_start[0] = 0;
+    g.tile_start[1] = g.layer[0].num_tiles;
+    forge::TileLaunch l{&g, g.tile_start[1], dev.num_sms, stream};
     // epi is kEpiStoreGrad (dW to memory) or kEpiOptFP32 (the fused step, whose epilogue follows the state dtype)
     TileFn fn = tile_fn(k, shape->state, epi, ts, e4m3);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
@@ -471,7 +480,9 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
 
 forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* shape, cudaStream_t stream,
                     const DeviceInfo& dev) {
-    forge::TileArgs a;
+    forge::TileGroup<1> g;
+    g.n = 1;
+    forge::TileArgs& a = g.layer[0];
     std::memset(&a, 0, sizeof(a));
     a.d_out = static_cast<int>(shape->d_out);
     a.d_in = static_cast<int>(shape->d_in);
@@ -488,18 +499,15 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.acc_wait_limit_ns = acc_wait_limit(a.wait_limit_ns, a.k_blocks);
     a.withhold_first_stage = g_withhold_next.exchange(0);
-
-    forge::TileLaunch l;
     // A = dY [T, d_out] read K-major with the same box as the weight gradient's dY^T; B = W
     // [d_out, d_in] read MN-major like X
-    forge_status st = make_operand_map(&l.tmap_dy, dY, shape->d_out, shape->T);
+    forge_status st = make_operand_map(&g.maps[0], dY, shape->d_out, shape->T);
     if (st != FORGE_OK) return st;
-    st = make_operand_map(&l.tmap_x, W, shape->d_in, shape->d_out);
+    st = make_operand_map(&g.maps[1], W, shape->d_in, shape->d_out);
     if (st != FORGE_OK) return st;
-    l.args = &a;
-    l.num_tiles = a.num_tiles;
-    l.num_sms = dev.num_sms;
-    l.stream = stream;
+    g.tile_start[0] = 0;
+    g.tile_start[1] = a.num_tiles;
+    forge::TileLaunch l{&g, a.num_tiles, dev.num_sms, stream};
     TileFn fn = tile_fn(FORGE_SGD, FORGE_STATE_FP32, forge::kEpiDX, ts, false);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
@@ -675,6 +683,70 @@ forge_status forge_linear_backward(const void* dY, const void* X, void* W, void*
     st = launch_dx(dY, W, dX, shape, stream);
     if (st != FORGE_OK) return st;
     return launch_fused(dY, X, W, m, v, qscales, opt_kind, hp, shape, step, seed, stream);
+}
+
+forge_status forge_fused_dw_step_layers(const forge_layer* layers, int32_t n_layers, int32_t state,
+                                        forge_opt_kind opt_kind, const forge_hparams* hp, int64_t step,
+                                        struct CUstream_st* stream) {
+    if (n_layers < 0 || (n_layers > 0 && layers == nullptr)) return FORGE_ERR_INVALID_ARGUMENT;
+    auto shape_of = [&](const forge_layer& L) { return forge_shape{L.T, L.d_out, L.d_in, state, 0}; };
+    for (int32_t i = 0; i < n_layers; ++i) {
+        const forge_layer& L = layers[i];
+        const forge_shape sh = shape_of(L);
+        forge_status st = check_fused(L.dY, L.X, L.W, L.m, L.v, L.qscales, opt_kind, hp, &sh, step);
+        if (st != FORGE_OK) return st;
+    }
+    if (n_layers == 0) return FORGE_OK;
+    DeviceInfo* dev = nullptr;
+    forge_status st = device_info(&dev);
+    if (st != FORGE_OK) return st;
+    // layers that run together: non-empty, with tokens, whose preferred tile is a CTA pair; together
+    // they must still fill more than half the SMs, else each takes its own shape
+    auto pair_shaped = [](const forge_layer& L) {
+        const bool rows256 = L.d_out % 256 == 0 || (L.d_out % 128 != 0 && L.d_out > 1024);
+        const bool cols256 = L.d_in % 256 == 0 || (L.d_in % 128 != 0 && L.d_in > 1024);
+        return L.T > 0 && L.d_out > 0 && L.d_in > 0 && rows256 && cols256;
+    };
+    int64_t pair_ctas = 0;
+    for (int32_t i = 0; i < n_layers; ++i)
+        if (pair_shaped(layers[i])) pair_ctas += 2 * ceil_div(layers[i].d_out, 256) * ceil_div(layers[i].d_in, 256);
+    const bool group = 2 * pair_ctas > dev->num_sms;
+    TileFn fn = group ? tile_fn_v<256, 2, forge::kOpsBF16, forge::kMaxGroup>(opt_kind, state) : nullptr;
+    if (group && fn == nullptr) return FORGE_ERR_UNSUPPORTED;
+    constexpr TileShape kPair{256, 2};
+    int32_t next = 0;  // layers [0, next) are launched
+    while (next < n_layers) {
+        // a layer with no pair-shaped neighbour to share a launch with runs alone, on the
+        // single-layer kernel (the grouped one reads its arguments through a layer index)
+        const bool alone = next + 1 >= n_layers || !pair_shaped(layers[next + 1]);
+        if (!group || !pair_shaped(layers[next]) || alone) {
+            const forge_layer& L = layers[next++];
+            const forge_shape sh = shape_of(L);
+            st = launch_fused(L.dY, L.X, L.W, L.m, L.v, L.qscales, opt_kind, hp, &sh, step, L.seed, stream);
+            if (st != FORGE_OK) return st;
+            continue;
+        }
+        // up to kMaxGroup consecutive pair-shaped layers in one launch
+        static thread_local forge::TileGroup<forge::kMaxGroup> g;
+        g.n = 0;
+        g.tile_start[0] = 0;
+        const int withhold = g_withhold_next.exchange(0);
+        while (next < n_layers && g.n < forge::kMaxGroup && pair_shaped(layers[next])) {
+            const forge_layer& L = layers[next++];
+            const forge_shape sh = shape_of(L);
+            st = prepare_layer(g.layer[g.n], &g.maps[2 * g.n], L.dY, L.X, nullptr, L.W, L.m, L.v, L.qscales, opt_kind,
+                               hp, &sh, step, L.seed, *dev, kPair, false, 1.0f, nullptr, nullptr,
+                               g.n == 0 ? withhold : 0);
+            if (st != FORGE_OK) return st;
+            g.tile_start[g.n + 1] = g.tile_start[g.n] + g.layer[g.n].num_tiles;
+            ++g.n;
+        }
+        forge::TileLaunch l{&g, g.tile_start[g.n], dev->num_sms, stream};
+        g_launches.fetch_add(1);
+        st = cuda_status(fn(l));
+        if (st != FORGE_OK) return st;
+    }
+    return FORGE_OK;
 }
 
 forge_status forge_dw_gemm(const void* dY, const void* X, float* dW, const forge_shape* shape,

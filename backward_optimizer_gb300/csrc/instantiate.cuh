@@ -9,11 +9,14 @@
 
 namespace forge {
 
-template <int OPT, int EPI, int BN, int CL, int OPS>
+// a launch copies its whole group into the kernel's parameter space, whose limit is 32764 bytes
+static_assert(sizeof(TileGroup<kMaxGroup>) <= 32764, "group of layers too large for the kernel parameters");
+
+template <int OPT, int EPI, int BN, int CL, int OPS, int G>
 cudaError_t launch_tile(const TileLaunch& l) {
     constexpr int CG = CL == 1 ? 1 : 2;
     using C = TileCfg<BN, CG, EPI, OPS>;
-    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT, OPS>;
+    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT, OPS, G>;
     static std::atomic<uint64_t> configured{0};  // one bit per device ordinal
     static std::atomic<int> max_clusters[64];    // co-resident clusters per device
     int dev = 0;
@@ -48,7 +51,7 @@ cudaError_t launch_tile(const TileLaunch& l) {
     const int cap = CL == 1 ? l.num_sms : max_clusters[dev].load();
     const int units = l.num_tiles < cap ? l.num_tiles : cap;
     cfg.gridDim = dim3(units * CL, 1, 1);
-    return cudaLaunchKernelEx(&cfg, kernel, l.tmap_dy, l.tmap_x, *l.args);
+    return cudaLaunchKernelEx(&cfg, kernel, *static_cast<const TileGroup<G>*>(l.group));
 }
 
 // CTA count and cluster size a launch_tile<..., BN, CL> call with `num_tiles` tiles would use.
@@ -56,7 +59,7 @@ template <int OPT, int EPI, int BN, int CL>
 cudaError_t tile_grid(int num_tiles, int num_sms, int* ctas) {
     constexpr int CG = CL == 1 ? 1 : 2;
     using C = TileCfg<BN, CG, EPI>;
-    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT, kOpsBF16>;
+    auto kernel = forge_tile_kernel<BN, CL, EPI, OPT, kOpsBF16, 1>;
     int cap = num_sms;
     if (CL > 1) {
         cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -88,13 +91,17 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 }  // namespace forge
 
 #define FORGE_INSTANTIATE_TILES_OPS(OPT, EPI, OPS)                                               \
-    template cudaError_t forge::launch_tile<OPT, EPI, 128, 1, OPS>(const forge::TileLaunch&);       \
-    template cudaError_t forge::launch_tile<OPT, EPI, 256, 1, OPS>(const forge::TileLaunch&);       \
-    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2, OPS>(const forge::TileLaunch&);
+    template cudaError_t forge::launch_tile<OPT, EPI, 128, 1, OPS, 1>(const forge::TileLaunch&);    \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 1, OPS, 1>(const forge::TileLaunch&);    \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2, OPS, 1>(const forge::TileLaunch&);
+
+// Groups of up to kMaxGroup layers: CTA pairs, bf16 operands.
+#define FORGE_INSTANTIATE_GROUP(OPT, EPI) \
+    template cudaError_t forge::launch_tile<OPT, EPI, 256, 2, forge::kOpsBF16, forge::kMaxGroup>(const forge::TileLaunch&);
 
 // 128 x 64 tiles for small layers: bf16 operands, every epilogue but the INT8 one.
 #define FORGE_INSTANTIATE_NARROW(OPT, EPI) \
-    template cudaError_t forge::launch_tile<OPT, EPI, 64, 1, forge::kOpsBF16>(const forge::TileLaunch&);
+    template cudaError_t forge::launch_tile<OPT, EPI, 64, 1, forge::kOpsBF16, 1>(const forge::TileLaunch&);
 
 #define FORGE_INSTANTIATE_TILES(OPT, EPI) FORGE_INSTANTIATE_TILES_OPS(OPT, EPI, forge::kOpsBF16)
 
@@ -107,13 +114,16 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
 #define FORGE_INSTANTIATE_OPT(OPT)                    \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptFP32) \
     FORGE_INSTANTIATE_NARROW(OPT, forge::kEpiOptFP32) \
+    FORGE_INSTANTIATE_GROUP(OPT, forge::kEpiOptFP32) \
     template cudaError_t forge::launch_opt<OPT, 0>(const forge::OptArgs&, int, cudaStream_t);
 
 #define FORGE_INSTANTIATE_OPT_INT8(OPT)               \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptINT8) \
+    FORGE_INSTANTIATE_GROUP(OPT, forge::kEpiOptINT8) \
     template cudaError_t forge::launch_opt<OPT, 1>(const forge::OptArgs&, int, cudaStream_t);
 
 #define FORGE_INSTANTIATE_OPT_BF16(OPT)               \
     FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptBF16) \
     FORGE_INSTANTIATE_NARROW(OPT, forge::kEpiOptBF16) \
+    FORGE_INSTANTIATE_GROUP(OPT, forge::kEpiOptBF16) \
     template cudaError_t forge::launch_opt<OPT, 2>(const forge::OptArgs&, int, cudaStream_t);

@@ -11,12 +11,15 @@ namespace forge {
 
 struct TileArgs;
 struct OptArgs;
+template <int G> struct TileGroup;
+
+// Group sizes the tile kernels are built for: one layer per launch, or up to kMaxGroup independent
+// layers on CTA pairs (forge_fused_dw_step_layers).
+constexpr int kMaxGroup = 16;
 
 struct TileLaunch {
-    CUtensorMap tmap_dy;
-    CUtensorMap tmap_x;
-    const TileArgs* args;
-    int num_tiles;  // tiles of the launch's shape (per CTA or CTA pair)
+    const void* group;  // the TileGroup<G> of the launch (host memory, copied into the kernel's parameters)
+    int num_tiles;      // tiles of all the group's layers (per CTA or CTA pair)
     int num_sms;
     cudaStream_t stream;
 };
@@ -27,7 +30,8 @@ struct TileLaunch {
 // BN: tile columns (128, or 256 = two 128 x 128 tiles side by side).
 // CL: CTAs per cluster (1: a 128 x BN tile per CTA; 2: a 256 x BN tile per CTA pair).
 // OPS: operand format of dY and X, 0 = bf16, 1 = E4M3 (the gradient tile is scaled by s_dY * s_X).
-template <int OPT, int EPI, int BN, int CL, int OPS> cudaError_t launch_tile(const TileLaunch& l);
+// G: the group size the kernel is built for (1, or kMaxGroup).
+template <int OPT, int EPI, int BN, int CL, int OPS, int G> cudaError_t launch_tile(const TileLaunch& l);
 
 // CTAs a tile launch of the given shape would run (persistent grid size).
 cudaError_t tile_ctas(int bn, int cl, int num_tiles, int num_sms, int* ctas);

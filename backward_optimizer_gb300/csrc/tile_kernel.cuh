@@ -116,6 +116,27 @@ struct TileArgs {
     int withhold_first_stage;     // test switch: the producer arms its first stage but never fills it, so a wait runs out
 };
 
+// Up to G independent layers in one launch: their tiles are numbered one layer after another
+// (layer l owns tiles tile_start[l] .. tile_start[l+1]-1) and visited by one persistent schedule,
+// so the pipeline fills and drains once for the group instead of once per layer, and the last
+// wave of one layer overlaps the first of the next.  A single-layer call is a group of one.  The
+// tensor maps live in the kernel's parameter space (64-byte aligned, as TMA requires).
+template <int G>
+struct TileGroup {
+    int n;                        // layers, 1 .. G
+    int tile_start[G + 1];        // prefix sums of the layers' tile counts
+    CUtensorMap maps[2 * G];      // per layer: dY (or dY for dX), X (or W for dX)
+    TileArgs layer[G];
+};
+
+// The layer owning tile `tile`, from a layer index known to be at or before it.
+template <int G>
+__device__ __forceinline__ int layer_of(const TileGroup<G>& grp, int tile, int l) {
+    if constexpr (G == 1) return 0;  // a compile-time layer: its arguments are read at fixed offsets
+    while (l + 1 < grp.n && tile >= grp.tile_start[l + 1]) ++l;
+    return l;
+}
+
 // ---------------------------------------------------------------- bounded waits
 
 struct AbortCtx {
@@ -612,10 +633,9 @@ __device__ __forceinline__ void drain_copies(uint64_t* full, uint64_t n_own, uin
     }
 }
 
-template <int BN, int CL, int EPI, int OPT, int OPS>
+template <int BN, int CL, int EPI, int OPT, int OPS, int G>
 __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
-    forge_tile_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
-                      const TileArgs a) {
+    forge_tile_kernel(const __grid_constant__ TileGroup<G> grp) {
     static_assert(CL == 1 || CL == 2, "cluster size");
     static_assert(OPS == kOpsBF16 || EPI != kEpiDX, "the input gradient takes bf16 operands");
     using O = OperandTraits<OPS>;
@@ -658,8 +678,10 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
         mbar_init(peer_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmap_dy);
-        tma_prefetch_desc(&tmap_x);
+        for (int l = 0; l < grp.n; ++l) {
+            tma_prefetch_desc(&grp.maps[2 * l]);
+            tma_prefetch_desc(&grp.maps[2 * l + 1]);
+        }
     }
     if (warp == 1) {
         tmem_alloc<CG>(tmem_slot, C::kTmemCols);
@@ -670,8 +692,9 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
     if constexpr (CL > 1) cluster_sync();  // the peer's barriers exist before anything signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const AbortCtx ab{abort_flag, a.status, a.wait_limit_ns};
-    const int kblocks = a.k_blocks;
+    const TileArgs& a0 = grp.layer[0];  // status word, wait limits and test switch: the same for every layer
+    const AbortCtx ab{abort_flag, a0.status, a0.wait_limit_ns};
+    const int num_tiles = grp.tile_start[grp.n];
     uint64_t n_issued = 0;   // producer: stages passed (armed and copied, but for the withheld one)
     int64_t withheld = -1;   // producer: the stage the test switch left without this CTA's copies
 
@@ -682,17 +705,23 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             const uint64_t keep = policy_evict_last();
-            for (int tile = first_tile; ok && tile < a.num_tiles; tile += tile_stride) {
+            int l = 0;
+            for (int tile = first_tile; ok && tile < num_tiles; tile += tile_stride) {
+                l = layer_of(grp, tile, l);
+                const TileArgs& a = grp.layer[l];
+                const CUtensorMap* tmap_dy = &grp.maps[2 * l];
+                const CUtensorMap* tmap_x = &grp.maps[2 * l + 1];
                 int mb, nb;
-                tile_coords(tile, a.order, mb, nb);
+                tile_coords(tile - grp.tile_start[l], a.order, mb, nb);
                 const int row_a = mb * kBM * CG + static_cast<int>(rank) * kBM;
                 const int col_b = nb * BN + static_cast<int>(rank) * C::kBLoad;
+                const int kblocks = a.k_blocks;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, ab)) { ok = false; break; }
                     uint32_t bar = smem_addr(&full[stage]);
                     if constexpr (CG == 2) bar = map_to_rank(bar, 0);
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], CG * C::kStageBytes);
-                    if (a.withhold_first_stage && rank == 0 && tile == first_tile && kb == 0) {
+                    if (a0.withhold_first_stage && rank == 0 && tile == first_tile && kb == 0) {
                         // test switch: arm this stage but never copy into it, so the MMA thread's wait
                         // for it runs out
                         withheld = static_cast<int64_t>(n_issued);
@@ -708,23 +737,23 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
                             // the stage (64 token rows at j * 8 KiB)
 #pragma unroll
                             for (int j = 0; j < 2; ++j)
-                                tma_load_2d_cg<CG>(a_dst + j * 8192, &tmap_dy, bar, row_a, k0 + 64 * j, keep);
+                                tma_load_2d_cg<CG>(a_dst + j * 8192, tmap_dy, bar, row_a, k0 + 64 * j, keep);
 #pragma unroll
                             for (int j = 0; j < C::kBLoad / 128; ++j)
 #pragma unroll
                                 for (int h = 0; h < 2; ++h)
-                                    tma_load_2d_cg<CG>(b_dst + j * O::kBlockBytes + h * 8192, &tmap_x, bar,
+                                    tma_load_2d_cg<CG>(b_dst + j * O::kBlockBytes + h * 8192, tmap_x, bar,
                                                        col_b + 128 * j, k0 + 64 * h, keep);
                         } else {
 #pragma unroll
                             for (int j = 0; j < 2; ++j) {
                                 const int r = row_a + 64 * j;
-                                tma_load_2d_cg<CG>(a_dst + j * kBK * 128, &tmap_dy, bar, kAKMajor ? k0 : r,
+                                tma_load_2d_cg<CG>(a_dst + j * kBK * 128, tmap_dy, bar, kAKMajor ? k0 : r,
                                                    kAKMajor ? r : k0, keep);
                             }
 #pragma unroll
                             for (int j = 0; j < C::kBLoad / 64; ++j)
-                                tma_load_2d_cg<CG>(b_dst + j * kBK * 128, &tmap_x, bar, col_b + 64 * j, k0, keep);
+                                tma_load_2d_cg<CG>(b_dst + j * kBK * 128, tmap_x, bar, col_b + 64 * j, k0, keep);
                         }
                     }
                     ++n_issued;
@@ -748,7 +777,10 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued_any = false;
-            for (int tile = first_tile; ok && tile < a.num_tiles; tile += tile_stride) {
+            int l = 0;
+            for (int tile = first_tile; ok && tile < num_tiles; tile += tile_stride) {
+                l = layer_of(grp, tile, l);
+                const int kblocks = grp.layer[l].k_blocks;
                 if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, ab)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -783,7 +815,7 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
             }
             if (!ok && issued_any) {
                 tc_commit_local<CG>(drain);
-                drain_bounded(drain, 0, a.wait_limit_ns);
+                drain_bounded(drain, 0, a0.wait_limit_ns);
             }
         }
     } else {
@@ -792,21 +824,25 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
         const int quarter = warp & 3;   // a warp may only touch TMEM lanes 32*(warp%4) .. +31
         const int half = e >> 2;                // column part owned by this warp
         constexpr int kWidth = BN / (C::kEpiWarps / 4);
-        // the wait for a finished accumulator spans a whole tile mainloop, which grows with T
-        const AbortCtx ab_acc{abort_flag, a.status, a.acc_wait_limit_ns};
         if constexpr (EPI == kEpiOptFP32 || EPI == kEpiOptBF16) {
-            if (first_tile < a.num_tiles) {
+            if (first_tile < num_tiles) {
+                const int l0 = layer_of(grp, first_tile, 0);
                 int mb, nb;
-                tile_coords(first_tile, a.order, mb, nb);
+                tile_coords(first_tile - grp.tile_start[l0], grp.layer[l0].order, mb, nb);
                 prefetch_first_run<OPT, EPI == kEpiOptBF16>(
-                    a, mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32, nb * BN + half * kWidth);
+                    grp.layer[l0], mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32, nb * BN + half * kWidth);
             }
         }
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = first_tile; tile < a.num_tiles; tile += tile_stride) {
+        int l = 0;
+        for (int tile = first_tile; tile < num_tiles; tile += tile_stride) {
+            l = layer_of(grp, tile, l);
+            const TileArgs& a = grp.layer[l];
+            // the wait for a finished accumulator spans a whole tile mainloop, which grows with T
+            const AbortCtx ab_acc{abort_flag, a0.status, a.acc_wait_limit_ns};
             int mb, nb;
-            tile_coords(tile, a.order, mb, nb);
+            tile_coords(tile - grp.tile_start[l], a.order, mb, nb);
             int ok = 1;
             if (lane == 0) ok = wait_bounded(&acc_full[acc], acc_phase, ab_acc) ? 1 : 0;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -820,10 +856,11 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
             if constexpr (EPI == kEpiDX) epi_store_dx<kWidth>(a, row0, col0, taddr);
             else if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth, kScale>(a, row0, col0, taddr, strip);
             else if constexpr (EPI == kEpiOptFP32 || EPI == kEpiOptBF16) {
+                // the next tile's first run is prefetched only within the same layer
                 int row0n = -1, col0n = 0;
-                if (tile + tile_stride < a.num_tiles) {
+                if (tile + tile_stride < num_tiles && layer_of(grp, tile + tile_stride, l) == l) {
                     int mbn, nbn;
-                    tile_coords(tile + tile_stride, a.order, mbn, nbn);
+                    tile_coords(tile + tile_stride - grp.tile_start[l], a.order, mbn, nbn);
                     row0n = mbn * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
                     col0n = nbn * BN + half * kWidth;
                 }
@@ -851,15 +888,15 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
         if constexpr (CG == 2) {
             counted = false;
             const uint64_t t0 = global_timer_ns();
-            while (!counted && global_timer_ns() - t0 <= 4 * a.wait_limit_ns) counted = mbar_try_wait_cluster(peer_done, 0);
+            while (!counted && global_timer_ns() - t0 <= 4 * a0.wait_limit_ns) counted = mbar_try_wait_cluster(peer_done, 0);
             if (counted) n_peer = ld_shared_volatile_u64(peer_count);
         }
         if (counted) {
-            drain_copies<C::kStages, CG>(full, n_issued, n_peer, withheld, C::kStageBytes, a.wait_limit_ns);
+            drain_copies<C::kStages, CG>(full, n_issued, n_peer, withheld, C::kStageBytes, a0.wait_limit_ns);
         } else {
             // the odd CTA never reported (it is itself stuck past every limit): wait for the last
             // phase this CTA armed on each slot, bounded
-            drain_copies<C::kStages, 1>(full, n_issued, n_issued, withheld, C::kStageBytes, a.wait_limit_ns);
+            drain_copies<C::kStages, 1>(full, n_issued, n_issued, withheld, C::kStageBytes, a0.wait_limit_ns);
         }
     }
     // a pair tears down together: its MMAs read both CTAs' shared memory and write both TMEMs, and

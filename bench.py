@@ -232,13 +232,30 @@ def run_gpu(args, rank, world):
             fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], args.opt, hp, t_step,
                              seed=0x5EED + i, stream=on)
 
-    def fused_pass(ev=None):
+    # bf16 operands: every layer of the step in one call (forge_fused_dw_step_layers), which runs
+    # the layers that take CTA pairs together, up to 16 per launch; E4M3 operands: one call per layer
+    grouped = not e4m3 and not args.per_layer_calls and len(layers) > 1
+    group_args = [(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], 0x5EED + i) for i, L in enumerate(layers)]
+    calls_per_step = 1 if grouped else len(layers)
+
+    def per_layer_pass(ev=None, on=None):
+        on = stream if on is None else on
         for i, L in enumerate(layers):
             if ev is not None:
-                ev[i][0].record(stream)
-            fused(i, L)
+                ev[i][0].record(on)
+            fused(i, L, on=on)
             if ev is not None:
-                ev[i][1].record(stream)
+                ev[i][1].record(on)
+
+    def fused_pass(ev=None, on=None):
+        on = stream if on is None else on
+        if not grouped:
+            return per_layer_pass(ev, on)
+        if ev is not None:
+            ev[0][0].record(on)
+        fg.fused_dw_step_layers(group_args, args.opt, hp, t_step, stream=on)
+        if ev is not None:
+            ev[0][1].record(on)
 
     def barrier():
         if world > 1:
@@ -272,7 +289,7 @@ def run_gpu(args, rank, world):
     # launch duration (the roofline).  Kept out of the step timing: recording two events per launch
     # costs host time that a small layer's launch does not hide.
     per_launch = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in layers] for _ in range(args.steps)]
+                   for _ in range(calls_per_step)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -286,6 +303,22 @@ def run_gpu(args, rank, world):
     launch_pass_ms = l0.elapsed_time(l1) / args.steps
     if fg.sync_status() != 0:
         raise RuntimeError("device status in the per-launch timing")
+    # the same step as one call per layer (one launch each), for comparison with the grouped call
+    per_layer_ms = float("nan")
+    if grouped:
+        for _ in range(args.warmup):
+            per_layer_pass()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        p0.record(stream)
+        for _ in range(args.steps):
+            per_layer_pass()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        per_layer_ms = p0.elapsed_time(p1) / args.steps
+        if fg.sync_status() != 0:
+            raise RuntimeError("device status in the per-layer timing")
 
     # ---- the same fused pass captured once in a CUDA graph and replayed: no host launch path per
     # layer (it matters only for small layers, whose kernels are shorter than a launch)
@@ -293,9 +326,7 @@ def run_gpu(args, rank, world):
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side), torch.cuda.graph(graph):
-        cap = torch.cuda.current_stream()
-        for i, L in enumerate(layers):
-            fused(i, L, on=cap)
+        fused_pass(on=torch.cuda.current_stream())
     stream.wait_stream(side)
     for _ in range(args.warmup):
         graph.replay()
@@ -456,13 +487,15 @@ def run_gpu(args, rank, world):
         raise RuntimeError(f"device status {status} in the dX / backward timing")
     del dxs
 
-    elapsed_ms, unfused_ms, e2e_ms, dx_ms, bwd_ms, graph_ms, unfused_graph_ms = max_over_ranks(
-        [elapsed_ms, unfused_ms, e2e_ms, timed["dx"], timed["backward"], graph_ms, unfused_graph_ms], world, dev)
+    elapsed_ms, unfused_ms, e2e_ms, dx_ms, bwd_ms, graph_ms, unfused_graph_ms, per_layer_ms = max_over_ranks(
+        [elapsed_ms, unfused_ms, e2e_ms, timed["dx"], timed["backward"], graph_ms, unfused_graph_ms, per_layer_ms],
+        world, dev)
     ms_step = elapsed_ms / args.steps
     return dict(ms_step=ms_step, flops_step=flops_step, launch_ms=launch_ms, launches=launches,
                 unfused_ms=unfused_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, clocks=clocks.summary(),
                 grad_pool_unfused=grad_pool_unfused, mem_fused=mem0, wl=wl, dx_ms=dx_ms, bwd_ms=bwd_ms, graph_ms=graph_ms,
-                launch_pass_ms=launch_pass_ms, unfused_graph_ms=unfused_graph_ms,
+                launch_pass_ms=launch_pass_ms, unfused_graph_ms=unfused_graph_ms, per_layer_ms=per_layer_ms,
+                calls_per_step=calls_per_step, grouped=grouped,
                 dx_launch_ms=dx_launch_ms)
 
 
@@ -486,7 +519,12 @@ def run_sweep(name, opt, steps, warmup, rank, world):
             import torch.distributed as dist
             dist.barrier()
 
+    group_args = [(L["dy"], L["x"], L["w"], L["m"], L["v"], None, 0x5EED + i) for i, L in enumerate(layers)]
+
     def fused_pass():
+        fg.fused_dw_step_layers(group_args, opt, hp, t_step, stream=stream)
+
+    def per_layer_pass():
         for i, L in enumerate(layers):
             fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], None, opt, hp, t_step, seed=0x5EED + i,
                              stream=stream)
@@ -507,9 +545,13 @@ def run_sweep(name, opt, steps, warmup, rank, world):
     torch.cuda.synchronize()
     base = torch.cuda.memory_allocated()
     torch.cuda.reset_peak_memory_stats()
+    # the sweep runs at the power cap (a step is 0.16 s of full load): one call per layer and one
+    # grouped call measured within the noise of each other, so the sweep keeps one call per layer,
+    # the way a backward pass hands over its layers, and times the grouped call beside it
     with ClockSampler(torch.cuda.current_device()) as clocks:
-        fused_ms = timed(fused_pass)
+        fused_ms = timed(per_layer_pass)
     fused_pool = torch.cuda.max_memory_allocated() - base
+    grouped_ms = timed(fused_pass)
     if fg.sync_status() != 0:
         raise RuntimeError("device status after the sweep's fused steps")
     torch.cuda.reset_peak_memory_stats()
@@ -527,8 +569,9 @@ def run_sweep(name, opt, steps, warmup, rank, world):
         raise RuntimeError("device status after the sweep's two-phase steps")
     del dws, layers, act_cache
     torch.cuda.empty_cache()
-    fused_ms, unfused_ms = max_over_ranks([fused_ms, unfused_ms], world, dev)
+    fused_ms, unfused_ms, grouped_ms = max_over_ranks([fused_ms, unfused_ms, grouped_ms], world, dev)
     return dict(wl=wl, fused_ms=fused_ms, unfused_ms=unfused_ms, fused_pool=fused_pool, unfused_pool=unfused_pool,
+                grouped_ms=grouped_ms,
                 clocks=clocks.summary(), steps=steps, warmup=warmup)
 
 
@@ -627,6 +670,8 @@ def main():
                     help="dY/X format: bf16, or E4M3 codes with per-tensor or per-channel scales")
     ap.add_argument("--oracle-rows", type=int, default=0, help="rows per layer of the oracle sample (0: sized by time)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-layer-calls", action="store_true",
+                    help="time the fused step as one call per layer instead of one call over all layers")
     ap.add_argument("--sweep", default="qwen14b-sweep",
                     help="many-layer sweep timed after the main workload, fused against two-phase ('none': skip)")
     ap.add_argument("--sweep-steps", type=int, default=5)
@@ -697,13 +742,14 @@ def main():
     peak_source = (f"2 x bf16_tflops of {peaks_src} (nominal fp8/bf16 dense ratio 4.5/2.25)" if e4m3
                    else f"bf16_tflops of {peaks_src}")
     n_layers = len(r["wl"].layers)
-    avg_launch_ms = statistics.mean(r["launch_ms"])
-    flops_launch = r["flops_step"] / n_layers
+    avg_launch_ms = statistics.mean(r["launch_ms"])  # per call: the grouped call, or one layer's
+    calls = r["calls_per_step"]
+    flops_launch = r["flops_step"] / calls
     achieved = flops_launch / (avg_launch_ms * 1e-3) / 1e12
     value = job_throughput(r["flops_step"], world, r["ms_step"])
     # the epilogue side of the same launches: HBM bytes per launch over the same launch time
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    alg_bytes = algorithmic_bytes(r["wl"], args.opt, args.state, args.operands) / n_layers
+    alg_bytes = algorithmic_bytes(r["wl"], args.opt, args.state, args.operands) / calls
     traffic = _ncu_traffic(args.workload, args.opt, args.state) if not e4m3 else None
     hbm = {"unit": "GB/s", "peak": hbm_peak, "algorithmic_bytes_per_launch": alg_bytes,
            "achieved_algorithmic": alg_bytes / (avg_launch_ms * 1e-3) / 1e9,
@@ -714,6 +760,12 @@ def main():
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16", "data": "synthetic", "config": config,
+        "calls": {"fused": "one forge_fused_dw_step_layers call per step (layers on CTA pairs run together, up to 16 "
+                           "per launch)" if r["grouped"] else "one forge_fused_dw_step call per layer",
+                  "launches_per_step": r["launches"] / args.steps},
+        "per_layer": None if not r["grouped"] else {
+            "ms_per_step": r["per_layer_ms"], "value": job_throughput(r["flops_step"], world, r["per_layer_ms"]),
+            "what": "the same step as one forge_fused_dw_step call (one launch) per layer"},
         "unfused": {"ms_per_step": r["unfused_ms"], "value": job_throughput(r["flops_step"], world, r["unfused_ms"]),
                     "speedup_fused": r["unfused_ms"] / r["ms_step"],
                     "graph_ms_per_step": r["unfused_graph_ms"],
@@ -735,7 +787,7 @@ def main():
     if r["dx_launch_ms"]:  # bf16 operands only: dX = dY W needs dY in bf16
         line["dx"] = {"ms_per_step": r["dx_ms"], "value": job_throughput(r["flops_step"], world, r["dx_ms"]),
                       "unit": "TFLOP/s", "avg_launch_ms": statistics.mean(r["dx_launch_ms"]),
-                      "frac": flops_launch / (statistics.mean(r["dx_launch_ms"]) * 1e-3) / 1e12 / bf16_peak}
+                      "frac": r["flops_step"] / n_layers / (statistics.mean(r["dx_launch_ms"]) * 1e-3) / 1e12 / bf16_peak}
         line["layer_backward"] = {"ms_per_step": r["bwd_ms"],
                                   "value": job_throughput(2 * r["flops_step"], world, r["bwd_ms"]),
                                   "unit": "TFLOP/s", "what": "dX then the fused step, per layer, one stream"}
@@ -748,10 +800,13 @@ def main():
             "steps": sweep["steps"], "warmup": sweep["warmup"],
             "fused": {"ms_per_step": sweep["fused_ms"], "value": fused_v, "unit": "TFLOP/s",
                       "frac": fused_v / world / sus,
-                      "peak": sus, "peak_source": f"bf16_tflops_sustained of {peaks_src} (a step of {len(sw.layers)} launches)"},
+                      "peak": sus, "peak_source": f"bf16_tflops_sustained of {peaks_src} (a step of {len(sw.layers)} layers)",
+                      "what": "one forge_fused_dw_step call per layer (280 launches)"},
             "unfused": {"ms_per_step": sweep["unfused_ms"],
                         "value": job_throughput(sw.flops_per_step(), world, sweep["unfused_ms"]), "unit": "TFLOP/s"},
             "speedup_fused": sweep["unfused_ms"] / sweep["fused_ms"],
+            "grouped": {"ms_per_step": sweep["grouped_ms"],
+                        "what": "the fused step as one forge_fused_dw_step_layers call (launches of up to 16 layers)"},
             "grad_pool_bytes": {"fused_hbm": sweep["fused_pool"], "unfused_hbm": sweep["unfused_pool"],
                                 "what": "peak HBM allocated during the step beyond W/m/v/dY/X (torch allocator)"},
             "clocks": sweep["clocks"]}

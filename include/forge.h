@@ -155,6 +155,41 @@ FORGE_API forge_status forge_fused_dw_step(const void *dY, const void *X, void *
                                  const forge_hparams *hp, const forge_shape *shape,
                                  int64_t step, uint64_t seed, struct CUstream_st *stream);
 
+/* One layer of forge_fused_dw_step_layers: what forge_fused_dw_step takes for it. */
+typedef struct forge_layer {
+    const void *dY;   /* [T, d_out] bfloat16 */
+    const void *X;    /* [T, d_in] bfloat16 */
+    void *W;          /* [d_out, d_in] bfloat16, updated in place */
+    void *m;          /* moments as for forge_fused_dw_step (NULL where the optimizer keeps none) */
+    void *v;
+    float *qscales;   /* INT8 states: 2 * d_out * d_in / 64 scales; NULL otherwise */
+    int64_t T, d_out, d_in;
+    uint64_t seed;    /* the layer's stochastic-rounding seed */
+} forge_layer;
+
+/*
+ * forge_fused_dw_step_layers -- forge_fused_dw_step for several independent layers at once
+ * (§2 Methodology, Core mechanism, applied to every layer of a backward pass; the tile kernel's
+ * persistent loop, §4's removal of the separate optimizer launch, extended across layers).
+ *
+ *   The result is bit for bit that of calling forge_fused_dw_step on each layer in turn with the
+ *   same opt_kind, hp, step and state (every element's update and Philox counter depend only on its
+ *   own layer).  Layers whose preferred tile is a CTA pair (d_out and d_in multiples of 256, or
+ *   ragged above 1024) run together: their tiles are numbered layer after layer and visited by one
+ *   persistent schedule, up to 16 layers per launch, so the pipeline fills and drains once per
+ *   launch instead of once per layer.  Other layers (and layers with T == 0) are launched one by
+ *   one, as forge_fused_dw_step would.
+ *
+ *   layers: n_layers entries, host memory, read during the call only.  The layers must be
+ *   independent: no layer's W, m, v or qscales may overlap any other buffer of any layer.
+ *   state: a forge_state_dtype, the same for every layer.  bf16 operands only (the E4M3 entry
+ *   points take one layer per call).  Every layer is checked as forge_fused_dw_step checks its
+ *   arguments before anything is launched; an error names no layer and launches nothing.
+ */
+FORGE_API forge_status forge_fused_dw_step_layers(const forge_layer *layers, int32_t n_layers, int32_t state,
+                                                  forge_opt_kind opt_kind, const forge_hparams *hp, int64_t step,
+                                                  struct CUstream_st *stream);
+
 /*
  * forge_dw_gemm -- the weight gradient alone, written to device memory: dW [d_out,
  * d_in] binary32 row-major, dW = dY^T X accumulated in FP32.  This is the first

@@ -42,6 +42,22 @@ int main(void) {
     expect("E4M3 channel scales missing",
            forge_fused_dw_step_e4m3_channels(p, p, NULL, NULL, p, p, p, NULL, FORGE_ADAMW, &hp, &shape, 1, 0, NULL),
            FORGE_ERR_INVALID_ARGUMENT);
+    forge_layer layers[2];
+    memset(layers, 0, sizeof(layers));
+    for (int i = 0; i < 2; ++i) {
+        layers[i].dY = p; layers[i].X = p; layers[i].W = p; layers[i].m = p; layers[i].v = p;
+        layers[i].T = 256; layers[i].d_out = 512; layers[i].d_in = 256; layers[i].seed = (uint64_t)i;
+    }
+    expect("no layers", forge_fused_dw_step_layers(NULL, 0, FORGE_STATE_FP32, FORGE_ADAMW, &hp, 1, NULL), FORGE_OK);
+    expect("layers missing", forge_fused_dw_step_layers(NULL, 2, FORGE_STATE_FP32, FORGE_ADAMW, &hp, 1, NULL),
+           FORGE_ERR_INVALID_ARGUMENT);
+    layers[1].W = (char *)p + 8;
+    expect("second layer misaligned", forge_fused_dw_step_layers(layers, 2, FORGE_STATE_FP32, FORGE_ADAMW, &hp, 1, NULL),
+           FORGE_ERR_MISALIGNED);
+    layers[1].W = p;
+    layers[1].d_in = 100;
+    expect("second layer's size", forge_fused_dw_step_layers(layers, 2, FORGE_STATE_FP32, FORGE_ADAMW, &hp, 1, NULL),
+           FORGE_ERR_INVALID_ARGUMENT);
     forge_shape empty = {0, 0, 256, FORGE_STATE_FP32, 0};
     expect("empty layer", forge_fused_dw_step(NULL, NULL, NULL, NULL, NULL, NULL, FORGE_ADAMW, &hp, &empty, 1, 0, NULL),
            FORGE_OK);

@@ -249,3 +249,24 @@ def test_hyperparameter_struct_follows_a_mutable_object():
     frozen = Hparams(lr=2e-3)
     assert fg._hp_arg(frozen)._obj is fg._hp_arg(Hparams(lr=2e-3))._obj
     assert fg._hp_arg({"lr": 3e-3})._obj.lr == pytest.approx(3e-3)
+
+
+def test_layers_call_checks_every_layer_before_launching(L):
+    """forge_fused_dw_step_layers: each layer is checked as forge_fused_dw_step would check it, and
+    an error in any layer launches nothing (no device is needed to see the argument errors)."""
+    hps = fg.hparams_struct()
+    arr = (fg.ForgeLayer * 3)()
+    for i in range(3):
+        arr[i] = fg.ForgeLayer(0x10000, 0x10000, 0x10000, 0x10000, 0x10000, None, 256, 512, 256, i)
+    call = lambda n, state=0, step=1: L.forge_fused_dw_step_layers(arr, n, state, 0, ctypes.byref(hps), step, None)
+    assert call(0) == 0
+    assert call(3, step=0) == 1                      # step < 1
+    arr[2].W = 0x10008
+    assert call(3) == 3                              # the third layer's W is misaligned
+    assert call(2) == 4                              # the first two pass the checks; no device here
+    arr[2].W = 0x10000
+    arr[1].m = None
+    assert call(3) == 1                              # AdamW keeps m
+    arr[1].m = 0x10000
+    assert call(3, state=1) == 1                     # INT8 states need qscales
+    assert L.forge_fused_dw_step_layers(None, 2, 0, 0, ctypes.byref(hps), 1, None) == 1
