@@ -126,22 +126,31 @@ __device__ __forceinline__ float int8_at_flipped(uint32_t flipped, int k) {
                      8388736.0f);
 }
 
-// Encoding against one scale s: r = RN(1/s), q = RN(x r).  Then |q - x/s| <= |x/s| (2^-23 + 2^-48)
-// < 2^-16 (|x| <= absmax, so |x/s| <= 127.00001), and RN(x/s) lies within 2^-18 of x/s, so the two
-// differ by less than 2^-15.  Where q is farther than 2^-14 from every half-integer both round to
-// the same integer, which RN(q + 1.5 * 2^23) holds in its low mantissa bits (|q| < 2^22); the
-// clamp cannot act (|q| < 127.5).  Elsewhere -- near or at a tie, s subnormal, 0 or not finite, x
-// NaN -- the code comes from the IEEE division of int8_code.
+// Encoding against one scale s: r = rcp.approx(s), the hardware reciprocal (at most 2^-23 absolute
+// error for s in [1, 2), so |r s - 1| <= 2^-22 at any normal s), and q = RN(x r).  Then
+// |q - x/s| <= |x/s| (2^-22 + 2^-24 + 2^-46) < 3.8e-5 (|x| <= absmax, so |x/s| <= 127.00001), and
+// RN(x/s) lies within 2^-18 of x/s, so the two differ by less than 4.2e-5 < 2^-14.  Where q is
+// farther than 2^-14 from every half-integer both round to the same integer, which
+// RN(q + 1.5 * 2^23) holds in its low mantissa bits (|q| < 2^22); the clamp cannot act
+// (|q| < 127.5).  Elsewhere -- near or at a tie, s subnormal, 0 or not finite, x NaN -- the code
+// comes from the IEEE division of int8_code.  The reciprocal only chooses between the two paths:
+// every code equals clamp(rne(RN(x/s))) either way.
 struct Int8Coder {
     float s, r;
     bool fast;  // s normal and 1/s normal
 };
 
+__device__ __forceinline__ float rcp_approx(float s) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+    return r;
+}
+
 __device__ __forceinline__ Int8Coder int8_coder(float s) {
     Int8Coder c;
     c.s = s;
     c.fast = s >= 0x1p-126f && s <= 0x1p125f;
-    c.r = c.fast ? __frcp_rn(s) : 0.0f;
+    c.r = c.fast ? rcp_approx(s) : 0.0f;
     return c;
 }
 
