@@ -289,8 +289,8 @@ __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int 
 // Dense states: binary32 (BF16S = false) or bfloat16 rounded stochastically with their own Philox
 // streams (BF16S = true).  The update always runs on binary32 moments; only their storage differs.
 template <int OPT, int WIDTH, bool BF16S, bool SCALE, int R>
-__device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int col0, uint32_t taddr,
-                                              uint8_t* strip, int row0n = -1, int col0n = 0) {
+__device__ __forceinline__ void epi_opt_dense(const TileArgs& a, const OptScalars& s, int row0, int col0,
+                                              uint32_t taddr, uint8_t* strip, int row0n = -1, int col0n = 0) {
     using Tr = OptTraits<OPT>;
     constexpr int kSW = BF16S ? 4 : 8;  // 32-bit words holding a lane's 8 moment values
     const int lane = threadIdx.x & 31;
@@ -364,8 +364,8 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, int row0, int c
                         if constexpr (Tr::kM) { m0 = __uint_as_float(m[r][j]); m1 = __uint_as_float(m[r][j + 1]); }
                         if constexpr (Tr::kV) { v0 = __uint_as_float(v[r][j]); v1 = __uint_as_float(v[r][j + 1]); }
                     }
-                    const float w0 = opt_update<OPT, true>(__uint_as_float(g[j]), bf16_lo(wp), m0, v0, a.s);
-                    const float w1 = opt_update<OPT, true>(__uint_as_float(g[j + 1]), bf16_hi(wp), m1, v1, a.s);
+                    const float w0 = opt_update<OPT, true>(__uint_as_float(g[j]), bf16_lo(wp), m0, v0, s);
+                    const float w1 = opt_update<OPT, true>(__uint_as_float(g[j + 1]), bf16_hi(wp), m1, v1, s);
                     w[r][j >> 1] = sr_bf16(w0, sr_r16(p, j)) | (sr_bf16(w1, sr_r16(p, j + 1)) << 16);
                     if constexpr (BF16S) {
                         if constexpr (Tr::kM) m[r][j >> 1] = sr_bf16(m0, sr_r16(pm, j)) | (sr_bf16(m1, sr_r16(pm, j + 1)) << 16);
@@ -491,7 +491,8 @@ __device__ __forceinline__ void strip_load_run(const uint8_t* strip, uint32_t r,
 }
 
 template <int OPT>
-__device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e, bool ok, const uint32_t (&g)[8],
+__device__ __forceinline__ void int8_row_update(const TileArgs& a, const OptScalars& s, size_t e, bool ok,
+                                                const uint32_t (&g)[8],
                                                 const Int8RowIn<OPT>& in) {
     using Tr = OptTraits<OPT>;
     const Philox4 p = sr_words(e >> 3, a.seed, a.step);
@@ -503,7 +504,7 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e, boo
         const float wf = (j & 1) ? bf16_hi(in.w[j >> 1]) : bf16_lo(in.w[j >> 1]);
         float mm = Tr::kM ? __fmul_rn(int8_at_flipped(in.mq[j >> 2], j & 3), in.ms) : 0.f;
         float vv = Tr::kV ? __fmul_rn(int8_at_flipped(in.vq[j >> 2], j & 3), in.vs) : 0.f;
-        const float wn = opt_update<OPT, false>(__uint_as_float(g[j]), wf, mm, vv, a.s);
+        const float wn = opt_update<OPT, false>(__uint_as_float(g[j]), wf, mm, vv, s);
         const uint32_t b = sr_bf16(wn, sr_r16(p, j));
         wo[j >> 1] = (j & 1) ? (wo[j >> 1] | (b << 16)) : b;
         mn[j] = mm;
@@ -555,8 +556,8 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, size_t e, boo
 }
 
 template <int OPT, int WIDTH, bool SCALE, bool PREFETCH>
-__device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int col0, uint32_t taddr,
-                                             uint8_t* strip) {
+__device__ __forceinline__ void epi_opt_int8(const TileArgs& a, const OptScalars& s, int row0, int col0,
+                                             uint32_t taddr, uint8_t* strip) {
     static_assert(WIDTH % 64 == 0, "whole quantisation blocks");
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t q = lane & 7u, rsub = lane >> 3;  // column run (8 columns) and first row of this lane
@@ -580,7 +581,7 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
                 if (k < 7) int8_row_load<OPT>(a, e0 + (k + 1) * row_step, row + 4 * (k + 1) < a.d_out, in[(k + 1) & 1]);
                 uint32_t g[8];
                 strip_load_run(half, rsub + 4u * k, q & 3u, g);
-                int8_row_update<OPT>(a, e0 + k * row_step, row + 4 * k < a.d_out, g, in[k & 1]);
+                int8_row_update<OPT>(a, s, e0 + k * row_step, row + 4 * k < a.d_out, g, in[k & 1]);
             }
         } else {
             // enough warps per scheduler to cover the load latency without a second row in flight
@@ -590,7 +591,7 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, int row0, int co
                 int8_row_load<OPT>(a, e0 + k * row_step, row + 4 * k < a.d_out, in);
                 uint32_t g[8];
                 strip_load_run(half, rsub + 4u * k, q & 3u, g);
-                int8_row_update<OPT>(a, e0 + k * row_step, row + 4 * k < a.d_out, g, in);
+                int8_row_update<OPT>(a, s, e0 + k * row_step, row + 4 * k < a.d_out, g, in);
             }
         }
         __syncwarp();  // every lane has read the strips before the next block overwrites them
@@ -692,7 +693,9 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
     if constexpr (CL > 1) cluster_sync();  // the peer's barriers exist before anything signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const TileArgs& a0 = grp.layer[0];  // status word, wait limits and test switch: the same for every layer
+    // status word, wait limits, test switch and optimizer scalars (one optimizer, hyperparameter set and
+    // step per launch): the same for every layer, read at a fixed offset of the parameter bank
+    const TileArgs& a0 = grp.layer[0];
     const AbortCtx ab{abort_flag, a0.status, a0.wait_limit_ns};
     const int num_tiles = grp.tile_start[grp.n];
     uint64_t n_issued = 0;   // producer: stages passed (armed and copied, but for the withheld one)
@@ -865,9 +868,9 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
                     col0n = nbn * BN + half * kWidth;
                 }
                 epi_opt_dense<OPT, kWidth, EPI == kEpiOptBF16, kScale, (C::kEpiWarps == 8 ? 4 : 1)>(
-                    a, row0, col0, taddr, strip, row0n, col0n);
+                    a, a0.s, row0, col0, taddr, strip, row0n, col0n);
             }
-            else epi_opt_int8<OPT, kWidth, kScale, C::kEpiWarps == 8>(a, row0, col0, taddr, strip);
+            else epi_opt_int8<OPT, kWidth, kScale, C::kEpiWarps == 8>(a, a0.s, row0, col0, taddr, strip);
             // the buffer's TMEM columns may be overwritten once every lane's reads of them have
             // completed (tcgen05.wait::ld) and been ordered before the arrive (tcgen05 fence); the
             // arrive publishes no memory, so it is relaxed
