@@ -108,3 +108,14 @@ def test_roofline_bound_is_the_slower_unit():
     r8 = bench.roofline_entry(flops, b8, 0.28, 2 * 1938.1, 6789.0, None, {}, "t", "h")
     assert r8["bound"] == "hbm" and r8["unit"] == "GB/s"
     assert r8["achieved"] == pytest.approx(b8 / 0.28e-3 / 1e9) and r8["other"]["bound"] == "tensor"
+
+
+def test_tensor_peak_follows_the_power_cap():
+    """A timed region whose clock samples saw the power cap is held to the sustained GEMM figure;
+    any other to the burst figure (and to the fallback when no peaks file gives one)."""
+    peaks = {"bf16_tflops": 1938.1, "bf16_tflops_sustained": 1717.2}
+    assert bench.tensor_peak_for(peaks, {"reasons": ["sw_power_cap"]}) == (1717.2, "bf16_tflops_sustained")
+    assert bench.tensor_peak_for(peaks, {"reasons": []}) == (1938.1, "bf16_tflops")
+    assert bench.tensor_peak_for(peaks, None) == (1938.1, "bf16_tflops")
+    assert bench.tensor_peak_for({"bf16_tflops": 1900.0}, {"reasons": ["sw_power_cap"]}) == (1900.0, "bf16_tflops")
+    assert bench.tensor_peak_for({}, {"reasons": []})[0] == bench.FALLBACK_PEAKS["bf16_tflops"]
