@@ -43,7 +43,12 @@ constexpr int kBK = 64;          // tokens per pipeline stage = 128 bytes of one
 constexpr int kUmmaK = 16;       // K of one kind::f16 MMA
 constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
 
-enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3, kEpiOptBF16 = 4 };
+// kEpiOptINT8Deep: INT8 states on a CTA pair with 8 epilogue warps instead of 16.  Half the
+// transpose strips leave shared memory for 5 operand stages instead of 3, which a long token run,
+// where the mainloop rather than the INT8 epilogue sets the pace, needs to keep the tensor core fed.
+enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3, kEpiOptBF16 = 4,
+                     kEpiOptINT8Deep = 5 };
+__host__ __device__ constexpr bool int8_epi(int epi) { return epi == kEpiOptINT8 || epi == kEpiOptINT8Deep; }
 
 // Operand formats.  Either way a stage row is 128 bytes (the swizzle span) and a stage of one
 // operand is 16 KiB per 128 MN rows: 64 tokens of bf16, or 128 tokens of E4M3, whose products the
@@ -62,7 +67,7 @@ template <int BN, int CG, int EPI, int OPS = kOpsBF16>
 struct TileCfg {
     // 64-column tiles (one X box per stage, N = 64 MMAs) serve small layers with bf16 operands and
     // epilogues that work on 32-column runs; E4M3 rows hold 128 elements, INT8 blocks 64 per warp
-    static_assert(BN == 128 || BN == 256 || (BN == 64 && CG == 1 && OPS == kOpsBF16 && EPI != kEpiOptINT8),
+    static_assert(BN == 128 || BN == 256 || (BN == 64 && CG == 1 && OPS == kOpsBF16 && !int8_epi(EPI)),
                   "tile width");
     static_assert(CG == 1 || CG == 2, "CTA group");
     static constexpr int kBLoad = BN / CG;         // X columns staged by this CTA
@@ -72,16 +77,16 @@ struct TileCfg {
     static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator (128 lanes x BN)
     // epilogue warps: two per TMEM lane quarter, each owning half the tile's columns.  A CTA pair
     // runs four per quarter, one 64-column block each, where the epilogue rather than the
-    // operand stream sets the pace: the INT8-state epilogue, whose dependent arithmetic needs
-    // more warps per scheduler to keep issuing, and any optimizer epilogue behind the E4M3
-    // mainloop, which is half as long as the bf16 one
+    // operand stream sets the pace: the INT8-state epilogue (kEpiOptINT8; not kEpiOptINT8Deep),
+    // whose dependent arithmetic needs more warps per scheduler to keep issuing, and any optimizer
+    // epilogue behind the E4M3 mainloop, which is half as long as the bf16 one
     static constexpr bool kWideEpi =
         CG == 2 && (EPI == kEpiOptINT8 || (OPS == kOpsE4M3 && (EPI == kEpiOptFP32 || EPI == kEpiOptBF16)));
     static constexpr int kEpiWarps = kWideEpi ? 16 : 8;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     // one warp's 32 x 32 FP32 transpose strip; the INT8 epilogue stages two (a 64-column block);
     // the input-gradient epilogue stores rows as they come out of TMEM and needs none
-    static constexpr int kStripBytes = EPI == kEpiDX ? 0 : (EPI == kEpiOptINT8 ? 2 : 1) * 32 * 32 * 4;
+    static constexpr int kStripBytes = EPI == kEpiDX ? 0 : (int8_epi(EPI) ? 2 : 1) * 32 * 32 * 4;
     static constexpr int kEpiBytes = kEpiWarps * kStripBytes;
     static constexpr int kBarrierBytes = 256;
     static constexpr int kMaxSmem = 232448;

@@ -141,3 +141,26 @@ def test_withheld_stage_in_a_grouped_launch():
     assert fg.sync_status() == 0
     for L, R in zip(layers, ref):
         assert _same(L["w"], R["w"]) and _same(L["m"], R["m"])
+
+
+@pytest.mark.parametrize("Ts", [(8192, 6144), (8192, 4096)])
+def test_int8_layers_with_long_token_runs_equal_per_layer_calls(Ts):
+    """INT8 states on CTA pairs take the 8-warp epilogue from 6144 tokens on, in a single-layer
+    call and in a group whose layers all have that many; a group with a shorter layer keeps the
+    16-warp one.  The two epilogues do the same per-element arithmetic, so the grouped call still
+    equals the per-layer calls bit for bit either way."""
+    hp = default_hparams("adamw", lr=1e-3)
+    shapes = [(2048, 1280, Ts[0]), (1024, 1536, Ts[1])]
+    layers = _states("adamw", shapes, "int8", seed=61)
+    ref = _clone(layers)
+    before = fg.launch_count()
+    fg.fused_dw_step_layers([(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], L["seed"]) for L in layers], "adamw",
+                            hp, 4)
+    assert fg.launch_count() - before == 1
+    for L in ref:
+        fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], "adamw", hp, 4, seed=L["seed"])
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    for i, (L, R) in enumerate(zip(layers, ref)):
+        for k in ("w", "m", "v", "q"):
+            assert _same(L[k], R[k]), f"layer {i} {shapes[i]}: {k} differs"

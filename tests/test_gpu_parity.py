@@ -188,6 +188,36 @@ def test_fused_int8_matches_oracle(opt, d_out, d_in):
         assert_moments(q[n64:], ref["v_scales"].ravel(), "v scales")
 
 
+@pytest.mark.parametrize("opt, T", [("adamw", 8192), ("lion", 6144), ("rmsprop", 4096)])
+def test_fused_int8_long_token_runs_match_oracle(opt, T):
+    """INT8 states on CTA pairs over long token runs: from 6144 tokens on the pair kernel runs its
+    8-warp epilogue (two 64-column blocks per warp, the next row's inputs loaded while a row
+    updates); at 4096 the 16-warp one.  Codes and scales against the oracle with the summation
+    allowance of T tokens."""
+    d_out, d_in = PAIR
+    assert fg.launch_shape(d_out, d_in, T)["cluster"] == 2
+    dy, x, w, _, _ = _layer(d_out, d_in, T, opt, seed=44)
+    mq, ms, vq, vs = _int8_state(w.shape, 19)
+    hp = default_hparams(opt, lr=1e-3)
+    W, M, V, Q = dev(w), torch.from_numpy(mq).cuda(), torch.from_numpy(vq).cuda(), _qscales_tensor(ms, vs)
+    fg.fused_dw_step(dy.cuda(), x.cuda(), W, M, V, Q, opt, hp, 6, seed=23)
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    ref = ostep.fused_step(opt, bits(dy), bits(x), bits(w), mq, vq, hp, 6, 23, "int8", ms, vs)
+    e = np.arange(d_out * d_in, dtype=np.uint64).reshape(d_out, d_in)
+    rt = moment_rtol(T)
+    extra = gradient_sensitivity(opt, ref["g"], bits(w), mq, vq, hp, 6, 23, e, rt, "int8", ms, vs)
+    assert_weights(bits(W), ref["W"], w_old_bits=bits(w), extra_tol=extra)
+    q = Q.cpu().numpy()
+    n64 = w.numel() // 64
+    if ref["m"] is not None:
+        assert_codes(M.cpu().numpy(), ref["m"], "m codes")
+        assert_moments(q[:n64], ref["m_scales"].ravel(), "m scales", rtol=rt)
+    if ref["v"] is not None:
+        assert_codes(V.cpu().numpy(), ref["v"], "v codes")
+        assert_moments(q[n64:], ref["v_scales"].ravel(), "v scales", rtol=moment_rtol(T, squared=True))
+
+
 @pytest.mark.parametrize("opt, d_out, d_in", [(o, d_out, d_in) for o in ("adamw", "lion", "adagrad")
                                                for d_out, d_in in SHAPES])
 def test_fused_equals_unfused_bitwise(opt, d_out, d_in):
