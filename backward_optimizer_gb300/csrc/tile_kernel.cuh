@@ -315,7 +315,9 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, const OptScalar
         for (int kk = 0; kk < 4; kk += R) {
             uint32_t w[R][4], m[R][kSW], v[R][kSW];
             bool ok[R];
-            // the W/m/v loads do not depend on the gradient: issue them before the TMEM read
+            // the W/m/v loads do not depend on the gradient: issue them before the TMEM read.  They
+            // are read once: L2 may evict them first, ahead of the operand slices
+            const uint64_t once = policy_evict_first();
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int k = kk + r;
@@ -323,13 +325,13 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, const OptScalar
                 // a run outside the layer loads the layer's first run instead (always valid) and
                 // stores nothing, so the loads stay unconditional
                 const size_t el = ok[r] ? lane_base + k * row_step + c : 0;
-                ld_v4(a.W + el, w[r]);
+                ld_v4_policy(a.W + el, w[r], once);
                 if constexpr (BF16S) {
-                    if constexpr (Tr::kM) ld_v4(static_cast<uint16_t*>(a.m) + el, m[r]);
-                    if constexpr (Tr::kV) ld_v4(static_cast<uint16_t*>(a.v) + el, v[r]);
+                    if constexpr (Tr::kM) ld_v4_policy(static_cast<uint16_t*>(a.m) + el, m[r], once);
+                    if constexpr (Tr::kV) ld_v4_policy(static_cast<uint16_t*>(a.v) + el, v[r], once);
                 } else {
-                    if constexpr (Tr::kM) ld_v8(static_cast<float*>(a.m) + el, m[r]);
-                    if constexpr (Tr::kV) ld_v8(static_cast<float*>(a.v) + el, v[r]);
+                    if constexpr (Tr::kM) ld_v8_policy(static_cast<float*>(a.m) + el, m[r], once);
+                    if constexpr (Tr::kV) ld_v8_policy(static_cast<float*>(a.v) + el, v[r], once);
                 }
                 // the next 32 columns' W/m/v into L2 now, so their loads wait on L2 rather than DRAM;
                 // in the last step, the first 32 columns of this warp's next tile
