@@ -47,11 +47,15 @@ cudaError_t launch_tile(const TileLaunch& l) {
         }
         configured.fetch_or(bit);
     }
-    // persistent grid: one CTA per SM (or one cluster per CL SMs), never more units than tiles
+    // persistent grid: one CTA per SM (or one cluster per CL SMs), never more units than tiles.
+    // Pair kernels with bf16 operands split a short last wave into half tiles (schedule.h).
     const int cap = CL == 1 ? l.num_sms : max_clusters[dev].load();
-    const int units = l.num_tiles < cap ? l.num_tiles : cap;
+    constexpr bool kSplitTail = CG == 2 && BN == 256 && OPS == kOpsBF16;
+    const int split_from = kSplitTail ? split_tail_from(l.num_tiles, cap) : l.num_tiles;
+    const int launch_tiles = l.num_tiles + (l.num_tiles - split_from);
+    const int units = launch_tiles < cap ? launch_tiles : cap;
     cfg.gridDim = dim3(units * CL, 1, 1);
-    return cudaLaunchKernelEx(&cfg, kernel, *static_cast<const TileGroup<G>*>(l.group));
+    return cudaLaunchKernelEx(&cfg, kernel, *static_cast<const TileGroup<G>*>(l.group), split_from);
 }
 
 // CTA count and cluster size a launch_tile<..., BN, CL> call with `num_tiles` tiles would use.

@@ -38,4 +38,26 @@ FORGE_HD void tile_coords(int tile, const TileOrder& o, int& mb, int& nb) {
     nb = o.raster_cols ? p : q;
 }
 
+// First tile of a pair launch's split tail.  The persistent grid runs `units` pairs; when the last
+// wave of 256 x 256 tiles would occupy at most half of them, its tiles run as two 256 x 128 halves
+// each (the kernel numbers them after the whole tiles), so that the wave occupies up to all of the
+// pairs.  Returns `tiles` when nothing is split: a single wave, a full last wave, or one more than
+// half full (two rounds of halves would take longer than one of whole tiles).
+FORGE_HD int split_tail_from(int tiles, int units) {
+    if (units <= 0 || tiles <= units) return tiles;
+    const int rest = tiles % units;
+    return (rest > 0 && 2 * rest <= units) ? tiles - rest : tiles;
+}
+
+// Launch tile t -> the tile of the layers' order it covers (returned) and its part: -1 the whole
+// tile, 0 or 1 the left or right 128 columns of it.  Tiles from `split_from` on are halves.
+FORGE_HD int tail_tile(int t, int split_from, int& part) {
+    if (t < split_from) {
+        part = -1;
+        return t;
+    }
+    part = (t - split_from) & 1;
+    return split_from + ((t - split_from) >> 1);
+}
+
 }  // namespace forge

@@ -275,14 +275,15 @@ __device__ __forceinline__ void strip_load_row(const uint8_t* strip, int k, uint
         ld_shared_v4(base + r * 128u + (((2u * (lane & 3u) + h) ^ sub_row) << 4), &out[4 * h]);
 }
 
+// width: columns of this warp's part (WIDTH, or half of it on a split tail tile)
 template <int WIDTH, bool SCALE>
-__device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int col0, uint32_t taddr,
+__device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int col0, uint32_t taddr, int width,
                                                uint8_t* strip) {
     const int lane = threadIdx.x & 31;
     const int row = row0 + (lane >> 2), col = col0 + 8 * (lane & 3);
     float* base = a.dW + static_cast<size_t>(row) * a.d_in + col;
 #pragma unroll 1
-    for (int c = 0; c < WIDTH; c += 32) {
+    for (int c = 0; c < width; c += 32) {
         uint32_t t[4][8];
         strip_transpose<SCALE>(taddr + c, strip, t, a, row0 + lane, col0 + c);
         if (col + c < a.d_in) {
@@ -297,7 +298,8 @@ __device__ __forceinline__ void epi_store_grad(const TileArgs& a, int row0, int 
 // streams (BF16S = true).  The update always runs on binary32 moments; only their storage differs.
 template <int OPT, int WIDTH, bool BF16S, bool SCALE, int R>
 __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, const OptScalars& s, int row0, int col0,
-                                              uint32_t taddr, uint8_t* strip, int row0n = -1, int col0n = 0) {
+                                              uint32_t taddr, int width, uint8_t* strip, int row0n = -1,
+                                              int col0n = 0) {
     using Tr = OptTraits<OPT>;
     constexpr int kSW = BF16S ? 4 : 8;  // 32-bit words holding a lane's 8 moment values
     const int lane = threadIdx.x & 31;
@@ -306,7 +308,7 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, const OptScalar
     const size_t lane_base = static_cast<size_t>(row) * a.d_in + col;
     const size_t row_step = static_cast<size_t>(8) * a.d_in;
 #pragma unroll 1
-    for (int c = 0; c < WIDTH; c += 32) {
+    for (int c = 0; c < width; c += 32) {
         // R of the four row groups hold their W/m/v in registers at once: all four with two
         // epilogue warps per scheduler, so that every group's loads overlap the TMEM read; one
         // with four warps per scheduler, whose 96 registers a thread leave no room for more and
@@ -335,7 +337,7 @@ __device__ __forceinline__ void epi_opt_dense(const TileArgs& a, const OptScalar
                 }
                 // the next 32 columns' W/m/v into L2 now, so their loads wait on L2 rather than DRAM;
                 // in the last step, the first 32 columns of this warp's next tile
-                const bool last = c + 32 >= WIDTH;
+                const bool last = c + 32 >= width;
                 const int rn = last ? row0n + (lane >> 2) + 8 * k : row + 8 * k;
                 const int cn = last ? col0n + 8 * (lane & 3) : col + c + 32;
                 if ((!last || row0n >= 0) && cn < a.d_in && rn < a.d_out) {
@@ -429,11 +431,11 @@ __device__ __forceinline__ void prefetch_first_run(const TileArgs& a, int row0, 
 // not a multiple of the tile height) are computed on TMA's zero fill and not stored; past the last
 // column (d_in a multiple of 8 only) a 16-column piece shrinks to its first 8 or is skipped.
 template <int WIDTH>
-__device__ __forceinline__ void epi_store_dx(const TileArgs& a, int row0, int col0, uint32_t taddr) {
+__device__ __forceinline__ void epi_store_dx(const TileArgs& a, int row0, int col0, uint32_t taddr, int width) {
     const int row = row0 + static_cast<int>(threadIdx.x & 31u);
     uint16_t* out = a.dX + static_cast<size_t>(row) * a.d_in + col0;
 #pragma unroll 1
-    for (int c = 0; c < WIDTH; c += 32) {
+    for (int c = 0; c < width; c += 32) {
         uint32_t g[32];
         tmem_ld_32x32b_x32(taddr + c, g);  // warp-wide: every lane takes part, stored or not
         tmem_ld_wait(g);
@@ -564,16 +566,20 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, const OptScal
     }
 }
 
+// width: columns of this warp's part (a multiple of 64).  krange: the row iterations k (rows
+// rsub + 4k) this warp updates, first | (end << 4): all eight, or on a split tail tile, where the
+// 16-warp epilogue (no PREFETCH) gives each 64-column block to two warps, k < 4 or k >= 4.  Each
+// warp still stages the block's whole gradient strips.
 template <int OPT, int WIDTH, bool SCALE, bool PREFETCH>
 __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, const OptScalars& s, int row0, int col0,
-                                             uint32_t taddr, uint8_t* strip) {
+                                             uint32_t taddr, int width, uint8_t* strip, int krange) {
     static_assert(WIDTH % 64 == 0, "whole quantisation blocks");
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t q = lane & 7u, rsub = lane >> 3;  // column run (8 columns) and first row of this lane
     const uint8_t* half = strip + (q >> 2) * 4096;    // the 32-column strip holding the run
     const int row = row0 + static_cast<int>(rsub);
 #pragma unroll 1
-    for (int c = 0; c < WIDTH; c += 64) {
+    for (int c = 0; c < width; c += 64) {
         // d_in is a multiple of 64, so a 64-column block lies wholly inside or outside the layer:
         // the same for every lane of the warp
         if (col0 + c >= a.d_in) break;
@@ -595,7 +601,7 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, const OptScalars
         } else {
             // enough warps per scheduler to cover the load latency without a second row in flight
 #pragma unroll 1
-            for (int k = 0; k < 8; ++k) {
+            for (int k = krange & 15; k < (krange >> 4); ++k) {
                 Int8RowIn<OPT> in;
                 int8_row_load<OPT>(a, e0 + k * row_step, row + 4 * k < a.d_out, in);
                 uint32_t g[8];
@@ -645,7 +651,7 @@ __device__ __forceinline__ void drain_copies(uint64_t* full, uint64_t n_own, uin
 
 template <int BN, int CL, int EPI, int OPT, int OPS, int G>
 __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
-    forge_tile_kernel(const __grid_constant__ TileGroup<G> grp) {
+    forge_tile_kernel(const __grid_constant__ TileGroup<G> grp, const int split_from) {
     static_assert(CL == 1 || CL == 2, "cluster size");
     static_assert(OPS == kOpsBF16 || EPI != kEpiDX, "the input gradient takes bf16 operands");
     using O = OperandTraits<OPS>;
@@ -706,7 +712,11 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
     // step per launch): the same for every layer, read at a fixed offset of the parameter bank
     const TileArgs& a0 = grp.layer[0];
     const AbortCtx ab{abort_flag, a0.status, a0.wait_limit_ns};
-    const int num_tiles = grp.tile_start[grp.n];
+    // pair kernels with bf16 operands run the tiles from split_from on as two 256 x 128 halves
+    // (schedule.h, split_tail_from); the others take split_from = the tile count
+    constexpr bool kSplitTail = CG == 2 && BN == 256 && OPS == kOpsBF16;
+    const int layer_tiles = grp.tile_start[grp.n];
+    const int num_tiles = kSplitTail ? layer_tiles + (layer_tiles - split_from) : layer_tiles;
     uint64_t n_issued = 0;   // producer: stages passed (armed and copied, but for the withheld one)
     int64_t withheld = -1;   // producer: the stage the test switch left without this CTA's copies
 
@@ -719,14 +729,20 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
             const uint64_t keep = policy_evict_last();
             int l = 0;
             for (int tile = first_tile; ok && tile < num_tiles; tile += tile_stride) {
-                l = layer_of(grp, tile, l);
+                int part = -1;
+                const int ot = kSplitTail ? tail_tile(tile, split_from, part) : tile;
+                l = layer_of(grp, ot, l);
                 const TileArgs& a = grp.layer[l];
                 const CUtensorMap* tmap_dy = &grp.maps[2 * l];
                 const CUtensorMap* tmap_x = &grp.maps[2 * l + 1];
                 int mb, nb;
-                tile_coords(tile - grp.tile_start[l], a.order, mb, nb);
+                tile_coords(ot - grp.tile_start[l], a.order, mb, nb);
                 const int row_a = mb * kBM * CG + static_cast<int>(rank) * kBM;
-                const int col_b = nb * BN + static_cast<int>(rank) * C::kBLoad;
+                // a half tile's 128 columns: each CTA of the pair stages 64 of them in its first box
+                // (its second box, still copied so that every stage carries the same bytes, holds
+                // the next 64 columns, which the N = 128 MMA does not read)
+                const int col_b = part < 0 ? nb * BN + static_cast<int>(rank) * C::kBLoad
+                                           : nb * BN + part * (BN / 2) + static_cast<int>(rank) * (C::kBLoad / 2);
                 const int kblocks = a.k_blocks;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, ab)) { ok = false; break; }
@@ -786,13 +802,17 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
             // ------------------------------------------------ MMA issuer (the even CTA of a pair)
             constexpr uint32_t idesc = OPS == kOpsE4M3 ? idesc_e4m3_f32(kBM * CG, BN, true, true)
                                                        : idesc_bf16_f32(kBM * CG, BN, !kAKMajor, true);
+            constexpr uint32_t idesc_half = idesc_bf16_f32(kBM * CG, BN / 2, !kAKMajor, true);  // split tail
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, issued_any = false;
             int l = 0;
             for (int tile = first_tile; ok && tile < num_tiles; tile += tile_stride) {
-                l = layer_of(grp, tile, l);
+                int part = -1;
+                const int ot = kSplitTail ? tail_tile(tile, split_from, part) : tile;
+                l = layer_of(grp, ot, l);
                 const int kblocks = grp.layer[l].k_blocks;
+                const uint32_t id = part < 0 ? idesc : idesc_half;
                 if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, ab)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -812,8 +832,8 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
                         const uint64_t ad = kAKMajor ? smem_desc_sw128(a_base + kk * 32, 16, 1024)
                                                      : smem_desc_sw128(a_base + kk * O::kStepBytes, O::kBlockBytes, 1024);
                         const uint64_t bd = smem_desc_sw128(b_base + kk * O::kStepBytes, O::kBlockBytes, 1024);
-                        if constexpr (OPS == kOpsE4M3) tc_mma_e4m3<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                        else tc_mma_bf16<CG>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        if constexpr (OPS == kOpsE4M3) tc_mma_e4m3<CG>(d_tmem, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
+                        else tc_mma_bf16<CG>(d_tmem, ad, bd, id, (kb | kk) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
                     // the slot is free once read: tell both CTAs of the pair, whose copies fill it
@@ -836,50 +856,81 @@ __global__ void __launch_bounds__(TileCfg<BN, CL, EPI, OPS>::kThreads, 1)
         const int quarter = warp & 3;   // a warp may only touch TMEM lanes 32*(warp%4) .. +31
         const int half = e >> 2;                // column part owned by this warp
         constexpr int kWidth = BN / (C::kEpiWarps / 4);
+        // this warp's columns within the tile's accumulator (offset, width) and, for the 16-warp
+        // INT8 epilogue, its row iterations (epi_opt_int8's krange): a half tile's 128 columns are
+        // split between the column parts (parts of 128 columns take 64), or, with 64-column parts,
+        // two parts share a block and split its rows
+        auto cols_of = [&](int part, int& off, int& width, int& krange) {
+            off = half * kWidth;
+            width = kWidth;
+            krange = 8 << 4;
+            if (kSplitTail && part >= 0) {
+                if constexpr (kWidth >= 128) {
+                    width = kWidth / 2;
+                    off = half * width;
+                } else {
+                    off = (half & 1) * kWidth;
+                    krange = (half >> 1) ? (4 | (8 << 4)) : (4 << 4);
+                }
+            }
+        };
         if constexpr (EPI == kEpiOptFP32 || EPI == kEpiOptBF16) {
             if (first_tile < num_tiles) {
-                const int l0 = layer_of(grp, first_tile, 0);
-                int mb, nb;
-                tile_coords(first_tile - grp.tile_start[l0], grp.layer[l0].order, mb, nb);
-                prefetch_first_run<OPT, EPI == kEpiOptBF16>(
-                    grp.layer[l0], mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32, nb * BN + half * kWidth);
+                int part = -1;
+                const int ot = kSplitTail ? tail_tile(first_tile, split_from, part) : first_tile;
+                const int l0 = layer_of(grp, ot, 0);
+                int mb, nb, off, width, krange;
+                tile_coords(ot - grp.tile_start[l0], grp.layer[l0].order, mb, nb);
+                cols_of(part, off, width, krange);
+                prefetch_first_run<OPT, EPI == kEpiOptBF16>(grp.layer[l0],
+                                                            mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32,
+                                                            nb * BN + (part > 0 ? BN / 2 : 0) + off);
             }
         }
         int acc = 0;
         uint32_t acc_phase = 0;
         int l = 0;
         for (int tile = first_tile; tile < num_tiles; tile += tile_stride) {
-            l = layer_of(grp, tile, l);
+            int part = -1;
+            const int ot = kSplitTail ? tail_tile(tile, split_from, part) : tile;
+            l = layer_of(grp, ot, l);
             const TileArgs& a = grp.layer[l];
             // the wait for a finished accumulator spans a whole tile mainloop, which grows with T
             const AbortCtx ab_acc{abort_flag, a0.status, a.acc_wait_limit_ns};
             int mb, nb;
-            tile_coords(tile - grp.tile_start[l], a.order, mb, nb);
+            tile_coords(ot - grp.tile_start[l], a.order, mb, nb);
             int ok = 1;
             if (lane == 0) ok = wait_bounded(&acc_full[acc], acc_phase, ab_acc) ? 1 : 0;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             tc_fence_after();
+            int off, width, krange;
+            cols_of(part, off, width, krange);
             const int row0 = mb * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
-            const int col0 = nb * BN + half * kWidth;
+            const int col0 = nb * BN + (part > 0 ? BN / 2 : 0) + off;
             const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + half * kWidth);
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + off);
             uint8_t* strip = strips + e * C::kStripBytes;
-            if constexpr (EPI == kEpiDX) epi_store_dx<kWidth>(a, row0, col0, taddr);
-            else if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth, kScale>(a, row0, col0, taddr, strip);
+            if constexpr (EPI == kEpiDX) epi_store_dx<kWidth>(a, row0, col0, taddr, width);
+            else if constexpr (EPI == kEpiStoreGrad) epi_store_grad<kWidth, kScale>(a, row0, col0, taddr, width, strip);
             else if constexpr (EPI == kEpiOptFP32 || EPI == kEpiOptBF16) {
                 // the next tile's first run is prefetched only within the same layer
                 int row0n = -1, col0n = 0;
-                if (tile + tile_stride < num_tiles && layer_of(grp, tile + tile_stride, l) == l) {
-                    int mbn, nbn;
-                    tile_coords(tile + tile_stride - grp.tile_start[l], a.order, mbn, nbn);
-                    row0n = mbn * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
-                    col0n = nbn * BN + half * kWidth;
+                if (tile + tile_stride < num_tiles) {
+                    int pn = -1;
+                    const int otn = kSplitTail ? tail_tile(tile + tile_stride, split_from, pn) : tile + tile_stride;
+                    if (layer_of(grp, otn, l) == l) {
+                        int mbn, nbn, offn, widthn, kn;
+                        tile_coords(otn - grp.tile_start[l], a.order, mbn, nbn);
+                        cols_of(pn, offn, widthn, kn);
+                        row0n = mbn * kBM * CG + static_cast<int>(rank) * kBM + quarter * 32;
+                        col0n = nbn * BN + (pn > 0 ? BN / 2 : 0) + offn;
+                    }
                 }
                 epi_opt_dense<OPT, kWidth, EPI == kEpiOptBF16, kScale, (C::kEpiWarps == 8 ? 4 : 1)>(
-                    a, a0.s, row0, col0, taddr, strip, row0n, col0n);
+                    a, a0.s, row0, col0, taddr, width, strip, row0n, col0n);
             }
-            else epi_opt_int8<OPT, kWidth, kScale, C::kEpiWarps == 8>(a, a0.s, row0, col0, taddr, strip);
+            else epi_opt_int8<OPT, kWidth, kScale, C::kEpiWarps == 8>(a, a0.s, row0, col0, taddr, width, strip, krange);
             // the buffer's TMEM columns may be overwritten once every lane's reads of them have
             // completed (tcgen05.wait::ld) and been ordered before the arrive (tcgen05 fence); the
             // arrive publishes no memory, so it is relaxed

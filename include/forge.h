@@ -310,7 +310,9 @@ FORGE_API void forge_debug_withhold_next_stage(void);
  * would occupy at most half the SMs takes 128 x 128, and if those would too, 128 x 64 -- half of
  * one of the method's tiles -- except with INT8 states), CTAs per thread-block cluster (1 or 2),
  * and CTAs launched on the current device.  E4M3 operands never take 128 x 64 tiles: where the
- * query answers 128 x 64 they run on 128 x 128.  Host-side query, no launch; it reads the
+ * query answers 128 x 64 they run on 128 x 128.  With bf16 operands, a pair launch whose last wave
+ * of 256 x 256 tiles would occupy at most half of the pairs runs those last tiles as two 256 x 128
+ * halves each (the query reports the 256 x 256 tile).  Host-side query, no launch; it reads the
  * device's SM count, so it needs a device (FORGE_ERR_CUDA or FORGE_ERR_NOT_SM103 otherwise). */
 FORGE_API forge_status forge_launch_shape(const forge_shape *shape, int32_t *tile_rows, int32_t *tile_cols,
                                           int32_t *cluster, int32_t *ctas);

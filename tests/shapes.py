@@ -9,7 +9,7 @@ they exercise and check it through the launch-shape query, so a change of that r
 """
 
 PAIR = (2048, 1280)        # 8 x 5 = 40 pair tiles of 256 x 256: 80 CTAs
-PAIR_MANY = (4096, 1280)   # 80 pair tiles, more than the 76 pairs resident at once: a persistent tail
+PAIR_MANY = (4096, 1280)   # 80 pair tiles for 76 pairs: the last 4 run as 8 half tiles of 256 x 128
 WIDE = (1152, 2560)        # d_out not a multiple of 256: 9 x 10 = 90 tiles of 128 x 256
 MID = (1536, 1536)         # 36 pair tiles would fill 72 SMs: 144 tiles of 128 x 128
 SMALL = (384, 384)         # 9 tiles of 128 x 128 would fill 9 SMs: 18 tiles of 128 x 64

@@ -71,7 +71,9 @@ def _exact_gradient(dy, x):
 
 # (d_out, d_in, T): a CTA pair on 256 x 256 tiles (40 pair tiles); one CTA on 128 x 256 tiles (90);
 # a CTA pair over a long token run (T = 8192)
-SHAPES = [(2048, 1280, 256, (256, 256)), (1152, 2560, 192, (128, 256)), (2048, 1280, 8192, (256, 256))]
+# the last: 80 pair tiles, whose last 4 run as 8 half tiles (two warps per 64-column block)
+SHAPES = [(2048, 1280, 256, (256, 256)), (1152, 2560, 192, (128, 256)), (2048, 1280, 8192, (256, 256)),
+          (4096, 1280, 128, (256, 256))]
 
 
 @pytest.mark.parametrize("opt", [o for o in OPTIMIZERS if o != "sgd"])

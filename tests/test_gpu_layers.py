@@ -164,3 +164,25 @@ def test_int8_layers_with_long_token_runs_equal_per_layer_calls(Ts):
     for i, (L, R) in enumerate(zip(layers, ref)):
         for k in ("w", "m", "v", "q"):
             assert _same(L[k], R[k]), f"layer {i} {shapes[i]}: {k} differs"
+
+
+@pytest.mark.parametrize("state", ["fp32", "int8"])
+def test_grouped_launch_with_a_split_tail_equals_per_layer_calls(state):
+    """Two 2048 x 1280 layers: 40 pair tiles each, one wave on its own; together 80 tiles, so the
+    grouped launch runs its last 4 as half tiles.  The sums do not depend on the tile shape, so
+    every byte still equals the per-layer calls'."""
+    hp = default_hparams("adamw", lr=1e-3)
+    shapes = [(2048, 1280, 320), (2048, 1280, 192)]
+    layers = _states("adamw", shapes, state, seed=77)
+    ref = _clone(layers)
+    before = fg.launch_count()
+    fg.fused_dw_step_layers([(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], L["seed"]) for L in layers], "adamw",
+                            hp, 2)
+    assert fg.launch_count() - before == 1
+    for L in ref:
+        fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], "adamw", hp, 2, seed=L["seed"])
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    for i, (L, R) in enumerate(zip(layers, ref)):
+        for k in ("w", "m", "v", "q"):
+            assert _same(L[k], R[k]), f"layer {i}: {k} differs"

@@ -36,7 +36,7 @@ def _layer(d_out, d_in, T, opt, seed=0, dy_std=1e-3, m_init="absnormal:1e-4", v_
 # ---------------------------------------------------------------------------- weight gradient
 
 @pytest.mark.parametrize("d_out, d_in, T", [(128, 128, 64), (512, 256, 256), (384, 640, 192), PAIR + (320,),
-                                            WIDE + (128,)])
+                                            WIDE + (128,), PAIR_MANY + (128,)])
 def test_dw_gemm_matches_oracle(d_out, d_in, T):
     dy = normal_bf16((T, d_out), 1e-2, seed=d_out + T)
     x = normal_bf16((T, d_in), 1.0, seed=d_in + 7 * T)
@@ -139,7 +139,7 @@ def test_tiny_workload_three_steps():
 
 # every tile kernel: a CTA pair on 256 x 256, one CTA on 128 x 256, one CTA on 128 x 128 (a layer
 # whose few pair tiles would leave most SMs idle), one CTA on 128 x 64 (small layers)
-SHAPES = [PAIR, WIDE, MID, SMALL, FEW_PAIRS]
+SHAPES = [PAIR, PAIR_MANY, WIDE, MID, SMALL, FEW_PAIRS]
 
 
 @pytest.mark.parametrize("opt, d_out, d_in", [(o,) + PAIR for o in OPTIMIZERS] + [(o,) + WIDE for o in OPTIMIZERS]
@@ -166,7 +166,8 @@ def test_fused_matches_oracle_every_optimizer(opt, d_out, d_in):
 
 
 @pytest.mark.parametrize("opt, d_out, d_in", [(o, 256, 384) for o in OPTIMIZERS if o != "sgd"]
-                         + [(o,) + PAIR for o in OPTIMIZERS if o != "sgd"] + [("adamw",) + WIDE, ("lion", 256, 768)])
+                         + [(o,) + PAIR for o in OPTIMIZERS if o != "sgd"] + [("adamw",) + WIDE, ("lion", 256, 768)]
+                         + [(o,) + PAIR_MANY for o in ("adamw", "lion", "adagrad")])
 def test_fused_int8_matches_oracle(opt, d_out, d_in):
     dy, x, w, _, _ = _layer(d_out, d_in, 128, opt, seed=4)
     mq, ms, vq, vs = _int8_state(w.shape, 9)
@@ -188,13 +189,14 @@ def test_fused_int8_matches_oracle(opt, d_out, d_in):
         assert_moments(q[n64:], ref["v_scales"].ravel(), "v scales")
 
 
-@pytest.mark.parametrize("opt, T", [("adamw", 8192), ("lion", 6144), ("rmsprop", 4096)])
-def test_fused_int8_long_token_runs_match_oracle(opt, T):
+@pytest.mark.parametrize("opt, T, shape", [("adamw", 8192, PAIR), ("lion", 6144, PAIR), ("rmsprop", 4096, PAIR),
+                                          ("sgd_momentum", 8192, PAIR_MANY)])
+def test_fused_int8_long_token_runs_match_oracle(opt, T, shape):
     """INT8 states on CTA pairs over long token runs: from 6144 tokens on the pair kernel runs its
     8-warp epilogue (two 64-column blocks per warp, the next row's inputs loaded while a row
-    updates); at 4096 the 16-warp one.  Codes and scales against the oracle with the summation
-    allowance of T tokens."""
-    d_out, d_in = PAIR
+    updates); at 4096 the 16-warp one.  4096 x 1280 ends on half tiles (one block per warp).
+    Codes and scales against the oracle with the summation allowance of T tokens."""
+    d_out, d_in = shape
     assert fg.launch_shape(d_out, d_in, T)["cluster"] == 2
     dy, x, w, _, _ = _layer(d_out, d_in, T, opt, seed=44)
     mq, ms, vq, vs = _int8_state(w.shape, 19)
@@ -243,7 +245,8 @@ def test_fused_equals_unfused_bitwise(opt, d_out, d_in):
 @pytest.mark.parametrize("opt, d_out, d_in", [("adamw",) + PAIR, ("lion",) + WIDE, ("adagrad",) + PAIR_MANY])
 def test_long_token_runs(opt, d_out, d_in):
     """T = 8192 (the coverage and Qwen3-14B workloads' token count) on CTA pairs and on 128 x 256
-    tiles; 4096 x 1280 has 80 pair tiles, more than the resident pairs."""
+    tiles; 4096 x 1280 has 80 pair tiles, more than the 76 resident pairs, and runs its last 4 as
+    half tiles."""
     T = 8192
     got = fg.launch_shape(d_out, d_in, T)
     assert (got["tile_rows"], got["tile_cols"], got["cluster"]) == TILE[(d_out, d_in)]

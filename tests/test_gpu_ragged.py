@@ -55,10 +55,11 @@ def _layer(d_out, d_in, T, opt, seed):
 
 # (d_out, d_in, T, tile): 128 x 64 with ragged rows, columns (d_in not a multiple of 16) and
 # tokens; a CTA pair whose last row tile leaves one CTA wholly outside the layer (54 pair tiles);
-# 128 x 256 with ragged columns (115 tiles); 128 x 128 with ragged rows and columns (110 tiles);
-# an 8 x 8 layer with one token
-CASES = [(200, 136, 100, (128, 64, 1)), (2056, 1288, 70, (256, 256, 2)), (2944, 1032, 64, (128, 256, 1)),
-         (1288, 1272, 90, (128, 128, 1)), (8, 8, 1, (128, 64, 1))]
+# the same with 102 pair tiles, whose last 26 run as half tiles (the right half of the last tile
+# column lies wholly past d_in); 128 x 256 with ragged columns (115 tiles); 128 x 128 with ragged
+# rows and columns (110 tiles); an 8 x 8 layer with one token
+CASES = [(200, 136, 100, (128, 64, 1)), (2056, 1288, 70, (256, 256, 2)), (4104, 1288, 70, (256, 256, 2)),
+         (2944, 1032, 64, (128, 256, 1)), (1288, 1272, 90, (128, 128, 1)), (8, 8, 1, (128, 64, 1))]
 
 
 @pytest.mark.parametrize("d_out, d_in, T, tile", CASES)
@@ -91,7 +92,7 @@ def test_fused_fp32_states_on_ragged_layers(opt, d_out, d_in, T, tile):
             assert _tail_intact(flat, old.numel())
 
 
-@pytest.mark.parametrize("d_out, d_in, T", [(200, 136, 100), (2056, 1288, 70)])
+@pytest.mark.parametrize("d_out, d_in, T", [(200, 136, 100), (2056, 1288, 70), (4104, 1288, 70)])
 def test_fused_bf16_states_on_ragged_layers(d_out, d_in, T):
     dy, x, w, m, v = _layer(d_out, d_in, T, "adamw", seed=5)
     m, v = m.to(torch.bfloat16), v.to(torch.bfloat16)

@@ -35,3 +35,17 @@ def test_groups_of_rows_sweep_one_column_at_a_time(report):
 def test_groups_of_columns_sweep_one_row_at_a_time(report):
     # the same grid in groups of 3 columns: tiles 0..2 are columns 0..2 of row 0
     assert report["cols3"] == ["0:0", "0:1", "2:1", "2:2", "10:1", "10:2", "11:0", "19:3"]
+
+
+def test_split_tail_covers_every_tile_and_shortens_the_last_wave(report):
+    """Tiles from split_tail_from on run as two 256 x 128 halves: every tile is covered once whole
+    or by both halves, and the busiest pair's work never grows and shrinks whenever a tail splits
+    (checked for 1..400 tiles over 1..100 pairs)."""
+    assert report["split_failures"] == ["0"]
+
+
+def test_split_tail_points_on_76_pairs(report):
+    # 256 tiles (4096^2): 3 whole waves, the 28 left split into 56 halves; 80 tiles (4096 x 1280):
+    # 4 left; 896 (a Llama MLP layer): 60 left, 120 halves would not fit one round, no split;
+    # 400 (Qwen3-14B q/o): 20 left; 76 and 152: full waves; 40: one wave; 1360: 68 left, no split
+    assert report["split_from"] == ["228", "76", "896", "380", "76", "40", "1360", "152"]
