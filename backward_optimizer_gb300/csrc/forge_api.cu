@@ -272,40 +272,30 @@ uint64_t acc_wait_limit(uint64_t base_ns, int64_t k_blocks) {
 using TileFn = cudaError_t (*)(const forge::TileLaunch&);
 using OptFn = cudaError_t (*)(const forge::OptArgs&, int, cudaStream_t);
 
-// INT8 states on a CTA pair with bf16 operands take the 8-warp epilogue (5 operand stages instead
-// of 3) from this many tokens on: there the mainloop, not the epilogue, sets the pace.  Same-box
-// A/B on 4096^2 layers: 16 warps 0.101 / 0.146 ms at T = 2048 / 4096 against 0.166 / 0.183 ms;
-// 8 warps 0.223 / 0.379 ms at T = 8192 / 16384 against 0.259 / 0.475 ms; even at T = 6144.
-constexpr int64_t kInt8DeepMinTokens = 6144;
-
 template <int OPT, int BN, int CL, int OPS, int G = 1>
-TileFn tile_fn_state(int state, bool deep) {
+TileFn tile_fn_state(int state) {
     using namespace forge;
     if (state == FORGE_STATE_INT8_B64) {
         if constexpr (BN == 64) return nullptr;  // INT8 blocks need 64 columns per epilogue warp
-        else if constexpr (BN == 256 && CL == 2 && OPS == kOpsBF16) {
-            return deep ? launch_tile<OPT, kEpiOptINT8Deep, BN, CL, OPS, G> : launch_tile<OPT, kEpiOptINT8, BN, CL, OPS, G>;
-        } else {
-            return launch_tile<OPT, kEpiOptINT8, BN, CL, OPS, G>;
-        }
+        else return launch_tile<OPT, kEpiOptINT8, BN, CL, OPS, G>;
     }
     if (state == FORGE_STATE_BF16) return launch_tile<OPT, kEpiOptBF16, BN, CL, OPS, G>;
     return launch_tile<OPT, kEpiOptFP32, BN, CL, OPS, G>;
 }
 
 template <int BN, int CL, int OPS, int G = 1>
-TileFn tile_fn_v(forge_opt_kind k, int state, bool deep = false) {
+TileFn tile_fn_v(forge_opt_kind k, int state) {
     using namespace forge;
     switch (k) {
-        case FORGE_ADAMW: return tile_fn_state<kAdamW, BN, CL, OPS, G>(state, deep);
-        case FORGE_NADAM: return tile_fn_state<kNAdam, BN, CL, OPS, G>(state, deep);
-        case FORGE_RADAM: return tile_fn_state<kRAdam, BN, CL, OPS, G>(state, deep);
-        case FORGE_LION: return tile_fn_state<kLion, BN, CL, OPS, G>(state, deep);
-        case FORGE_RMSPROP: return tile_fn_state<kRMSprop, BN, CL, OPS, G>(state, deep);
-        case FORGE_ADAGRAD: return tile_fn_state<kAdaGrad, BN, CL, OPS, G>(state, deep);
+        case FORGE_ADAMW: return tile_fn_state<kAdamW, BN, CL, OPS, G>(state);
+        case FORGE_NADAM: return tile_fn_state<kNAdam, BN, CL, OPS, G>(state);
+        case FORGE_RADAM: return tile_fn_state<kRAdam, BN, CL, OPS, G>(state);
+        case FORGE_LION: return tile_fn_state<kLion, BN, CL, OPS, G>(state);
+        case FORGE_RMSPROP: return tile_fn_state<kRMSprop, BN, CL, OPS, G>(state);
+        case FORGE_ADAGRAD: return tile_fn_state<kAdaGrad, BN, CL, OPS, G>(state);
         case FORGE_SGD:
             return state == FORGE_STATE_FP32 ? launch_tile<kSGD, kEpiOptFP32, BN, CL, OPS, G> : nullptr;
-        case FORGE_SGD_MOMENTUM: return tile_fn_state<kSGDMomentum, BN, CL, OPS, G>(state, deep);
+        case FORGE_SGD_MOMENTUM: return tile_fn_state<kSGDMomentum, BN, CL, OPS, G>(state);
     }
     return nullptr;
 }
@@ -351,7 +341,7 @@ TileShape pick_dx_shape(int64_t T, int64_t /*d_out*/, int64_t d_in, int num_sms)
 }
 
 template <int OPS>
-TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t, bool deep) {
+TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t) {
     using namespace forge;
     if (epi == kEpiDX) {
         if constexpr (OPS != kOpsBF16) return nullptr;
@@ -367,7 +357,7 @@ TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t, bool deep)
         }
         return t.bn == 256 ? launch_tile<0, kEpiStoreGrad, 256, 1, OPS, 1> : launch_tile<0, kEpiStoreGrad, 128, 1, OPS, 1>;
     }
-    if (t.cg == 2) return tile_fn_v<256, 2, OPS>(k, state, deep);
+    if (t.cg == 2) return tile_fn_v<256, 2, OPS>(k, state);
     if (t.bn == 64) {
         if constexpr (OPS != kOpsBF16) return nullptr;
         else return state == FORGE_STATE_INT8_B64 ? nullptr : tile_fn_v<64, 1, OPS>(k, state);
@@ -375,11 +365,8 @@ TileFn tile_fn_ops(forge_opt_kind k, int state, int epi, TileShape t, bool deep)
     return t.bn == 256 ? tile_fn_v<256, 1, OPS>(k, state) : tile_fn_v<128, 1, OPS>(k, state);
 }
 
-// T: the call's token count (it picks the INT8 pair epilogue)
-TileFn tile_fn(forge_opt_kind k, int state, int epi, TileShape t, bool e4m3, int64_t T) {
-    const bool deep = T >= kInt8DeepMinTokens;
-    return e4m3 ? tile_fn_ops<forge::kOpsE4M3>(k, state, epi, t, deep)
-                : tile_fn_ops<forge::kOpsBF16>(k, state, epi, t, deep);
+TileFn tile_fn(forge_opt_kind k, int state, int epi, TileShape t, bool e4m3) {
+    return e4m3 ? tile_fn_ops<forge::kOpsE4M3>(k, state, epi, t) : tile_fn_ops<forge::kOpsBF16>(k, state, epi, t);
 }
 
 template <int OPT>
@@ -485,7 +472,7 @@ forge_status run_tile(const void* dY, const void* X, float* dW, void* W, void* m
     g.tile_start[1] = g.layer[0].num_tiles;
     forge::TileLaunch l{&g, g.tile_start[1], dev.num_sms, stream};
     // epi is kEpiStoreGrad (dW to memory) or kEpiOptFP32 (the fused step, whose epilogue follows the state dtype)
-    TileFn fn = tile_fn(k, shape->state, epi, ts, e4m3, shape->T);
+    TileFn fn = tile_fn(k, shape->state, epi, ts, e4m3);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(l));
@@ -521,7 +508,7 @@ forge_status run_dx(const void* dY, const void* W, void* dX, const forge_shape* 
     g.tile_start[0] = 0;
     g.tile_start[1] = a.num_tiles;
     forge::TileLaunch l{&g, a.num_tiles, dev.num_sms, stream};
-    TileFn fn = tile_fn(FORGE_SGD, FORGE_STATE_FP32, forge::kEpiDX, ts, false, shape->T);
+    TileFn fn = tile_fn(FORGE_SGD, FORGE_STATE_FP32, forge::kEpiDX, ts, false);
     if (fn == nullptr) return FORGE_ERR_UNSUPPORTED;
     g_launches.fetch_add(1);
     return cuda_status(fn(l));
@@ -754,15 +741,9 @@ forge_status forge_fused_dw_step_layers(const forge_layer* layers, int32_t n_lay
             g.tile_start[g.n + 1] = g.tile_start[g.n] + g.layer[g.n].num_tiles;
             ++g.n;
         }
-        // the 8-warp INT8 epilogue when every layer of the group has a long token run
-        int64_t min_T = layers[next - g.n].T;
-        for (int32_t i = next - g.n; i < next; ++i) min_T = layers[i].T < min_T ? layers[i].T : min_T;
-        TileFn gfn = min_T >= kInt8DeepMinTokens
-                         ? tile_fn_v<256, 2, forge::kOpsBF16, forge::kMaxGroup>(opt_kind, state, true)
-                         : fn;
         forge::TileLaunch l{&g, g.tile_start[g.n], dev->num_sms, stream};
         g_launches.fetch_add(1);
-        st = cuda_status(gfn(l));
+        st = cuda_status(fn(l));
         if (st != FORGE_OK) return st;
     }
     return FORGE_OK;

@@ -121,13 +121,9 @@ cudaError_t launch_opt(const OptArgs& a, int grid, cudaStream_t stream) {
     FORGE_INSTANTIATE_GROUP(OPT, forge::kEpiOptFP32) \
     template cudaError_t forge::launch_opt<OPT, 0>(const forge::OptArgs&, int, cudaStream_t);
 
-// INT8 states add the 8-warp pair epilogue for long token runs (bf16 operands, single layers and
-// groups).
-#define FORGE_INSTANTIATE_OPT_INT8(OPT)                                                                           \
-    FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptINT8)                                                            \
-    FORGE_INSTANTIATE_GROUP(OPT, forge::kEpiOptINT8)                                                            \
-    template cudaError_t forge::launch_tile<OPT, forge::kEpiOptINT8Deep, 256, 2, forge::kOpsBF16, 1>(const forge::TileLaunch&); \
-    FORGE_INSTANTIATE_GROUP(OPT, forge::kEpiOptINT8Deep)                                                        \
+#define FORGE_INSTANTIATE_OPT_INT8(OPT)               \
+    FORGE_INSTANTIATE_TILES(OPT, forge::kEpiOptINT8) \
+    FORGE_INSTANTIATE_GROUP(OPT, forge::kEpiOptINT8) \
     template cudaError_t forge::launch_opt<OPT, 1>(const forge::OptArgs&, int, cudaStream_t);
 
 #define FORGE_INSTANTIATE_OPT_BF16(OPT)               \

@@ -43,12 +43,7 @@ constexpr int kBK = 64;          // tokens per pipeline stage = 128 bytes of one
 constexpr int kUmmaK = 16;       // K of one kind::f16 MMA
 constexpr int kStatusTimeout = 6;  // FORGE_ERR_TIMEOUT
 
-// kEpiOptINT8Deep: INT8 states on a CTA pair with 8 epilogue warps instead of 16.  Half the
-// transpose strips leave shared memory for 5 operand stages instead of 3, which a long token run,
-// where the mainloop rather than the INT8 epilogue sets the pace, needs to keep the tensor core fed.
-enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3, kEpiOptBF16 = 4,
-                     kEpiOptINT8Deep = 5 };
-__host__ __device__ constexpr bool int8_epi(int epi) { return epi == kEpiOptINT8 || epi == kEpiOptINT8Deep; }
+enum EpiKind : int { kEpiStoreGrad = 0, kEpiOptFP32 = 1, kEpiOptINT8 = 2, kEpiDX = 3, kEpiOptBF16 = 4 };
 
 // Operand formats.  Either way a stage row is 128 bytes (the swizzle span) and a stage of one
 // operand is 16 KiB per 128 MN rows: 64 tokens of bf16, or 128 tokens of E4M3, whose products the
@@ -67,7 +62,7 @@ template <int BN, int CG, int EPI, int OPS = kOpsBF16>
 struct TileCfg {
     // 64-column tiles (one X box per stage, N = 64 MMAs) serve small layers with bf16 operands and
     // epilogues that work on 32-column runs; E4M3 rows hold 128 elements, INT8 blocks 64 per warp
-    static_assert(BN == 128 || BN == 256 || (BN == 64 && CG == 1 && OPS == kOpsBF16 && !int8_epi(EPI)),
+    static_assert(BN == 128 || BN == 256 || (BN == 64 && CG == 1 && OPS == kOpsBF16 && EPI != kEpiOptINT8),
                   "tile width");
     static_assert(CG == 1 || CG == 2, "CTA group");
     static constexpr int kBLoad = BN / CG;         // X columns staged by this CTA
@@ -77,8 +72,8 @@ struct TileCfg {
     static constexpr int kTmemCols = 2 * BN;       // double-buffered FP32 accumulator (128 lanes x BN)
     // epilogue warps: two per TMEM lane quarter, each owning half the tile's columns.  A CTA pair
     // runs four per quarter, one 64-column block each, where the epilogue rather than the
-    // operand stream sets the pace: the INT8-state epilogue (kEpiOptINT8; not kEpiOptINT8Deep),
-    // whose dependent arithmetic needs more warps per scheduler to keep issuing, and the
+    // operand stream sets the pace: the INT8-state epilogue, whose dependent arithmetic needs more
+    // warps per scheduler to keep issuing, and the
     // bfloat16-state epilogue behind the E4M3 mainloop, which is half as long as the bf16 one.
     // Binary32 states behind the E4M3 mainloop keep two warps per quarter: their W/m/v stream
     // needs the four row groups each such warp keeps in flight more than it needs more warps
@@ -86,9 +81,10 @@ struct TileCfg {
     static constexpr bool kWideEpi = CG == 2 && (EPI == kEpiOptINT8 || (OPS == kOpsE4M3 && EPI == kEpiOptBF16));
     static constexpr int kEpiWarps = kWideEpi ? 16 : 8;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
-    // one warp's 32 x 32 FP32 transpose strip; the INT8 epilogue stages two (a 64-column block);
-    // the input-gradient epilogue stores rows as they come out of TMEM and needs none
-    static constexpr int kStripBytes = EPI == kEpiDX ? 0 : (int8_epi(EPI) ? 2 : 1) * 32 * 32 * 4;
+    // one warp's 4 KiB transpose strip: 32 x 32 binary32 values, or for the INT8 epilogue 16 rows
+    // of a 64-column block; the input-gradient epilogue stores rows as they come out of TMEM and
+    // needs none
+    static constexpr int kStripBytes = EPI == kEpiDX ? 0 : 32 * 32 * 4;
     static constexpr int kEpiBytes = kEpiWarps * kStripBytes;
     static constexpr int kBarrierBytes = 256;
     static constexpr int kMaxSmem = 232448;
@@ -494,11 +490,43 @@ __device__ __forceinline__ void int8_row_load(const TileArgs& a, size_t e, bool 
     }
 }
 
-// The 8 gradient values of strip row r, columns 8 c8 .. 8 c8 + 7 (c8 < 4) of a 32-column strip.
-__device__ __forceinline__ void strip_load_run(const uint8_t* strip, uint32_t r, uint32_t c8, uint32_t (&out)[8]) {
-    const uint32_t base = smem_addr(strip) + r * 128u;
+// The INT8 epilogue's strip: 16 rows x 64 columns of the binary32 gradient, the rows 16 hh ..
+// 16 hh + 15 of a warp's 32 (one 64-column block), 256 bytes a row, its 16-byte chunk c at chunk
+// position c ^ (r mod 8).  Half the rows at a time keep the strip at 4 KiB a warp, so 16 epilogue
+// warps leave shared memory for 5 operand stages.  The TMEM reads are warp-wide; only the lanes of
+// rows 16 hh .. 16 hh + 15 store (16 lanes x 16 bytes: two wavefronts, no bank conflict).
+template <bool SCALE>
+__device__ __forceinline__ void int8_strip_store(uint32_t taddr, uint8_t* strip, const TileArgs& a, int row0,
+                                                 int col0, int hh) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t r = lane & 15u;  // strip row, for the lanes that store
+    const bool mine = (lane >> 4) == static_cast<uint32_t>(hh);
+    const uint32_t base = smem_addr(strip) + r * 256u;
+    __syncwarp();  // earlier reads of the strip are complete
+    // one 32-column read in registers at a time (unrolled, the second read is hoisted above the
+    // first's stores and both stay live)
+#pragma unroll 1
+    for (uint32_t h = 0; h < 2; ++h) {
+        uint32_t g[32];
+        tmem_ld_32x32b_x32(taddr + 32u * h, g);
+        tmem_ld_wait(g);
+        scale_strip<SCALE>(g, a, row0 + static_cast<int>(lane), col0 + 32 * static_cast<int>(h));
+        if (mine) {
 #pragma unroll
-    for (uint32_t h = 0; h < 2; ++h) ld_shared_v4(base + (((2u * c8 + h) ^ (r & 7u)) << 4), &out[4 * h]);
+            for (uint32_t j = 0; j < 8; ++j)
+                st_shared_v4(base + (((8u * h + j) ^ (r & 7u)) << 4), g[4 * j], g[4 * j + 1], g[4 * j + 2],
+                             g[4 * j + 3]);
+        }
+    }
+    __syncwarp();
+}
+
+// The 8 gradient values of INT8 strip row r (< 16), columns 8 q .. 8 q + 7 (q < 8).  The 32 lanes
+// of a warp read rows rsub + 4k' (rsub < 4) and runs q < 8: four wavefronts, no bank conflict.
+__device__ __forceinline__ void int8_strip_load_run(const uint8_t* strip, uint32_t r, uint32_t q, uint32_t (&out)[8]) {
+    const uint32_t base = smem_addr(strip) + r * 256u;
+#pragma unroll
+    for (uint32_t h = 0; h < 2; ++h) ld_shared_v4(base + (((2u * q + h) ^ (r & 7u)) << 4), &out[4 * h]);
 }
 
 template <int OPT>
@@ -568,49 +596,61 @@ __device__ __forceinline__ void int8_row_update(const TileArgs& a, const OptScal
 
 // width: columns of this warp's part (a multiple of 64).  krange: the row iterations k (rows
 // rsub + 4k) this warp updates, first | (end << 4): all eight, or on a split tail tile, where the
-// 16-warp epilogue (no PREFETCH) gives each 64-column block to two warps, k < 4 or k >= 4.  Each
-// warp still stages the block's whole gradient strips.
+// 16-warp epilogue (no PREFETCH) gives each 64-column block to two warps, k < 4 or k >= 4.  Rows
+// are staged in two halves (int8_strip_store): iterations 0..3, then 4..7.
 template <int OPT, int WIDTH, bool SCALE, bool PREFETCH>
 __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, const OptScalars& s, int row0, int col0,
                                              uint32_t taddr, int width, uint8_t* strip, int krange) {
     static_assert(WIDTH % 64 == 0, "whole quantisation blocks");
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t q = lane & 7u, rsub = lane >> 3;  // column run (8 columns) and first row of this lane
-    const uint8_t* half = strip + (q >> 2) * 4096;    // the 32-column strip holding the run
     const int row = row0 + static_cast<int>(rsub);
 #pragma unroll 1
     for (int c = 0; c < width; c += 64) {
         // d_in is a multiple of 64, so a 64-column block lies wholly inside or outside the layer:
         // the same for every lane of the warp
         if (col0 + c >= a.d_in) break;
-        strip_store<SCALE>(taddr + c, strip, a, row0 + static_cast<int>(lane), col0 + c);
-        strip_store<SCALE>(taddr + c + 32, strip + 4096, a, row0 + static_cast<int>(lane), col0 + c + 32);
-        const size_t e0 = static_cast<size_t>(row) * a.d_in + col0 + c + 8 * q;
-        const size_t row_step = static_cast<size_t>(4) * a.d_in;
         if constexpr (PREFETCH) {
-            // the next row's inputs load while this one updates
+            const size_t e0 = static_cast<size_t>(row) * a.d_in + col0 + c + 8 * q;
+            const size_t row_step = static_cast<size_t>(4) * a.d_in;
+            // the next row's inputs load while this one updates (across the two halves too)
             Int8RowIn<OPT> in[2];
             int8_row_load<OPT>(a, e0, row < a.d_out, in[0]);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (k < 7) int8_row_load<OPT>(a, e0 + (k + 1) * row_step, row + 4 * (k + 1) < a.d_out, in[(k + 1) & 1]);
-                uint32_t g[8];
-                strip_load_run(half, rsub + 4u * k, q & 3u, g);
-                int8_row_update<OPT>(a, s, e0 + k * row_step, row + 4 * k < a.d_out, g, in[k & 1]);
+            for (int hh = 0; hh < 2; ++hh) {
+                int8_strip_store<SCALE>(taddr + c, strip, a, row0, col0 + c, hh);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int k = 4 * hh + kk;
+                    if (k < 7)
+                        int8_row_load<OPT>(a, e0 + (k + 1) * row_step, row + 4 * (k + 1) < a.d_out, in[(k + 1) & 1]);
+                    uint32_t g[8];
+                    int8_strip_load_run(strip, rsub + 4u * kk, q, g);
+                    int8_row_update<OPT>(a, s, e0 + k * row_step, row + 4 * k < a.d_out, g, in[k & 1]);
+                }
             }
         } else {
             // enough warps per scheduler to cover the load latency without a second row in flight
 #pragma unroll 1
-            for (int k = krange & 15; k < (krange >> 4); ++k) {
-                Int8RowIn<OPT> in;
-                int8_row_load<OPT>(a, e0 + k * row_step, row + 4 * k < a.d_out, in);
-                uint32_t g[8];
-                strip_load_run(half, rsub + 4u * k, q & 3u, g);
-                int8_row_update<OPT>(a, s, e0 + k * row_step, row + 4 * k < a.d_out, g, in);
+            for (int hh = (krange & 15) >> 2; hh < ((krange >> 4) + 3) >> 2; ++hh) {
+                int8_strip_store<SCALE>(taddr + c, strip, a, row0, col0 + c, hh);
+                // this half's first row of the lane, and its element index
+                const int rh = row + 16 * hh;
+                const size_t eh = static_cast<size_t>(rh) * a.d_in + col0 + c + 8 * q;
+#pragma unroll 1
+                for (int kk = 0; kk < 4; ++kk) {
+                    const size_t e = eh + static_cast<size_t>(4 * kk) * a.d_in;
+                    const bool ok = rh + 4 * kk < a.d_out;
+                    Int8RowIn<OPT> in;
+                    int8_row_load<OPT>(a, e, ok, in);
+                    uint32_t g[8];
+                    int8_strip_load_run(strip, rsub + 4u * kk, q, g);
+                    int8_row_update<OPT>(a, s, e, ok, g, in);
+                }
             }
         }
-        __syncwarp();  // every lane has read the strips before the next block overwrites them
     }
+    __syncwarp();  // every lane has read the strip before the warp's next tile overwrites it
 }
 
 // ---------------------------------------------------------------- the kernel

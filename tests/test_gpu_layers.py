@@ -145,10 +145,9 @@ def test_withheld_stage_in_a_grouped_launch():
 
 @pytest.mark.parametrize("Ts", [(8192, 6144), (8192, 4096)])
 def test_int8_layers_with_long_token_runs_equal_per_layer_calls(Ts):
-    """INT8 states on CTA pairs take the 8-warp epilogue from 6144 tokens on, in a single-layer
-    call and in a group whose layers all have that many; a group with a shorter layer keeps the
-    16-warp one.  The two epilogues do the same per-element arithmetic, so the grouped call still
-    equals the per-layer calls bit for bit either way."""
+    """INT8 states over long token runs, grouped and per layer: the epilogue stages each block's
+    rows in two halves between the operand stages; the grouped call still equals the per-layer
+    calls bit for bit."""
     hp = default_hparams("adamw", lr=1e-3)
     shapes = [(2048, 1280, Ts[0]), (1024, 1536, Ts[1])]
     layers = _states("adamw", shapes, "int8", seed=61)

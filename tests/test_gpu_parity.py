@@ -192,9 +192,8 @@ def test_fused_int8_matches_oracle(opt, d_out, d_in):
 @pytest.mark.parametrize("opt, T, shape", [("adamw", 8192, PAIR), ("lion", 6144, PAIR), ("rmsprop", 4096, PAIR),
                                           ("sgd_momentum", 8192, PAIR_MANY)])
 def test_fused_int8_long_token_runs_match_oracle(opt, T, shape):
-    """INT8 states on CTA pairs over long token runs: from 6144 tokens on the pair kernel runs its
-    8-warp epilogue (two 64-column blocks per warp, the next row's inputs loaded while a row
-    updates); at 4096 the 16-warp one.  4096 x 1280 ends on half tiles (one block per warp).
+    """INT8 states on CTA pairs over long token runs (16 epilogue warps, rows staged in two
+    halves, 5 operand stages); 4096 x 1280 ends on half tiles, where two warps share each block.
     Codes and scales against the oracle with the summation allowance of T tokens."""
     d_out, d_in = shape
     assert fg.launch_shape(d_out, d_in, T)["cluster"] == 2
