@@ -510,7 +510,10 @@ __device__ __forceinline__ void int8_strip_store(uint32_t taddr, uint8_t* strip,
         uint32_t g[32];
         tmem_ld_32x32b_x32(taddr + 32u * h, g);
         tmem_ld_wait(g);
-        scale_strip<SCALE>(g, a, row0 + static_cast<int>(lane), col0 + 32 * static_cast<int>(h));
+        // per-channel scales here; a per-tensor scale multiplies each lane's 8 values as it reads
+        // them (int8_scale_run), once per element rather than once per half
+        if (SCALE && a.row_scales != nullptr)
+            scale_strip<SCALE>(g, a, row0 + static_cast<int>(lane), col0 + 32 * static_cast<int>(h));
         if (mine) {
 #pragma unroll
             for (uint32_t j = 0; j < 8; ++j)
@@ -519,6 +522,17 @@ __device__ __forceinline__ void int8_strip_store(uint32_t taddr, uint8_t* strip,
         }
     }
     __syncwarp();
+}
+
+// A per-tensor gradient scale (E4M3 operands), applied to the values a lane reads from the strip.
+template <bool SCALE>
+__device__ __forceinline__ void int8_scale_run(const TileArgs& a, uint32_t (&g)[8]) {
+    if constexpr (SCALE) {
+        if (a.row_scales == nullptr) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[j] = __float_as_uint(__fmul_rn(__uint_as_float(g[j]), a.g_scale));
+        }
+    }
 }
 
 // The 8 gradient values of INT8 strip row r (< 16), columns 8 q .. 8 q + 7 (q < 8).  The 32 lanes
@@ -626,6 +640,7 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, const OptScalars
                         int8_row_load<OPT>(a, e0 + (k + 1) * row_step, row + 4 * (k + 1) < a.d_out, in[(k + 1) & 1]);
                     uint32_t g[8];
                     int8_strip_load_run(strip, rsub + 4u * kk, q, g);
+                    int8_scale_run<SCALE>(a, g);
                     int8_row_update<OPT>(a, s, e0 + k * row_step, row + 4 * k < a.d_out, g, in[k & 1]);
                 }
             }
@@ -645,6 +660,7 @@ __device__ __forceinline__ void epi_opt_int8(const TileArgs& a, const OptScalars
                     int8_row_load<OPT>(a, e, ok, in);
                     uint32_t g[8];
                     int8_strip_load_run(strip, rsub + 4u * kk, q, g);
+                    int8_scale_run<SCALE>(a, g);
                     int8_row_update<OPT>(a, s, e, ok, g, in);
                 }
             }

@@ -112,10 +112,11 @@ def test_fused_bf16_states_on_ragged_layers(d_out, d_in, T):
         assert _tail_intact(flat, t.numel())
 
 
-@pytest.mark.parametrize("d_out, d_in, T", [(200, 320, 100), (2056, 1088, 70)])
+@pytest.mark.parametrize("d_out, d_in, T", [(200, 320, 100), (2056, 1088, 70), (4104, 1088, 70)])
 def test_fused_int8_states_on_ragged_layers(d_out, d_in, T):
     """d_in a multiple of 64 (1088 = 17 blocks, a ragged 256-column tile of a CTA pair), ragged rows
-    and tokens."""
+    and tokens; 4104 x 1088 has 85 pair tiles, whose last 9 run as half tiles (two warps per block;
+    the right half of the last tile column lies wholly past d_in)."""
     dy, x, w, _, _ = _layer(d_out, d_in, T, "adamw", seed=7)
     rng = np.random.default_rng(7)
     m32 = (f32(moment_init("absnormal:1e-4", w.shape, 8)) * np.sign(rng.standard_normal(w.shape))).astype(np.float32)
@@ -143,7 +144,7 @@ def test_fused_int8_states_on_ragged_layers(d_out, d_in, T):
         assert _tail_intact(flat, n)
 
 
-@pytest.mark.parametrize("d_out, d_in, T", [(200, 136, 100), (2056, 1288, 70)])
+@pytest.mark.parametrize("d_out, d_in, T", [(200, 136, 100), (2056, 1288, 70), (4104, 1288, 70)])
 def test_fused_equals_unfused_on_ragged_layers(d_out, d_in, T):
     """The two-phase kernel's last warp is partly past the end (d_out d_in / 8 not a multiple of 32)."""
     dy, x, w, m, v = _layer(d_out, d_in, T, "adamw", seed=9)
@@ -165,9 +166,10 @@ def test_fused_equals_unfused_on_ragged_layers(d_out, d_in, T):
     assert_moments(dW.cpu().numpy(), ostep.dw(bits(dy), bits(x)), "dW", rtol=moment_rtol(T))
 
 
-@pytest.mark.parametrize("T, d_out, d_in", [(100, 200, 136), (70, 1096, 1288), (300, 8, 264)])
+@pytest.mark.parametrize("T, d_out, d_in", [(100, 200, 136), (70, 1096, 1288), (300, 8, 264), (4104, 520, 1288)])
 def test_dx_on_ragged_layers(T, d_out, d_in):
-    """dX with a ragged reduction (d_out), ragged columns (d_in not a multiple of 16: 16-byte stores)."""
+    """dX with a ragged reduction (d_out), ragged columns (d_in not a multiple of 16: 16-byte stores);
+    4104 tokens x 1288 columns make 102 pair tiles, whose last 26 run as half tiles."""
     dy = torch.randn(T, d_out, generator=torch.Generator().manual_seed(T)).mul(1e-3).to(torch.bfloat16)
     w = torch.randn(d_out, d_in, generator=torch.Generator().manual_seed(d_in)).mul(2e-2).to(torch.bfloat16)
     flat = torch.full((T * d_in + GUARD,), _pattern(torch.bfloat16), dtype=torch.bfloat16, device="cuda")
