@@ -185,3 +185,23 @@ def test_grouped_launch_with_a_split_tail_equals_per_layer_calls(state):
     for i, (L, R) in enumerate(zip(layers, ref)):
         for k in ("w", "m", "v", "q"):
             assert _same(L[k], R[k]), f"layer {i}: {k} differs"
+
+
+def test_split_tail_across_a_layer_boundary():
+    """1536 x 3328 (78 pair tiles) and 256 x 512 (2): the grouped launch's 80 tiles end on a split
+    tail of 4 tiles, two from each layer, so half tiles of both layers run in the last wave."""
+    hp = default_hparams("adamw", lr=1e-3)
+    shapes = [(1536, 3328, 128), (256, 512, 192)]
+    layers = _states("adamw", shapes, "fp32", seed=83)
+    ref = _clone(layers)
+    before = fg.launch_count()
+    fg.fused_dw_step_layers([(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], L["seed"]) for L in layers], "adamw",
+                            hp, 3)
+    assert fg.launch_count() - before == 1
+    for L in ref:
+        fg.fused_dw_step(L["dy"], L["x"], L["w"], L["m"], L["v"], L["q"], "adamw", hp, 3, seed=L["seed"])
+    torch.cuda.synchronize()
+    assert fg.sync_status() == 0
+    for i, (L, R) in enumerate(zip(layers, ref)):
+        for k in ("w", "m", "v"):
+            assert _same(L[k], R[k]), f"layer {i}: {k} differs"
