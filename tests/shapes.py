@@ -4,8 +4,10 @@ The fused step prefers a CTA pair on 256 x 256 tiles (d_out and d_in multiples o
 CTA on 128 x 256 (d_in a multiple of 256), else 128 x 128; a layer whose preferred shape would
 occupy at most half the SMs (76) takes 128 x 128 tiles instead, and if those would too, 128 x 64
 tiles (bf16 operands with binary32 or bfloat16 states; INT8 states and E4M3 operands stay on
-128 x 128).  The parity tests name the shape
-they exercise and check it through the launch-shape query, so a change of that rule shows there.
+128 x 128).  With bf16 operands, a pair launch whose last wave would occupy at most half of the 76
+pairs runs that wave's tiles as two 256 x 128 halves each (the query still reports 256 x 256).
+The parity tests name the shape they exercise and check it through the launch-shape query, so a
+change of that rule shows there.
 """
 
 PAIR = (2048, 1280)        # 8 x 5 = 40 pair tiles of 256 x 256: 80 CTAs
