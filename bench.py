@@ -620,6 +620,17 @@ class OracleSample:
             flops += 2 * self.wl.T * r * l.d_in
         return flops, secs
 
+    def whole(self, rows: int) -> bool:
+        """Whether a sample of `rows` rows per layer is the workload's whole step."""
+        return len(self.wl.layers) == len(self.layers) and all(rows >= l.d_out for l, *_ in self.layers)
+
+    def describe(self, rows: int) -> str:
+        """The sample in words: the rows of each sampled layer it covers."""
+        if self.whole(rows):
+            return f"the whole step of {self.wl.name} (every weight row of every layer)"
+        parts = ", ".join(f"{min(rows, l.d_out)} of {l.d_out} rows of {l.name}" for l, *_ in self.layers)
+        return f"the first weight rows of the first {len(self.layers)} layers of {self.wl.name}: {parts}"
+
     def rows_for(self, seconds: float) -> int:
         """Sample size (a multiple of 64 rows, 64 .. 4096) whose step takes about `seconds`."""
         f, s = self.run(64)
@@ -661,8 +672,8 @@ def cpu_baseline(args):
     flops, secs = sample.run(rows)
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
             "blas_threads": blas_threads(),
-            "sample": f"first {rows} weight rows of each of the first 3 layers of {args.workload} "
-                      f"(float64 NumPy oracle, whole step incl. Philox/SR), {secs:.1f} s"}
+            "sample": f"{sample.describe(rows)} (float64 NumPy oracle, whole step incl. Philox/SR), "
+                      f"{secs:.1f} s"}
 
 
 # ------------------------------------------------------------------------------------ main
@@ -716,12 +727,13 @@ def main():
         line = {"impl": "reference", "metric": metric, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": flops_step / (v * 1e12) * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": dict(config, ms_per_step="extrapolated to the full step at the "
-                                                                        "oracle's measured rate"),
+                "data": "synthetic",
+                "config": dict(config, ms_per_step="measured on the whole step" if sample.whole(rows) else
+                               "extrapolated to the full step at the oracle's measured rate"),
                 "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                                  "blas_threads": blas_threads(),
-                                 "sample": f"first {rows} weight rows of each of the first 3 layers per step "
-                                           f"(float64 NumPy oracle, whole step incl. Philox/SR)"},
+                                 "sample": f"{sample.describe(rows)}, per step (float64 NumPy oracle, whole "
+                                           f"step incl. Philox/SR)"},
                 "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "wall_s": time.perf_counter() - t0}
         print(json.dumps(line))

@@ -119,3 +119,14 @@ def test_tensor_peak_follows_the_power_cap():
     assert bench.tensor_peak_for(peaks, None) == (1938.1, "bf16_tflops")
     assert bench.tensor_peak_for({"bf16_tflops": 1900.0}, {"reasons": ["sw_power_cap"]}) == (1900.0, "bf16_tflops")
     assert bench.tensor_peak_for({}, {"reasons": []})[0] == bench.FALLBACK_PEAKS["bf16_tflops"]
+
+
+def test_oracle_sample_says_what_it_covers():
+    """The reference arm's sample names the rows it timed: the whole step for a layer smaller than
+    the sample (nothing extrapolated), else each sampled layer's first rows."""
+    import json
+    r = _run_bench("--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["cpu_baseline"]["sample"].startswith("the whole step of tiny")
+    assert line["config"]["ms_per_step"] == "measured on the whole step"
